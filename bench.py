@@ -1,0 +1,446 @@
+#!/usr/bin/env python3
+"""Benchmark of the MLA paged latent-cache decode step on B300.
+
+One step = one mla_decode_paged call (split-KV attention pass + log-sum-exp
+combine) over the whole batch of the V2-shaped decode workload: 32
+sequences x 4096 cached tokens, 128 heads, rows of 512 latent + 64 rotary
+bfloat16 numbers in 64-token blocks with a shuffled block table, latent
+queries [32, 1, 128, 576].  Inputs are seeded synthetic normal draws.
+
+Prints ONE JSON line (rank 0).  `value` is the algorithmic cache+query bytes
+of all ranks' steps divided by the device time of the timed steps (max over
+ranks), in GB/s.  Other keys: TFLOP/s, tokens/s, the roofline of the
+dominant kernel, an end-to-end figure through the public API with host
+buffers, the oracle timed on the host cores, and the SM clocks sampled
+during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mla|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import mla_inputs as mi  # noqa: E402
+
+METRIC = "MLA decode cache GB/s + TFLOP/s, % of B300 roofline; decode tokens/sec"
+L2_BYTES = 126 * 1024 * 1024
+PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+# --------------------------------------------------------------------------
+# workload arithmetic (algorithmic work, no padding / split / tail waste)
+# --------------------------------------------------------------------------
+
+def algorithmic_work(spec: mi.DecodeSpec, seqlens: np.ndarray):
+    """Bytes the method must read (every visible cache row once + the latent
+    queries) and FLOPs it must do (576-wide score and 512-wide value sum per
+    (query row, visible key))."""
+    D, elt = spec.D, 2
+    L = seqlens.astype(np.int64)
+    cache_bytes = int(L.sum()) * D * elt
+    q_bytes = spec.B * spec.T_q * spec.H * D * elt
+    if spec.causal:
+        vis = sum(int(l) - spec.T_q + t + 1 for l in L for t in range(spec.T_q))
+    else:
+        vis = int(L.sum()) * spec.T_q
+    flops = 2 * spec.H * vis * (D + spec.d_c)
+    out_bytes = spec.B * spec.T_q * spec.H * (spec.d_c + 1) * 4
+    return dict(cache_bytes=cache_bytes, q_bytes=q_bytes, bytes=cache_bytes + q_bytes,
+                flops=flops, out_bytes=out_bytes)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in PEAKS_FALLBACK}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def kernel_source_sha(name: str) -> str:
+    path = os.path.join(ROOT, "head_latent_attention_28_b300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def profiled_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken
+    on the kernel source as it is now (else None)."""
+    path = os.path.join(PROFILE_DIR, f"{os.path.splitext(kernel_file)[0]}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m_sha and m_tr) or m_sha.group(1) != kernel_source_sha(kernel_file):
+        return None
+    return float(m_tr.group(1))
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    REASONS = {  # NVML clocks-event reason bits
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+        0x100: "display_clock_setting"}
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.period, self._stop = period_s, threading.Event()
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # noqa: BLE001
+            self.err = repr(e)
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                bits = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for b, name in self.REASONS.items():
+                    if bits & b and name != "gpu_idle":
+                        self.reasons.add(name)
+            except Exception:  # noqa: BLE001
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.err}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples)}
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; replicas, no data-path collective)
+# --------------------------------------------------------------------------
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE={world}")
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("MLA_BENCH_BACKEND", "nccl")
+        dist.init_process_group(backend)
+        return rank, world, local, dist
+    return 0, 1, local, None
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# oracle timing (CPU baseline / reference arm)
+# --------------------------------------------------------------------------
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads", 0) for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:  # noqa: BLE001
+        pass
+    return os.cpu_count() or 1
+
+
+def time_oracle_sequences(inp, seqs):
+    """Run the fp64 oracle on the given sequences; returns (seconds, bytes)."""
+    import oracle as orc
+    s = inp.spec
+    t0 = time.perf_counter()
+    orc.decode_paged_logical(inp.q_bits, inp.cache_bits, inp.offsets, s.d_c,
+                             s.softmax_scale, s.causal, batch=seqs)
+    dt = time.perf_counter() - t0
+    nbytes = sum(int(inp.seqlens[b]) * s.D * 2 + s.T_q * s.H * s.D * 2 for b in seqs)
+    return dt, nbytes
+
+
+def cpu_baseline(inp, budget_s: float = 12.0):
+    """The oracle as it stands on the host cores, on whole sequences of the
+    workload, repeated until about budget_s seconds have passed."""
+    done_s, done_b, n, b = 0.0, 0, 0, 0
+    while done_s < budget_s:
+        dt, nb = time_oracle_sequences(inp, [b % inp.spec.B])
+        done_s += dt
+        done_b += nb
+        n += 1
+        b += 1
+    return {"value": done_b / done_s / 1e9, "unit": "GB/s", "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"{n} whole sequences ({inp.spec.seqlen or 'mixed'} tokens x {inp.spec.H} "
+                      f"heads each) of the {inp.spec.name} batch, fp64 numpy, {done_s:.1f} s"}
+
+
+def run_reference(args, spec):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    inp = mi.make_decode_inputs(spec, build_pool=False)
+    for i in range(args.warmup):
+        time_oracle_sequences(inp, [i % spec.B])
+    tot_s, tot_b = 0.0, 0
+    for i in range(args.steps):
+        dt, nb = time_oracle_sequences(inp, [(args.warmup + i) % spec.B])
+        tot_s += dt
+        tot_b += nb
+    value = tot_b / tot_s / 1e9
+    cores = blas_threads()
+    sample = f"one whole sequence of the {spec.name} batch per step (1/{spec.B} of the batch)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(spec, "fp64 numpy oracle on host cores"),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(spec, l2_note):
+    return {"workload": spec.name, "global_batch": spec.B, "seq_len": spec.seqlen,
+            "heads": spec.H, "q_tokens": spec.T_q, "d_c": spec.d_c, "d_rope": spec.d_r,
+            "page": mi.PAGE, "cache_dtype": "bf16", "softmax_scale": spec.softmax_scale,
+            "l2": l2_note, "parallelism": "replicas"}
+
+
+# --------------------------------------------------------------------------
+# the GPU arm
+# --------------------------------------------------------------------------
+
+def run_mla(args, spec):
+    import torch
+    rank, world, local, dist = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    import head_latent_attention_28_b300 as mla
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    dev = torch.device("cuda", local)
+
+    # rank r draws its own batch (same shapes, seed + r)
+    rspec = mi.DecodeSpec(**{**spec.__dict__, "seed": spec.seed + rank})
+    inp = mi.make_decode_inputs(rspec)
+    work = algorithmic_work(rspec, inp.seqlens)
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+    q = up(inp.q_bits)
+    pool0 = up(inp.pool_bits)
+    n_copies = max(3, math.ceil(3 * L2_BYTES / pool0.numel() / 2))
+    pools = [pool0] + [pool0.clone() for _ in range(n_copies - 1)]
+    bt = torch.from_numpy(inp.block_table).to(dev)
+    sl = torch.from_numpy(inp.seqlens).to(dev)
+    B, T_q, H, D = q.shape
+    ws = mla.alloc_workspace(B, T_q, H, spec.d_c, spec.d_r, torch.bfloat16, dev)
+    o = torch.empty((B, T_q, H, spec.d_c), device=dev, dtype=torch.float32)
+    lse = torch.empty((B, T_q, H), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(d_c=spec.d_c, softmax_scale=spec.softmax_scale, causal=spec.causal,
+              workspace=ws, o_lat=o, lse=lse, stream=stream)
+
+    def step(i, stage="both"):
+        mla.mla_decode_paged(q, pools[i % n_copies], bt, sl, stage=stage, **kw)
+
+    for i in range(args.warmup):
+        step(i)
+    st = mla.mla_check_status(stream)
+    if st != mla.MLA_OK:
+        raise SystemExit(f"decode failed: {mla.mla_status_string(st)}")
+
+    # ---- timed region: K whole steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier(dist, local)
+    torch.cuda.synchronize(dev)
+    with sampler:
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(dist, local)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(dist, ms)
+    if mla.mla_check_status(stream) != mla.MLA_OK:
+        raise SystemExit("decode reported a device error in the timed region")
+
+    # ---- per-kernel durations (same stream, events around each launch)
+    K2 = max(args.steps, 20)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K2)]
+    torch.cuda.synchronize(dev)
+    for i in range(K2):
+        evs[i][0].record(stream)
+        step(i, "partial")
+        evs[i][1].record(stream)
+        step(i, "combine")
+        evs[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    main_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    comb_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+
+    # ---- end to end through the public API with pinned host buffers
+    q_h = q.cpu().pin_memory()
+    bt_h = bt.cpu().pin_memory()
+    sl_h = sl.cpu().pin_memory()
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_d, bt_d, sl_d = torch.empty_like(q), torch.empty_like(bt), torch.empty_like(sl)
+    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4
+    d2h = o_h.numel() * 4 + lse_h.numel() * 4
+
+    def e2e_step(i):
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        mla.mla_decode_paged(q_d, pools[i % n_copies], bt_d, sl_d, d_c=spec.d_c,
+                             softmax_scale=spec.softmax_scale, causal=spec.causal,
+                             workspace=ws, o_lat=o, lse=lse, stream=stream)
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    barrier(dist, local)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1))
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    per_step_s = ms_max / 1e3 / args.steps
+    total_bytes = work["bytes"] * world * args.steps
+    value = total_bytes / (ms_max / 1e3) / 1e9
+    tflops = work["flops"] * world * args.steps / (ms_max / 1e3) / 1e12
+    t_mem = work["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = work["flops"] / (peaks["bf16_tflops"] * 1e12)
+    tc = mla.lib().mla_decode_path(T_q, H, spec.d_c, spec.d_r, mla.MLA_BF16) == 1
+    kernel_file = "decode_tc.cu" if tc else "decode_generic.cu"
+    achieved_gbs = work["bytes"] / (main_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm" if t_mem >= t_tc else "tensor",
+                "achieved": achieved_gbs if t_mem >= t_tc else work["flops"] / (main_ms / 1e3) / 1e12,
+                "peak": peaks["hbm_gbs"] if t_mem >= t_tc else peaks["bf16_tflops"],
+                "unit": "GB/s" if t_mem >= t_tc else "TFLOP/s",
+                "traffic": profiled_traffic(kernel_file, spec.name),
+                "kernel": kernel_file, "kernel_ms": main_ms, "combine_ms": comb_ms,
+                "peak_source": peak_src + " (burst; kernel timed alone)",
+                "achieved_tflops": work["flops"] / (main_ms / 1e3) / 1e12,
+                "tensor_peak_tflops": peaks["bf16_tflops"],
+                "step_roofline_us": 1e6 * max(t_mem, t_tc),
+                "step_frac_of_roofline": max(t_mem, t_tc) / per_step_s}
+    roofline["frac"] = roofline["achieved"] / roofline["peak"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded normal draws, shuffled block table)",
+        "config": workload_config(spec, f"inputs larger than L2: {n_copies} cache copies "
+                                        f"({n_copies * pool0.numel() * 2 / 1e6:.0f} MB) rotated"),
+        "tflops": tflops, "tokens_per_s": spec.B * spec.T_q * world * args.steps / (ms_max / 1e3),
+        "roofline": roofline,
+        "e2e": {"value": total_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / args.steps,
+                "note": "per step: latent queries, block table and lengths copied in from "
+                        "pinned host memory, o_lat and lse copied back; the cache is resident"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_budget)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["mla", "reference"], default="mla")
+    ap.add_argument("--workload", default=mi.V2_DECODE.name, choices=sorted(mi.DECODE_WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    spec = mi.DECODE_WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, spec)
+    return run_mla(args, spec)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

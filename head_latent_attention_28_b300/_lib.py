@@ -1,0 +1,250 @@
+"""ctypes binding of libmla.so: argument marshalling only.
+
+Every function here takes torch tensors that already live on the GPU, checks
+their shapes/dtypes, passes raw device pointers and sizes to the C ABI
+(include/mla.h) and raises MLAError on a non-zero status.  There is no
+fallback: if the library is missing the import of this module fails.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmla.so")
+
+MLA_OK = 0
+MLA_ERR_INVALID_ARG = 1
+MLA_ERR_UNSUPPORTED = 2
+MLA_ERR_CUDA = 3
+MLA_ERR_WORKSPACE = 4
+MLA_ERR_TIMEOUT = 5
+MLA_ERR_BAD_INDEX = 6
+MLA_F32 = 0
+MLA_BF16 = 1
+PAGE_SIZE = 64
+
+# name -> (restype, argtypes); mirrors include/mla.h
+_P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "mla_cache_append": (_I, [_P, _P, _I, _P, _P, _I, _P, _I, _I, _P, _I, _I, _I, _I, _I, _F, _P]),
+    "mla_absorb_query": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P]),
+    "mla_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "mla_decode_paged": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                              _P, _SZ, _P, _P, _P]),
+    "mla_decode_paged_partial": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
+                                      _I, _P, _SZ, _P, _P, _P]),
+    "mla_decode_combine": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                                _P, _SZ, _P, _P, _P]),
+    "mla_absorb_output": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "mla_status_string": (ctypes.c_char_p, [_I]),
+    "mla_last_cuda_error": (ctypes.c_char_p, []),
+    "mla_check_status": (_I, [_P]),
+    "mla_version": (_I, []),
+    "mla_decode_split_plan": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+    "mla_decode_num_workers": (_I, [_I, _I, _I, _I, _I, _I]),
+    "mla_decode_path": (_I, [_I, _I, _I, _I, _I]),
+}
+
+
+class MLAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = lib().mla_status_string(status).decode()
+        if status == MLA_ERR_CUDA:
+            msg += " (" + lib().mla_last_cuda_error().decode() + ")"
+        super().__init__(f"{where}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"libmla.so not built ({path}); run "
+                          "`python head_latent_attention_28_b300/build.py`")
+    cdll = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(cdll, name)
+        fn.restype, fn.argtypes = res, args
+    return cdll
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = load_library()
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != MLA_OK:
+        raise MLAError(status, where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return MLA_F32
+    if t.dtype == torch.bfloat16:
+        return MLA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+# --------------------------------------------------------------------------
+# the four calls
+# --------------------------------------------------------------------------
+
+def mla_cache_append(c, k_rope, seq_ids, positions, block_table, kv_cache, *,
+                     rope_base=10000.0, stream=None):
+    """Write rows [c ; RoPE(k_rope)] of n_new tokens into the paged cache."""
+    n_new, d_c = c.shape
+    d_r = k_rope.shape[1]
+    B, max_blocks = block_table.shape
+    num_blocks, page, D = kv_cache.shape
+    if D != d_c + d_r or k_rope.shape[0] != n_new or k_rope.dtype != c.dtype:
+        raise ValueError("shape/dtype mismatch")
+    st = lib().mla_cache_append(
+        _dev(c, "c"), _dev(k_rope, "k_rope"), _dtype_code(c),
+        _dev(seq_ids, "seq_ids", torch.int32), _dev(positions, "positions", torch.int32), n_new,
+        _dev(block_table, "block_table", torch.int32), B, max_blocks,
+        _dev(kv_cache, "kv_cache"), _dtype_code(kv_cache), num_blocks, page,
+        d_c, d_r, float(rope_base), _stream(stream))
+    _check(st, "mla_cache_append")
+
+
+def mla_absorb_query(q_nope, q_rope, positions, w_uk, *, rope_base=10000.0,
+                     q_dtype=None, out=None, stream=None):
+    """q_lat = [W^UK_h^T q_nope ; RoPE(q_rope)]  -> [N, H, d_c + d_r]."""
+    N, H, d_h = q_nope.shape
+    d_r = q_rope.shape[2]
+    d_c = w_uk.shape[1]
+    if w_uk.shape[0] != H * d_h or q_rope.shape[:2] != (N, H):
+        raise ValueError("shape mismatch")
+    if q_nope.dtype != w_uk.dtype or q_rope.dtype != w_uk.dtype:
+        raise TypeError("q_nope, q_rope and w_uk must share a dtype")
+    if out is None:
+        out = torch.empty((N, H, d_c + d_r), device=q_nope.device,
+                          dtype=q_dtype or q_nope.dtype)
+    st = lib().mla_absorb_query(
+        _dev(q_nope, "q_nope"), _dev(q_rope, "q_rope"), _dev(positions, "positions", torch.int32),
+        _dev(w_uk, "w_uk"), _dtype_code(w_uk), N, H, d_h, d_c, d_r, float(rope_base),
+        _dev(out, "q_lat"), _dtype_code(out), _stream(stream))
+    _check(st, "mla_absorb_query")
+    return out
+
+
+def mla_decode_workspace_size(B, T_q, H, d_c, d_r, dtype=torch.bfloat16) -> int:
+    code = MLA_BF16 if dtype == torch.bfloat16 else MLA_F32
+    return int(lib().mla_decode_workspace_size(B, T_q, H, d_c, d_r, code))
+
+
+def alloc_workspace(B, T_q, H, d_c, d_r, dtype=torch.bfloat16, device="cuda"):
+    n = mla_decode_workspace_size(B, T_q, H, d_c, d_r, dtype)
+    if n == 0:
+        raise ValueError("invalid decode dims")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def mla_decode_paged(q_lat, kv_cache, block_table, seqlens, *, d_c, softmax_scale,
+                     causal=False, workspace=None, o_lat=None, lse=None, want_lse=True,
+                     stream=None, stage="both"):
+    """Latent-space attention of q_lat [B, T_q, H, D] over the paged cache.
+
+    stage: "both" (mla_decode_paged), "partial" (mla_decode_paged_partial)
+    or "combine" (mla_decode_combine).
+    Returns (o_lat [B, T_q, H, d_c] float32, lse [B, T_q, H] float32 or None)."""
+    B, T_q, H, D = q_lat.shape
+    num_blocks, page, Dc = kv_cache.shape
+    d_r = D - d_c
+    if Dc != D or block_table.shape[0] != B or seqlens.shape != (B,):
+        raise ValueError("shape mismatch")
+    if q_lat.dtype != kv_cache.dtype:
+        raise TypeError("q_lat and kv_cache must share a dtype")
+    dev = q_lat.device
+    if workspace is None:
+        workspace = alloc_workspace(B, T_q, H, d_c, d_r, q_lat.dtype, dev)
+    if o_lat is None:
+        o_lat = torch.empty((B, T_q, H, d_c), device=dev, dtype=torch.float32)
+    if lse is None and want_lse:
+        lse = torch.empty((B, T_q, H), device=dev, dtype=torch.float32)
+    fn = {"both": lib().mla_decode_paged, "partial": lib().mla_decode_paged_partial,
+          "combine": lib().mla_decode_combine}[stage]
+    st = fn(
+        _dev(q_lat, "q_lat"), _dev(kv_cache, "kv_cache"), _dtype_code(q_lat),
+        _dev(block_table, "block_table", torch.int32), _dev(seqlens, "seqlens", torch.int32),
+        B, T_q, H, d_c, d_r, page, block_table.shape[1], num_blocks,
+        float(softmax_scale), 1 if causal else 0,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev(o_lat, "o_lat", torch.float32),
+        _dev(lse, "lse", torch.float32) if lse is not None else None, _stream(stream))
+    _check(st, "mla_decode_paged" + ("" if stage == "both" else "_" + stage))
+    return o_lat, lse
+
+
+def mla_absorb_output(o_lat, w_uv, w_o, *, out=None, stream=None):
+    """out = W^O concat_h(W^UV_h o_lat[:, h])  -> [N, d] float32."""
+    N, H, d_c = o_lat.shape
+    HD, d_c2 = w_uv.shape
+    d, HD2 = w_o.shape
+    if d_c2 != d_c or HD2 != HD or HD % H:
+        raise ValueError("shape mismatch")
+    if w_uv.dtype != w_o.dtype:
+        raise TypeError("w_uv and w_o must share a dtype")
+    if out is None:
+        out = torch.empty((N, d), device=o_lat.device, dtype=torch.float32)
+    st = lib().mla_absorb_output(
+        _dev(o_lat, "o_lat", torch.float32), _dev(w_uv, "w_uv"), _dev(w_o, "w_o"),
+        _dtype_code(w_uv), N, H, HD // H, d_c, d, _dev(out, "out", torch.float32),
+        _stream(stream))
+    _check(st, "mla_absorb_output")
+    return out
+
+
+def mla_decode_split_plan(seqlens, T_q, max_blocks_per_seq, num_workers):
+    """Host helper: (first_worker, last_worker, total_pages) per sequence."""
+    import numpy as np
+    sl = np.ascontiguousarray(seqlens, dtype=np.int32)
+    B = sl.shape[0]
+    first = np.empty(B, dtype=np.int32)
+    last = np.empty(B, dtype=np.int32)
+    total = ctypes.c_int64(0)
+    st = lib().mla_decode_split_plan(sl.ctypes.data, B, T_q, max_blocks_per_seq, num_workers,
+                                     first.ctypes.data, last.ctypes.data,
+                                     ctypes.addressof(total))
+    _check(st, "mla_decode_split_plan")
+    return first, last, int(total.value)
+
+
+def mla_decode_num_workers(B, T_q, H, d_c, d_r, dtype=torch.bfloat16) -> int:
+    code = MLA_BF16 if dtype == torch.bfloat16 else MLA_F32
+    return int(lib().mla_decode_num_workers(B, T_q, H, d_c, d_r, code))
+
+
+def mla_check_status(stream=None) -> int:
+    """Wait for the stream and return (and clear) the device error status."""
+    return int(lib().mla_check_status(_stream(stream)))
+
+
+def mla_status_string(status: int) -> str:
+    return lib().mla_status_string(status).decode()

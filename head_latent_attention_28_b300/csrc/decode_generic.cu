@@ -1,0 +1,329 @@
+// CUDA-core MLA decode: any d_c <= 512, any d_r, float or bfloat16 inputs.
+//
+// Serves the shapes the tensor-core kernel does not take (few heads, float
+// caches, odd widths) and is the reference-precision path: every product and
+// sum is in float (FFMA), exp2 in float, no reduced-precision operands.
+//
+// Math per (sequence b, query row r = t*H + h): online softmax over 32-token
+// tiles of the visible cache rows,
+//   m' = max(m, max_s z_s),  p_s = 2^(z_s - m'),  l' = l 2^(m - m') + sum p_s,
+//   O' = O 2^(m - m') + sum_s p_s C_s[0:d_c]
+// with z_s = log2(e) * scale * q . C_s, so that at the end o = O / l and
+// lse = ln 2 * (m + log2 l).  ("Attention, Part 2", absorbed path: scores
+// over the latent and the rotary key, causal mask, softmax, latent value sum.)
+#include "common.cuh"
+#include "internal.h"
+
+namespace mla {
+
+namespace {
+
+constexpr int GT = 256;   // threads per CTA
+constexpr int GRT = 16;   // query rows per CTA
+constexpr int GTK = 32;   // cache tokens per tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ int pages_of(int L, int T_q, int cap) {
+  return (L >= T_q && L <= cap) ? (L + kPage - 1) / kPage : 0;
+}
+
+// block-wide exclusive scan of one int per thread (GT threads); returns the
+// exclusive prefix and writes the block total to *total.
+__device__ int block_exclusive_scan(int v, int* scratch /*[GT/32 + 1]*/, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < GT / 32 ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < GT / 32) scratch[lane] = w;  // inclusive warp totals
+    if (lane == GT / 32 - 1) scratch[GT / 32] = w;
+  }
+  __syncthreads();
+  int warp_base = warp ? scratch[warp - 1] : 0;
+  *total = scratch[GT / 32];
+  int r = warp_base + x - v;
+  __syncthreads();
+  return r;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(GT) decode_generic_kernel(DecodeArgs a) {
+  extern __shared__ float smem[];
+  const int D = a.D, Dp = D + 1;
+  float* q_s = smem;                  // [GRT][D]
+  float* k_s = q_s + GRT * D;         // [GTK][Dp]
+  float* p_s = k_s + GTK * Dp;        // [GRT][GTK]  scores, then probabilities
+  float* alpha_s = p_s + GRT * GTK;   // [GRT]
+  float* m_s = alpha_s + GRT;         // [GRT]  running max (log2 units)
+  float* l_s = m_s + GRT;             // [GRT]  running sum
+  __shared__ long long tok_off[GTK];  // element offset of each tile row, -1 = absent
+  __shared__ int scan_tmp[GT / 32 + 1];
+  __shared__ long long red_tmp[GT / 32];
+  __shared__ int seg_start[GT];       // exclusive page prefix within the chunk
+  __shared__ int seg_first, seg_last;
+
+  const T* __restrict__ q = static_cast<const T*>(a.q);
+  const T* __restrict__ cache = static_cast<const T*>(a.cache);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int w = blockIdx.x;
+  const int rows = a.T_q * a.H;
+  const int r0 = blockIdx.y * GRT;
+  const int cap = a.max_blocks * kPage;
+  const float sl2 = a.scale * kLog2e;
+
+  // ---- pass 1: total pages (and the error flag for invalid lengths)
+  long long mine = 0;
+  bool bad = false;
+  for (int b = tid; b < a.B; b += GT) {
+    int L = a.seqlens[b];
+    int P = pages_of(L, a.T_q, cap);
+    bad |= (P == 0);
+    mine += P;
+  }
+  if (bad && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(a.err, kErrBadIndex);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if (lane == 0) red_tmp[warp] = mine;
+  __syncthreads();
+  long long Tpages = 0;
+  for (int i = 0; i < GT / 32; ++i) Tpages += red_tmp[i];
+  if (Tpages == 0) return;
+  const long long p0 = part_begin(Tpages, a.W, w), p1 = part_begin(Tpages, a.W, w + 1);
+  if (p0 >= p1) return;
+
+  // ---- pass 2: walk sequences in chunks, process the ones meeting [p0, p1)
+  long long base = 0;
+  for (int c0 = 0; c0 < a.B && base < p1; c0 += GT) {
+    const int bq = c0 + tid;
+    const int P = bq < a.B ? pages_of(a.seqlens[bq], a.T_q, cap) : 0;
+    int chunk_total;
+    const int excl = block_exclusive_scan(P, scan_tmp, &chunk_total);
+    seg_start[tid] = excl;
+    if (tid == 0) { seg_first = GT; seg_last = -1; }
+    __syncthreads();
+    {
+      long long S = base + excl;
+      if (P > 0 && S < p1 && S + P > p0) { atomicMin(&seg_first, tid); atomicMax(&seg_last, tid); }
+    }
+    __syncthreads();
+    const int f = seg_first, l = seg_last;
+    for (int i = f; i <= l; ++i) {
+      const int b = c0 + i;
+      const int L = a.seqlens[b];
+      const int Pb = pages_of(L, a.T_q, cap);
+      if (Pb == 0) continue;
+      const long long Sb = base + seg_start[i];
+      const long long g0 = Sb > p0 ? Sb : p0;
+      const long long g1 = (Sb + Pb) < p1 ? (Sb + Pb) : p1;
+      const int j0 = (int)(g0 - Sb), j1 = (int)(g1 - Sb);
+      const bool whole = (j0 == 0 && j1 == Pb);
+      if (j0 == 0 && blockIdx.y == 0 && tid == 0)
+        a.meta[b] = make_int2(part_worker_of(Tpages, a.W, Sb),
+                              part_worker_of(Tpages, a.W, Sb + Pb - 1));
+      const int tok0 = j0 * kPage;
+      const int tok1 = min(j1 * kPage, L);
+
+      // load this CTA's query rows
+      __syncthreads();
+      for (int i2 = tid; i2 < GRT * D; i2 += GT) {
+        int rr = i2 / D, k = i2 - rr * D;
+        int r = r0 + rr;
+        q_s[i2] = r < rows ? load_as_float(q, ((size_t)b * rows + r) * D + k) : 0.f;
+      }
+      if (tid < GRT) { m_s[tid] = -INFINITY; l_s[tid] = 0.f; }
+      float acc[GRT][2];
+#pragma unroll
+      for (int rr = 0; rr < GRT; ++rr) acc[rr][0] = acc[rr][1] = 0.f;
+
+      for (int s0 = tok0; s0 < tok1; s0 += GTK) {
+        __syncthreads();
+        if (tid < GTK) {
+          int s = s0 + tid;
+          long long off = -1;
+          if (s < tok1) {
+            int blk = a.block_table[(size_t)b * a.max_blocks + s / kPage];
+            if (blk >= 0 && blk < a.num_blocks) off = ((long long)blk * kPage + (s % kPage)) * D;
+            else atomicOr(a.err, kErrBadIndex);
+          }
+          tok_off[tid] = off;
+        }
+        __syncthreads();
+        for (int i2 = tid; i2 < GTK * D; i2 += GT) {
+          int j = i2 / D, k = i2 - j * D;
+          long long off = tok_off[j];
+          k_s[j * Dp + k] = off >= 0 ? load_as_float(cache, (size_t)off + k) : 0.f;
+        }
+        __syncthreads();
+        // scores: lane = token, rows warp and warp + 8
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int rr = warp + 8 * half;
+          const int r = r0 + rr;
+          const float* qr = q_s + rr * D;
+          const float* kr = k_s + lane * Dp;
+          float dot = 0.f;
+          for (int k = 0; k < D; ++k) dot = fmaf(qr[k], kr[k], dot);
+          const int s = s0 + lane;
+          const int t = r < rows ? r / a.H : 0;
+          const int lim = a.causal ? (L - a.T_q + t) : (L - 1);
+          const bool vis = r < rows && s < tok1 && tok_off[lane] >= 0 && s <= lim;
+          p_s[rr * GTK + lane] = vis ? dot * sl2 : -INFINITY;
+        }
+        __syncthreads();
+        // online softmax: warp handles rows 2*warp, 2*warp + 1
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int rr = 2 * warp + half;
+          float v = p_s[rr * GTK + lane];
+          float mx = v;
+#pragma unroll
+          for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          const float m_old = m_s[rr];
+          const float m_new = fmaxf(m_old, mx);
+          float p, alpha;
+          if (m_new == -INFINITY) { p = 0.f; alpha = 1.f; }
+          else { p = exp2f(v - m_new); alpha = exp2f(m_old - m_new); }
+          float sum = p;
+#pragma unroll
+          for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          p_s[rr * GTK + lane] = p;
+          __syncwarp();
+          if (lane == 0) { alpha_s[rr] = alpha; m_s[rr] = m_new; l_s[rr] = l_s[rr] * alpha + sum; }
+        }
+        __syncthreads();
+        // value sum over the first d_c numbers of each row
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = tid + cc * GT;
+          if (c < a.d_c) {
+#pragma unroll
+            for (int rr = 0; rr < GRT; ++rr) {
+              float x = acc[rr][cc] * alpha_s[rr];
+              const float* pr = p_s + rr * GTK;
+#pragma unroll 8
+              for (int j = 0; j < GTK; ++j) x = fmaf(pr[j], k_s[j * Dp + c], x);
+              acc[rr][cc] = x;
+            }
+          }
+        }
+      }
+      __syncthreads();
+      // epilogue
+      const int slot = b + w;
+#pragma unroll
+      for (int rr = 0; rr < GRT; ++rr) {
+        const int r = r0 + rr;
+        if (r >= rows) break;
+        const float lsum = l_s[rr], m = m_s[rr];
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        const float lse = lsum > 0.f ? (m + log2f(lsum)) * kLn2 : -INFINITY;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = tid + cc * GT;
+          if (c < a.d_c) {
+            if (whole) a.o[((size_t)b * rows + r) * a.d_c + c] = acc[rr][cc] * inv;
+            else a.ws_o[((size_t)slot * rows + r) * a.d_c + c] = acc[rr][cc] * inv;
+          }
+        }
+        if (tid == 0) {
+          if (whole) { if (a.lse) a.lse[(size_t)b * rows + r] = lse; }
+          else a.ws_lse[(size_t)slot * rows + r] = lse;
+        }
+      }
+    }
+    base += chunk_total;
+    __syncthreads();
+  }
+}
+
+constexpr int CT = 128;  // combine threads
+constexpr int CR = 4;    // rows per combine CTA
+
+// Merge the partial softmax results of sequences split across workers:
+// lse* = max_i lse_i, w_i = exp(lse_i - lse*) (0 for an empty part),
+// o = sum_i w_i o_i / sum_i w_i, lse = lse* + ln sum_i w_i.
+// Sequences with an invalid length get zero outputs here.
+__global__ void __launch_bounds__(CT) combine_kernel(DecodeArgs a) {
+  const int b = blockIdx.x;
+  const int rows = a.T_q * a.H;
+  const int L = a.seqlens[b];
+  const bool valid = L >= a.T_q && L <= a.max_blocks * kPage;
+  int2 m = make_int2(0, 0);
+  if (valid) m = a.meta[b];
+  if (valid && m.x == m.y) return;  // finished by its only worker
+  for (int r = blockIdx.y * CR; r < min(rows, (blockIdx.y + 1) * CR); ++r) {
+    const size_t orow = ((size_t)b * rows + r) * a.d_c;
+    if (!valid) {
+      for (int c = threadIdx.x; c < a.d_c; c += CT) a.o[orow + c] = 0.f;
+      if (threadIdx.x == 0 && a.lse) a.lse[(size_t)b * rows + r] = 0.f;
+      continue;
+    }
+    float lmax = -INFINITY;
+    for (int w = m.x; w <= m.y; ++w) lmax = fmaxf(lmax, a.ws_lse[(size_t)(b + w) * rows + r]);
+    float sumw = 0.f;
+    for (int w = m.x; w <= m.y; ++w) {
+      float lw = a.ws_lse[(size_t)(b + w) * rows + r];
+      sumw += (lw == -INFINITY) ? 0.f : expf(lw - lmax);
+    }
+    const float inv = sumw > 0.f ? 1.f / sumw : 0.f;
+    for (int c = threadIdx.x; c < a.d_c; c += CT) {
+      float acc = 0.f;
+      for (int w = m.x; w <= m.y; ++w) {
+        float lw = a.ws_lse[(size_t)(b + w) * rows + r];
+        float wt = (lw == -INFINITY) ? 0.f : expf(lw - lmax);
+        acc = fmaf(wt, a.ws_o[((size_t)(b + w) * rows + r) * a.d_c + c], acc);
+      }
+      a.o[orow + c] = acc * inv;
+    }
+    if (threadIdx.x == 0 && a.lse)
+      a.lse[(size_t)b * rows + r] = sumw > 0.f ? lmax + logf(sumw) : -INFINITY;
+  }
+}
+
+size_t generic_smem_bytes(int D) {
+  return sizeof(float) * ((size_t)GRT * D + (size_t)GTK * (D + 1) + GRT * GTK + 3 * GRT);
+}
+
+}  // namespace
+
+int generic_workers(int num_sms) { return num_sms; }
+
+cudaError_t launch_decode_generic(const DecodeArgs& a, cudaStream_t s) {
+  const size_t smem = generic_smem_bytes(a.D);
+  const int rows = a.T_q * a.H;
+  dim3 grid(a.W, (rows + GRT - 1) / GRT);
+  cudaError_t e;
+  if (a.dtype == BF16) {
+    e = cudaFuncSetAttribute(decode_generic_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    decode_generic_kernel<__nv_bfloat16><<<grid, GT, smem, s>>>(a);
+  } else {
+    e = cudaFuncSetAttribute(decode_generic_kernel<float>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    decode_generic_kernel<float><<<grid, GT, smem, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s) {
+  const int rows = a.T_q * a.H;
+  dim3 grid(a.B, (rows + CR - 1) / CR);
+  combine_kernel<<<grid, CT, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

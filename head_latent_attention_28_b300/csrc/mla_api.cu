@@ -1,0 +1,285 @@
+// C ABI entry points: host-side argument checks, workspace carving, kernel
+// selection, the per-device error word.  Declarations and the contract of
+// each call are in include/mla.h.
+#include <mutex>
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "../../include/mla.h"
+
+namespace {
+
+__device__ unsigned int g_mla_error = 0;  // bits mla::kErr*
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+thread_local char g_last_cuda[256] = "";
+
+int note_cuda(cudaError_t e) {
+  snprintf(g_last_cuda, sizeof(g_last_cuda), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return MLA_ERR_CUDA;
+}
+
+// Device address of the error word and SM count of the current device.
+cudaError_t device_info(unsigned** err, int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_mla_error);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_num_sms[dev] = n;
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  if (err) *err = g_err_ptr[dev];
+  if (sms) *sms = g_num_sms[dev];
+  return cudaSuccess;
+}
+
+bool dtype_ok(int d) { return d == MLA_F32 || d == MLA_BF16; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool decode_dims_ok(int B, int T_q, int H, int d_c, int d_r) {
+  return B >= 1 && T_q >= 1 && H >= 1 && d_c >= 1 && d_c <= 512 && d_r >= 0 &&
+         d_c + d_r <= 1024 && (long long)T_q * H <= (1 << 20);
+}
+
+int decode_workers(int dtype, int B, int T_q, int H, int d_c, int d_r, int sms) {
+  (void)B;
+  return mla::tc_supported(dtype, H, T_q, d_c, d_r) ? mla::tc_workers(sms)
+                                                     : mla::generic_workers(sms);
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_version(void) { return 100; }
+
+const char* mla_status_string(int s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: invalid argument (nothing launched)";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: unsupported shape or dtype";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA: a CUDA call failed";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace missing or too small";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a device wait gave up";
+    case MLA_ERR_BAD_INDEX: return "MLA_ERR_BAD_INDEX: block id or sequence length out of range";
+    default: return "unknown mla status";
+  }
+}
+
+const char* mla_last_cuda_error(void) { return g_last_cuda; }
+
+int mla_check_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return note_cuda(e);
+  unsigned v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_mla_error, sizeof(v));
+  if (e != cudaSuccess) return note_cuda(e);
+  if (v) {
+    unsigned z = 0;
+    e = cudaMemcpyToSymbol(g_mla_error, &z, sizeof(z));
+    if (e != cudaSuccess) return note_cuda(e);
+  }
+  if (v & mla::kErrTimeout) return MLA_ERR_TIMEOUT;
+  if (v & mla::kErrBadIndex) return MLA_ERR_BAD_INDEX;
+  return MLA_OK;
+}
+
+int mla_cache_append(const void* c, const void* k_rope, int dtype_in,
+                     const int32_t* seq_ids, const int32_t* positions, int n_new,
+                     const int32_t* block_table, int B, int max_blocks_per_seq,
+                     void* kv_cache, int cache_dtype, int num_blocks, int page_size,
+                     int d_c, int d_r, float rope_base, void* stream) {
+  if (n_new < 0 || B < 1 || d_c < 1 || d_r < 0 || (d_r & 1) || page_size != MLA_PAGE_SIZE ||
+      max_blocks_per_seq < 1 || num_blocks < 1 || !dtype_ok(dtype_in) || !dtype_ok(cache_dtype) ||
+      !(rope_base > 0.f))
+    return MLA_ERR_INVALID_ARG;
+  if (n_new == 0) return MLA_OK;
+  if (!c || (d_r > 0 && !k_rope) || !seq_ids || !positions || !block_table || !kv_cache)
+    return MLA_ERR_INVALID_ARG;
+  mla::AppendArgs a{c, k_rope, dtype_in, seq_ids, positions, n_new, block_table, B,
+                    max_blocks_per_seq, kv_cache, cache_dtype, num_blocks, d_c, d_r,
+                    rope_base, nullptr};
+  cudaError_t e = device_info(&a.err, nullptr);
+  if (e != cudaSuccess) return note_cuda(e);
+  e = mla::launch_cache_append(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : note_cuda(e);
+}
+
+int mla_absorb_query(const void* q_nope, const void* q_rope, const int32_t* positions,
+                     const void* w_uk, int dtype, int N, int H, int d_h, int d_c,
+                     int d_r, float rope_base, void* q_lat, int q_dtype, void* stream) {
+  if (N < 0 || H < 1 || d_h < 1 || d_c < 1 || d_r < 0 || (d_r & 1) || !dtype_ok(dtype) ||
+      !dtype_ok(q_dtype) || !(rope_base > 0.f) || d_h > 12288)
+    return MLA_ERR_INVALID_ARG;
+  if (N == 0) return MLA_OK;
+  if (!q_nope || (d_r > 0 && !q_rope) || !positions || !w_uk || !q_lat)
+    return MLA_ERR_INVALID_ARG;
+  mla::AbsorbQArgs a{q_nope, q_rope, positions, w_uk, dtype, N, H, d_h, d_c, d_r,
+                     rope_base, q_lat, q_dtype};
+  if (H > 65535) return MLA_ERR_UNSUPPORTED;
+  cudaError_t e = mla::launch_absorb_query(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : note_cuda(e);
+}
+
+int mla_absorb_output(const float* o_lat, const void* w_uv, const void* w_o, int dtype,
+                      int N, int H, int d_h, int d_c, int d, float* out, void* stream) {
+  if (N < 0 || H < 1 || d_h < 1 || d_c < 1 || d < 1 || !dtype_ok(dtype) ||
+      (long long)H * d_h > 32768)
+    return MLA_ERR_INVALID_ARG;
+  if (N == 0) return MLA_OK;
+  if (!o_lat || !w_uv || !w_o || !out) return MLA_ERR_INVALID_ARG;
+  mla::AbsorbOArgs a{o_lat, w_uv, w_o, dtype, N, H, d_h, d_c, d, out};
+  cudaError_t e = mla::launch_absorb_output(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : note_cuda(e);
+}
+
+size_t mla_decode_workspace_size(int B, int T_q, int H, int d_c, int d_r, int dtype) {
+  if (!decode_dims_ok(B, T_q, H, d_c, d_r) || !dtype_ok(dtype)) return 0;
+  int sms = 0;
+  if (device_info(nullptr, &sms) != cudaSuccess) return 0;
+  const int W = decode_workers(dtype, B, T_q, H, d_c, d_r, sms);
+  return mla::ws_layout(B, T_q * H, d_c, W).total;
+}
+
+int mla_decode_split_plan(const int32_t* seqlens_host, int B, int T_q, int max_blocks_per_seq,
+                          int num_workers, int32_t* first_worker, int32_t* last_worker,
+                          int64_t* total_pages) {
+  if (!seqlens_host || !first_worker || !last_worker || B < 1 || T_q < 1 ||
+      max_blocks_per_seq < 1 || num_workers < 1)
+    return MLA_ERR_INVALID_ARG;
+  const long long cap = (long long)max_blocks_per_seq * MLA_PAGE_SIZE;
+  long long T = 0;
+  for (int b = 0; b < B; ++b) {
+    const long long L = seqlens_host[b];
+    if (L >= T_q && L <= cap) T += (L + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
+  }
+  long long S = 0;
+  for (int b = 0; b < B; ++b) {
+    const long long L = seqlens_host[b];
+    if (L >= T_q && L <= cap) {
+      const long long P = (L + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
+      first_worker[b] = mla::part_worker_of(T, num_workers, S);
+      last_worker[b] = mla::part_worker_of(T, num_workers, S + P - 1);
+      S += P;
+    } else {
+      first_worker[b] = last_worker[b] = -1;
+    }
+  }
+  if (total_pages) *total_pages = T;
+  return MLA_OK;
+}
+
+int mla_decode_path(int T_q, int H, int d_c, int d_r, int dtype) {
+  if (!decode_dims_ok(1, T_q, H, d_c, d_r) || !dtype_ok(dtype)) return -1;
+  return mla::tc_supported(dtype, H, T_q, d_c, d_r) ? 1 : 0;
+}
+
+int mla_decode_num_workers(int B, int T_q, int H, int d_c, int d_r, int dtype) {
+  if (!decode_dims_ok(B, T_q, H, d_c, d_r) || !dtype_ok(dtype)) return 0;
+  int sms = 0;
+  if (device_info(nullptr, &sms) != cudaSuccess) return 0;
+  return decode_workers(dtype, B, T_q, H, d_c, d_r, sms);
+}
+
+}  // extern "C"
+
+namespace {
+
+enum DecodeStage { kStagePartial = 1, kStageCombine = 2, kStageBoth = 3 };
+
+int decode_impl(int stage, const void* q_lat, const void* kv_cache, int dtype,
+                const int32_t* block_table, const int32_t* seqlens,
+                int B, int T_q, int H, int d_c, int d_r, int page_size,
+                int max_blocks_per_seq, int num_blocks, float softmax_scale, int causal,
+                void* workspace, size_t workspace_bytes, float* o_lat, float* lse,
+                void* stream) {
+  if (!q_lat || !kv_cache || !block_table || !seqlens || !o_lat) return MLA_ERR_INVALID_ARG;
+  if (!decode_dims_ok(B, T_q, H, d_c, d_r) || !dtype_ok(dtype) || page_size != MLA_PAGE_SIZE ||
+      max_blocks_per_seq < 1 || num_blocks < 1 || !(softmax_scale > 0.f) ||
+      (long long)max_blocks_per_seq * MLA_PAGE_SIZE > (1LL << 30))
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_lat) || !aligned16(kv_cache) || !aligned16(o_lat)) return MLA_ERR_INVALID_ARG;
+  mla::DecodeArgs a{};
+  int sms = 0;
+  cudaError_t e = device_info(&a.err, &sms);
+  if (e != cudaSuccess) return note_cuda(e);
+  const bool tc = mla::tc_supported(dtype, H, T_q, d_c, d_r);
+  a.W = decode_workers(dtype, B, T_q, H, d_c, d_r, sms);
+  const mla::WsLayout L = mla::ws_layout(B, T_q * H, d_c, a.W);
+  if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  a.q = q_lat; a.cache = kv_cache; a.block_table = block_table; a.seqlens = seqlens;
+  a.dtype = dtype; a.B = B; a.T_q = T_q; a.H = H; a.d_c = d_c; a.d_r = d_r; a.D = d_c + d_r;
+  a.max_blocks = max_blocks_per_seq; a.num_blocks = num_blocks;
+  a.scale = softmax_scale; a.causal = causal ? 1 : 0;
+  a.o = o_lat; a.lse = lse;
+  a.meta = reinterpret_cast<int2*>(ws + L.meta_off);
+  a.ws_lse = reinterpret_cast<float*>(ws + L.lse_off);
+  a.ws_o = reinterpret_cast<float*>(ws + L.o_off);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (stage & kStagePartial) {
+    e = tc ? mla::launch_decode_tc(a, s) : mla::launch_decode_generic(a, s);
+    if (e != cudaSuccess) return note_cuda(e);
+  }
+  if (stage & kStageCombine) {
+    e = mla::launch_combine(a, s);
+    if (e != cudaSuccess) return note_cuda(e);
+  }
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_paged(const void* q_lat, const void* kv_cache, int dtype,
+                     const int32_t* block_table, const int32_t* seqlens,
+                     int B, int T_q, int H, int d_c, int d_r, int page_size,
+                     int max_blocks_per_seq, int num_blocks,
+                     float softmax_scale, int causal,
+                     void* workspace, size_t workspace_bytes,
+                     float* o_lat, float* lse, void* stream) {
+  return decode_impl(kStageBoth, q_lat, kv_cache, dtype, block_table, seqlens, B, T_q, H, d_c,
+                     d_r, page_size, max_blocks_per_seq, num_blocks, softmax_scale, causal,
+                     workspace, workspace_bytes, o_lat, lse, stream);
+}
+
+int mla_decode_paged_partial(const void* q_lat, const void* kv_cache, int dtype,
+                             const int32_t* block_table, const int32_t* seqlens,
+                             int B, int T_q, int H, int d_c, int d_r, int page_size,
+                             int max_blocks_per_seq, int num_blocks,
+                             float softmax_scale, int causal,
+                             void* workspace, size_t workspace_bytes,
+                             float* o_lat, float* lse, void* stream) {
+  return decode_impl(kStagePartial, q_lat, kv_cache, dtype, block_table, seqlens, B, T_q, H,
+                     d_c, d_r, page_size, max_blocks_per_seq, num_blocks, softmax_scale, causal,
+                     workspace, workspace_bytes, o_lat, lse, stream);
+}
+
+int mla_decode_combine(const void* q_lat, const void* kv_cache, int dtype,
+                       const int32_t* block_table, const int32_t* seqlens,
+                       int B, int T_q, int H, int d_c, int d_r, int page_size,
+                       int max_blocks_per_seq, int num_blocks,
+                       float softmax_scale, int causal,
+                       void* workspace, size_t workspace_bytes,
+                       float* o_lat, float* lse, void* stream) {
+  return decode_impl(kStageCombine, q_lat, kv_cache, dtype, block_table, seqlens, B, T_q, H,
+                     d_c, d_r, page_size, max_blocks_per_seq, num_blocks, softmax_scale, causal,
+                     workspace, workspace_bytes, o_lat, lse, stream);
+}
+
+}  // extern "C"

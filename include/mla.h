@@ -1,0 +1,260 @@
+/*
+ * mla.h -- C ABI of the multi-head latent attention (MLA) decode library.
+ *
+ * The library implements the inference path that the MLA pages describe:
+ * cache only the latent c_s = W^DKV h_s and the rotated decoupled key
+ * R_s k^R_s of every token, fold W^UK into the query, attend in latent
+ * space, and apply W^UV and W^O once to the attended latent.
+ *   - "Multi-head latent attention (MLA)" (ai-knowledge-tree, pillar E3),
+ *     sections 2 (down-projection, up-projections, folding) and 3
+ *     (decoupled RoPE key; score = content term + rotary term).
+ *   - "Attention, Part 2: MQA, GQA and MLA" (ishwarj.com), "The MLA
+ *     equations", "The trick that makes it fast: never rebuild at all"
+ *     (absorbed inference path), "Why position needs its own key".
+ *   - "How DeepSeek Rewrote the Transformer" (zhichai.net), "Absorbed
+ *     projections" (the value is the first d_c numbers of the key row).
+ *
+ * Conventions shared by every call:
+ *   - Every array pointer is a DEVICE pointer (cudaMalloc'd or torch
+ *     memory) owned by the caller, row-major and contiguous, 16-byte
+ *     aligned.  The library allocates no device memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call only enqueues work on it and returns; results are
+ *     ready when the stream reaches that point.
+ *   - Calls return an mla_status.  Host-side argument checks run before any
+ *     launch; when one fails nothing is launched.  Conditions that only the
+ *     device can see (a block id outside the pool, a sequence length outside
+ *     [T_q, max_blocks_per_seq * 64], a wait that ran out) are recorded in a
+ *     per-device error word; mla_check_status() reports and clears it.
+ *     Affected output rows are written as zeros, never read out of bounds.
+ *   - dtype codes: MLA_F32 (IEEE float) and MLA_BF16 (bfloat16).  Casts to
+ *     bfloat16 round to nearest even.  Accumulation is always in float.
+ *   - Cache layout ("paged pool"): kv_cache is [num_blocks, 64, D] with
+ *     D = d_c + d_r; row r of block k holds one token's [c ; R k^R].
+ *     block_table is int32 [B, max_blocks_per_seq]; token s of sequence b
+ *     lives in block block_table[b, s / 64], row s % 64.  Entries past a
+ *     sequence's last block are never read.
+ *   - Thread safety: calls keep no per-call state on the host or device
+ *     besides the error word, and may be made from several host threads.
+ */
+#ifndef MLA_H
+#define MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define MLA_OK              0
+#define MLA_ERR_INVALID_ARG 1  /* host check failed; nothing launched        */
+#define MLA_ERR_UNSUPPORTED 2  /* valid but unsupported dims/dtype combination */
+#define MLA_ERR_CUDA        3  /* a CUDA call failed; see mla_last_cuda_error */
+#define MLA_ERR_WORKSPACE   4  /* workspace NULL or smaller than required     */
+#define MLA_ERR_TIMEOUT     5  /* a device wait gave up (bounded spin)        */
+#define MLA_ERR_BAD_INDEX   6  /* device saw a bad block id or sequence length */
+
+/* dtype codes */
+#define MLA_F32  0
+#define MLA_BF16 1
+
+/* tokens per cache block; the only supported page size */
+#define MLA_PAGE_SIZE 64
+
+/*
+ * mla_cache_append -- write new tokens' rows into the paged cache.
+ *
+ * For i < n_new, with b = seq_ids[i], s = positions[i]:
+ *   row (b, s) <- [ c[i, 0:d_c] ; RoPE_s(k_rope[i, 0:d_r]) ]
+ * i.e. the cached row of "The MLA equations" (c = W_dkv x, kr = rope(W_kr x))
+ * and section 3 of the ai-knowledge-tree page: the latent is stored as is,
+ * only the decoupled key is rotated.  RoPE rotates adjacent pairs
+ * (x[2j], x[2j+1]) by s * base^(-2j/d_r) (RoFormer form); the angle and the
+ * rotation are evaluated in double precision, then cast to cache_dtype.
+ *
+ *   c          [n_new, d_c]  dtype_in        latent of each new token
+ *   k_rope     [n_new, d_r]  dtype_in        UNrotated decoupled key
+ *   seq_ids    [n_new]       int32           sequence of each token (< B)
+ *   positions  [n_new]       int32           token position s within it
+ *   block_table[B, max_blocks_per_seq] int32
+ *   kv_cache   [num_blocks, 64, d_c + d_r]  cache_dtype, written in place
+ * d_r must be even.  Host errors: NULL pointers, n_new < 0, B < 1, d_c < 1,
+ * d_r < 0 or odd, page_size != 64.  Device errors (MLA_ERR_BAD_INDEX):
+ * seq_ids[i] outside [0, B), position < 0 or >= max_blocks_per_seq * 64,
+ * block id outside [0, num_blocks); such rows are skipped.  n_new == 0
+ * launches nothing.
+ */
+int mla_cache_append(const void* c, const void* k_rope, int dtype_in,
+                     const int32_t* seq_ids, const int32_t* positions, int n_new,
+                     const int32_t* block_table, int B, int max_blocks_per_seq,
+                     void* kv_cache, int cache_dtype, int num_blocks, int page_size,
+                     int d_c, int d_r, float rope_base, void* stream);
+
+/*
+ * mla_absorb_query -- fold W^UK into the query and rotate the rotary query.
+ *
+ *   q_lat[n, h, 0:d_c]      = W^UK_h^T q_nope[n, h, :]      (float accumulate)
+ *   q_lat[n, h, d_c:d_c+d_r] = RoPE_{positions[n]}(q_rope[n, h, :])
+ * where W^UK_h is rows h*d_h .. (h+1)*d_h-1 of w_uk [H*d_h, d_c]
+ * ("The trick that makes it fast": the new query is multiplied by the
+ * transposed per-head key up-projection once, and the result is compared
+ * with the cached latents directly.)
+ *
+ *   q_nope [N, H, d_h]   dtype        content query W^Q h
+ *   q_rope [N, H, d_r]   dtype        UNrotated rotary query W^QR h
+ *   positions [N]        int32        position of each query token
+ *   w_uk   [H*d_h, d_c]  dtype
+ *   q_lat  [N, H, d_c + d_r]  q_dtype (output)
+ * Host errors: NULL pointers, non-positive dims, odd d_r, N < 0.
+ */
+int mla_absorb_query(const void* q_nope, const void* q_rope, const int32_t* positions,
+                     const void* w_uk, int dtype, int N, int H, int d_h, int d_c,
+                     int d_r, float rope_base, void* q_lat, int q_dtype, void* stream);
+
+/*
+ * mla_decode_workspace_size -- bytes of scratch mla_decode_paged needs for
+ * the split-KV partial results on the CURRENT device (it depends on the
+ * device's SM count and on which kernel the shape selects).  Returns 0 for
+ * invalid dims.
+ */
+size_t mla_decode_workspace_size(int B, int T_q, int H, int d_c, int d_r, int dtype);
+
+/*
+ * mla_decode_paged -- latent-space attention of T_q new query tokens per
+ * sequence against that sequence's paged cache (the decode hot path).
+ *
+ * For sequence b with L_b = seqlens[b] cached rows (INCLUDING the T_q new
+ * tokens, which the caller appended first), query token t at position
+ * L_b - T_q + t, head h, and row C_s = cache row of token s:
+ *   z_s   = softmax_scale * q_lat[b,t,h,:] . C_s          (content + rotary)
+ *   p     = softmax over visible s (s <= L_b - T_q + t if causal, else all)
+ *   o_lat[b,t,h,:] = sum_s p_s C_s[0:d_c]                 (V = first d_c)
+ *   lse[b,t,h]     = natural log of sum_s exp(z_s)
+ * ("The trick that makes it fast": scores and the softmax-weighted sum are
+ * taken over the cached latents themselves; section 3 of the
+ * ai-knowledge-tree page: score = content term + positional term.)
+ *
+ *   q_lat    [B, T_q, H, D]              dtype (MLA_BF16 or MLA_F32)
+ *   kv_cache [num_blocks, 64, D]         same dtype
+ *   block_table [B, max_blocks_per_seq]  int32
+ *   seqlens  [B]                         int32, device
+ *   o_lat    [B, T_q, H, d_c]            float (output)
+ *   lse      [B, T_q, H]                 float (output) or NULL
+ *   workspace, workspace_bytes           >= mla_decode_workspace_size(...)
+ * Long or ragged batches are split into page ranges processed in parallel
+ * (partial softmax results in the workspace) and merged by a log-sum-exp
+ * combine kernel.  The bf16 shape D = 576, d_c = 512, H*T_q >= 64 runs the
+ * tensor-core (tcgen05/TMEM) kernel; every other shape a CUDA-core kernel.
+ * Host errors: NULL pointers, B/T_q/H < 1, d_c < 1 or > 512, d_r < 0,
+ * D > 1024, page_size != 64, max_blocks_per_seq < 1, num_blocks < 1.
+ * Device errors (MLA_ERR_BAD_INDEX): L_b < T_q or L_b > 64*max_blocks_per_seq
+ * (that sequence's outputs are zero), a block id outside [0, num_blocks)
+ * (that page is treated as absent).  MLA_ERR_TIMEOUT: a bounded wait in the
+ * tensor-core kernel gave up; its outputs are then undefined but the context
+ * stays usable.
+ */
+int mla_decode_paged(const void* q_lat, const void* kv_cache, int dtype,
+                     const int32_t* block_table, const int32_t* seqlens,
+                     int B, int T_q, int H, int d_c, int d_r, int page_size,
+                     int max_blocks_per_seq, int num_blocks,
+                     float softmax_scale, int causal,
+                     void* workspace, size_t workspace_bytes,
+                     float* o_lat, float* lse, void* stream);
+
+/*
+ * mla_decode_paged_partial / mla_decode_combine -- the two launches that
+ * make up mla_decode_paged, exposed separately (same arguments) so that a
+ * caller can time, overlap or reorder them.  mla_decode_paged_partial runs
+ * the split-KV attention pass: sequences handled by a single worker get
+ * their final o_lat/lse, the others leave partial results in the workspace.
+ * mla_decode_combine then merges the partial results (log-sum-exp
+ * weighting) and writes zeros for sequences of invalid length.  Calling the
+ * partial pass, then the combine, on one stream, with unchanged arguments
+ * and workspace, is exactly mla_decode_paged.
+ */
+int mla_decode_paged_partial(const void* q_lat, const void* kv_cache, int dtype,
+                             const int32_t* block_table, const int32_t* seqlens,
+                             int B, int T_q, int H, int d_c, int d_r, int page_size,
+                             int max_blocks_per_seq, int num_blocks,
+                             float softmax_scale, int causal,
+                             void* workspace, size_t workspace_bytes,
+                             float* o_lat, float* lse, void* stream);
+int mla_decode_combine(const void* q_lat, const void* kv_cache, int dtype,
+                       const int32_t* block_table, const int32_t* seqlens,
+                       int B, int T_q, int H, int d_c, int d_r, int page_size,
+                       int max_blocks_per_seq, int num_blocks,
+                       float softmax_scale, int causal,
+                       void* workspace, size_t workspace_bytes,
+                       float* o_lat, float* lse, void* stream);
+
+/*
+ * mla_absorb_output -- apply W^UV per head, then W^O, to the attended latent.
+ *
+ *   o[n, h, v] = sum_c w_uv[h*d_h + v, c] * o_lat[n, h, c]
+ *   out[n, j]  = sum_{h,v} w_o[j, h*d_h + v] * o[n, h, v]
+ * ("The trick that makes it fast": the value up-projection is applied once,
+ * to the attended latent, followed by the output projection.)
+ *
+ *   o_lat [N, H, d_c] float;  w_uv [H*d_h, d_c] dtype;  w_o [d, H*d_h] dtype
+ *   out   [N, d] float (output)
+ * Host errors: NULL pointers, non-positive dims, H*d_h > 32768.
+ */
+int mla_absorb_output(const float* o_lat, const void* w_uv, const void* w_o, int dtype,
+                      int N, int H, int d_h, int d_c, int d, float* out, void* stream);
+
+/*
+ * mla_decode_split_plan -- HOST helper: which split workers mla_decode_paged
+ * assigns to each sequence, for a given worker count (no device needed).
+ *
+ * The pages of all valid sequences are laid end to end (sequence b owns
+ * ceil(L_b / 64) pages) and cut into num_workers ranges whose sizes differ
+ * by at most one page.  For each b, first_worker[b] / last_worker[b] get the
+ * first and last worker whose range meets sequence b (-1 for a sequence
+ * whose length is outside [T_q, 64 * max_blocks_per_seq]).  A sequence with
+ * first == last is finished by one worker; otherwise its partial results are
+ * merged by the log-sum-exp combine.  Returns the total page count through
+ * *total_pages (may be NULL).  All pointers are host pointers.
+ * Host errors: NULL arrays, B < 1, T_q < 1, max_blocks_per_seq < 1,
+ * num_workers < 1.
+ */
+int mla_decode_split_plan(const int32_t* seqlens_host, int B, int T_q, int max_blocks_per_seq,
+                          int num_workers, int32_t* first_worker, int32_t* last_worker,
+                          int64_t* total_pages);
+
+/*
+ * mla_decode_num_workers -- the worker count mla_decode_paged uses for this
+ * shape on the CURRENT device (depends on its SM count and on the kernel the
+ * shape selects).  Returns 0 for invalid dims or when no device is usable.
+ */
+int mla_decode_num_workers(int B, int T_q, int H, int d_c, int d_r, int dtype);
+
+/*
+ * mla_decode_path -- which attention kernel mla_decode_paged selects for a
+ * shape: 1 = tensor-core kernel (tcgen05/TMEM), 0 = CUDA-core kernel,
+ * -1 = invalid dims.  Host only; needs no device.
+ */
+int mla_decode_path(int T_q, int H, int d_c, int d_r, int dtype);
+
+/* Text for a status code (static storage). */
+const char* mla_status_string(int status);
+
+/* Text of the last CUDA error seen by this host thread ("" if none). */
+const char* mla_last_cuda_error(void);
+
+/*
+ * mla_check_status -- wait for `stream`, then read and clear the current
+ * device's error word.  Returns MLA_OK, MLA_ERR_BAD_INDEX, MLA_ERR_TIMEOUT
+ * (timeout wins if both were recorded) or MLA_ERR_CUDA.
+ */
+int mla_check_status(void* stream);
+
+/* Library ABI version (major * 100 + minor). */
+int mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H */

@@ -12,7 +12,7 @@ Readings where the pages are silent (each stated once, here):
     positions counted from 0.
   * Query t of a T_q-token step sits at position L - T_q + t, where L counts
     every cached row including the new ones; with the causal mask it sees
-    keys 0..L-T_q+t (the absorbed path's triu(..., 1) mask).
+    keys 0..L-T_q+t (a token attends to itself and to earlier tokens).
   * Query compression is left out: q^C = W^Q h and q^R = W^QR h directly.
   * d_v = d_h.
 """
@@ -94,7 +94,7 @@ def absorb_query(q_nope, q_rope_raw, positions, W_uk, base):
     q_nope = np.asarray(q_nope, dtype=np.float64)
     n, H, d_h = q_nope.shape
     W = np.asarray(W_uk, dtype=np.float64).reshape(H, d_h, -1)   # [H, d_h, d_c]
-    q_c = np.einsum("nhd,hdc->nhc", q_nope, W)
+    q_c = np.stack([q_nope[:, hh, :] @ W[hh] for hh in range(H)], axis=1)   # [n, H, d_c]
     q_r = rope(np.asarray(q_rope_raw, np.float64).transpose(1, 0, 2),
                positions, base).transpose(1, 0, 2)
     return np.concatenate([q_c, q_r], axis=-1)
@@ -151,7 +151,7 @@ def absorb_output(o_lat, W_uv, W_o):
     o_lat = np.asarray(o_lat, dtype=np.float64)
     n, H, d_c = o_lat.shape
     W = np.asarray(W_uv, dtype=np.float64).reshape(H, -1, d_c)   # [H, d_h, d_c]
-    o = np.einsum("nhc,hvc->nhv", o_lat, W)
+    o = np.stack([o_lat[:, hh, :] @ W[hh].T for hh in range(H)], axis=1)    # [n, H, d_h]
     return o.reshape(n, -1) @ np.asarray(W_o, dtype=np.float64).T
 
 
@@ -181,8 +181,8 @@ def full_model_unabsorbed(inp):
     kr = rope(kr_raw, pos, s.rope_base)                        # [n, d_r]
     W_uk = np.asarray(inp.W_uk, np.float64).reshape(H, d_h, d_c)
     W_uv = np.asarray(inp.W_uv, np.float64).reshape(H, d_h, d_c)
-    k_c = np.einsum("hdc,sc->hsd", W_uk, c)                   # [H, n, d_h]
-    v = np.einsum("hdc,sc->hsd", W_uv, c)                     # [H, n, d_h]
+    k_c = np.stack([c @ W_uk[hh].T for hh in range(H)])      # [H, n, d_h]
+    v = np.stack([c @ W_uv[hh].T for hh in range(H)])         # [H, n, d_h]
     q_nope, _, q_rope = project_queries(h, inp.W_q, inp.W_qr, H, d_h, s.d_r,
                                         pos, s.rope_base)
     qs = range(s.n_cached, s.n_tokens)
@@ -227,8 +227,8 @@ def full_model_rope_on_reconstructed_keys(inp):
     kr = rope(kr_raw, pos, s.rope_base)
     W_uk = np.asarray(inp.W_uk, np.float64).reshape(H, d_h, d_c)
     W_uv = np.asarray(inp.W_uv, np.float64).reshape(H, d_h, d_c)
-    k_c = rope(np.einsum("hdc,sc->hsd", W_uk, c), pos, s.rope_base)
-    v = np.einsum("hdc,sc->hsd", W_uv, c)
+    k_c = rope(np.stack([c @ W_uk[hh].T for hh in range(H)]), pos, s.rope_base)
+    v = np.stack([c @ W_uv[hh].T for hh in range(H)])
     q_nope, _, q_rope = project_queries(h, inp.W_q, inp.W_qr, H, d_h, s.d_r,
                                         pos, s.rope_base)
     q_nope_rot = rope(q_nope.transpose(1, 0, 2), pos, s.rope_base).transpose(1, 0, 2)

@@ -1,0 +1,109 @@
+"""CPU checks of the C ABI: the library loads, exports every declared entry
+point, rejects bad arguments on the host before touching a device, and its
+split planner partitions pages as documented."""
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+import head_latent_attention_28_b300 as mla
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "mla.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(mla_\w+)\s*\(", text))
+
+
+def test_header_declarations_match_binding_and_exports():
+    decl = declared_functions()
+    assert decl, "no declarations parsed"
+    assert decl == set(mla.SIGNATURES), decl ^ set(mla.SIGNATURES)
+    lib = mla.load_library()
+    for name in decl:
+        assert hasattr(lib, name)
+
+
+def test_status_strings_and_version():
+    for code in range(7):
+        assert mla.mla_status_string(code)
+    assert mla.lib().mla_version() >= 100
+
+
+def test_decode_rejects_bad_arguments_on_host():
+    lib = mla.lib()
+    P = 16  # a non-null, 16-byte aligned dummy address; never dereferenced
+    ok = dict(q=P, kv=P, dt=1, bt=P, sl=P, B=1, T_q=1, H=128, d_c=512, d_r=64, page=64,
+              maxb=4, nb=4, scale=0.07, causal=0, ws=P, wsb=1 << 30, o=P, lse=None, s=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.mla_decode_paged(a["q"], a["kv"], a["dt"], a["bt"], a["sl"], a["B"], a["T_q"],
+                                    a["H"], a["d_c"], a["d_r"], a["page"], a["maxb"], a["nb"],
+                                    a["scale"], a["causal"], a["ws"], a["wsb"], a["o"], a["lse"],
+                                    a["s"])
+    bad = [dict(q=None), dict(kv=None), dict(bt=None), dict(sl=None), dict(o=None),
+           dict(B=0), dict(T_q=0), dict(H=0), dict(d_c=0), dict(d_c=513), dict(d_r=-1),
+           dict(d_r=600), dict(page=32), dict(maxb=0), dict(nb=0), dict(scale=0.0),
+           dict(dt=7), dict(q=P + 2)]
+    for kw in bad:
+        assert call(**kw) == mla.MLA_ERR_INVALID_ARG, kw
+
+
+def test_other_calls_reject_bad_arguments_on_host():
+    lib = mla.lib()
+    P = 16
+    # append: odd d_r, bad page size, null cache
+    assert lib.mla_cache_append(P, P, 1, P, P, 1, P, 1, 4, P, 1, 4, 64, 512, 63, 1e4, None) == 1
+    assert lib.mla_cache_append(P, P, 1, P, P, 1, P, 1, 4, P, 1, 4, 32, 512, 64, 1e4, None) == 1
+    assert lib.mla_cache_append(P, P, 1, P, P, 1, P, 1, 4, None, 1, 4, 64, 512, 64, 1e4, None) == 1
+    assert lib.mla_cache_append(P, P, 1, P, P, 0, P, 1, 4, P, 1, 4, 64, 512, 64, 1e4, None) == 0
+    # absorb query / output
+    assert lib.mla_absorb_query(None, P, P, P, 1, 1, 8, 32, 64, 16, 1e4, P, 1, None) == 1
+    assert lib.mla_absorb_query(P, P, P, P, 1, 1, 8, 32, 64, 15, 1e4, P, 1, None) == 1
+    assert lib.mla_absorb_output(P, P, P, 1, 1, 8, 32, 64, 0, P, None) == 1
+    assert lib.mla_absorb_output(P, P, P, 1, 1, 256, 256, 64, 64, P, None) == 1  # H*d_h too big
+
+
+def brute_force_plan(seqlens, T_q, max_blocks, W):
+    """Explicit page list: page p goes to the worker w with
+    floor(T w / W) <= p < floor(T (w+1) / W)."""
+    cap = max_blocks * 64
+    owners = []
+    seq_of_page = []
+    for b, L in enumerate(seqlens):
+        if T_q <= L <= cap:
+            seq_of_page += [b] * ((L + 63) // 64)
+    T = len(seq_of_page)
+    for w in range(W):
+        owners += [w] * ((T * (w + 1)) // W - (T * w) // W)
+    first = [-1] * len(seqlens)
+    last = [-1] * len(seqlens)
+    for p, b in enumerate(seq_of_page):
+        if first[b] < 0:
+            first[b] = owners[p]
+        last[b] = owners[p]
+    return first, last, T
+
+
+@pytest.mark.parametrize("W", [1, 3, 74, 148, 1000])
+def test_split_plan_matches_brute_force(W):
+    rng = np.random.default_rng(W)
+    for trial in range(5):
+        B = int(rng.integers(1, 60))
+        seqlens = rng.integers(0, 3000, size=B).astype(np.int32)
+        seqlens[rng.random(B) < 0.1] = 5000       # over capacity -> invalid
+        f, l, T = mla.mla_decode_split_plan(seqlens, 2, 64, W)
+        bf, bl, bT = brute_force_plan(seqlens.tolist(), 2, 64, W)
+        assert T == bT
+        np.testing.assert_array_equal(f, bf)
+        np.testing.assert_array_equal(l, bl)
+        # partial slots b + w are distinct over all (sequence, worker) pairs
+        slots = [b + w for b in range(B) if f[b] >= 0 and f[b] != l[b]
+                 for w in range(f[b], l[b] + 1)]
+        assert len(slots) == len(set(slots))
+        assert all(s < B + W for s in slots)
