@@ -25,7 +25,9 @@ import json
 import math
 import os
 import re
+import shutil
 import statistics
+import subprocess
 import sys
 import threading
 import time
@@ -101,56 +103,82 @@ def profiled_traffic(kernel_file: str, workload: str):
 # --------------------------------------------------------------------------
 
 class ClockSampler:
+    """Samples the SM clock and the clock-event reasons of one GPU in the
+    background (NVML if importable, else `nvidia-smi -lms`)."""
     REASONS = {  # NVML clocks-event reason bits
-        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
-        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
-        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
-        0x100: "display_clock_setting"}
+        0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+        0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+        0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int, period_s: float = 0.005):
-        self.samples, self.reasons, self.max_mhz = [], set(), None
-        self.period, self._stop = period_s, threading.Event()
-        self.ok = False
+    def __init__(self, device_index: int, period_s: float = 0.01):
+        self.dev, self.period = device_index, period_s
+        self.samples, self.reasons, self.max_mhz, self.err = [], set(), None, None
+        self._stop = threading.Event()
+        self.mode = None
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
             self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
+            self.mode = "nvml"
         except Exception as e:  # noqa: BLE001
             self.err = repr(e)
+            if shutil.which("nvidia-smi"):
+                self.mode = "nvidia-smi"
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self.nv
         while not self._stop.is_set():
             try:
                 self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
                 bits = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                for b, name in self.REASONS.items():
-                    if bits & b and name != "gpu_idle":
-                        self.reasons.add(name)
+                self.reasons.update(n for b, n in self.REASONS.items() if bits & b)
             except Exception:  # noqa: BLE001
                 pass
             time.sleep(self.period)
 
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
+        if self.mode == "nvml":
+            self.t = threading.Thread(target=self._run_nvml, daemon=True)
             self.t.start()
+        elif self.mode == "nvidia-smi":
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.SMI_FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", str(int(self.period * 1000))],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         return self
 
     def __exit__(self, *a):
-        if self.ok:
+        if self.mode == "nvml":
             self._stop.set()
             self.t.join()
+        elif self.mode == "nvidia-smi":
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 8:
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for name, v in zip(names, f[4:8]):
+                    if v.lower() == "active":
+                        self.reasons.add(name)
 
     def summary(self):
-        if not self.ok:
+        if self.mode is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.err}
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples)}
+                "samples": len(self.samples), "source": self.mode}
 
 
 # --------------------------------------------------------------------------
@@ -427,8 +455,8 @@ def run_mla(args, spec):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["mla", "reference"], default="mla")
     ap.add_argument("--workload", default=mi.V2_DECODE.name, choices=sorted(mi.DECODE_WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=12.0)

@@ -19,14 +19,20 @@ enum DType { F32 = 0, BF16 = 1 };
 // Split-KV partition.
 //
 // Sequence b owns the global page range [S_b, S_b + P_b), P_b = ceil(L_b/64),
-// S_b = sum_{b'<b} P_b'.  With W workers and T = sum_b P_b pages, worker w
-// processes pages [floor(T*w/W), floor(T*(w+1)/W)): every worker gets the
-// same number of pages give or take one, whatever the length mix.  A sequence
+// S_b = sum_{b'<b} P_b'.  With T = sum_b P_b pages and W' = min(W, T) active
+// workers (W launched), worker w < W' processes pages
+// [floor(T*w/W'), floor(T*(w+1)/W')): every active worker gets the same
+// number of pages give or take one, whatever the length mix, and none is
+// empty (so the workers between a sequence's first and last one all hold a
+// part of it).  A sequence
 // whose pages fall to a single worker is finished by that worker; otherwise
 // every worker that touched it leaves a partial (o, lse) in slot b + w of the
 // workspace (b + w is unique among intersecting (b, w) pairs because both
 // page ranges are ordered), and the combine kernel merges them.
 // ---------------------------------------------------------------------------
+__host__ __device__ inline int part_active(long long T, int W) {
+  return (int)(T < (long long)W ? T : (long long)W);
+}
 __host__ __device__ inline long long part_begin(long long T, int W, int w) {
   return (T * (long long)w) / W;
 }

@@ -100,8 +100,9 @@ __global__ void __launch_bounds__(GT) decode_generic_kernel(DecodeArgs a) {
   long long Tpages = 0;
   for (int i = 0; i < GT / 32; ++i) Tpages += red_tmp[i];
   if (Tpages == 0) return;
-  const long long p0 = part_begin(Tpages, a.W, w), p1 = part_begin(Tpages, a.W, w + 1);
-  if (p0 >= p1) return;
+  const int Wa = part_active(Tpages, a.W);
+  if (w >= Wa) return;
+  const long long p0 = part_begin(Tpages, Wa, w), p1 = part_begin(Tpages, Wa, w + 1);
 
   // ---- pass 2: walk sequences in chunks, process the ones meeting [p0, p1)
   long long base = 0;
@@ -130,8 +131,8 @@ __global__ void __launch_bounds__(GT) decode_generic_kernel(DecodeArgs a) {
       const int j0 = (int)(g0 - Sb), j1 = (int)(g1 - Sb);
       const bool whole = (j0 == 0 && j1 == Pb);
       if (j0 == 0 && blockIdx.y == 0 && tid == 0)
-        a.meta[b] = make_int2(part_worker_of(Tpages, a.W, Sb),
-                              part_worker_of(Tpages, a.W, Sb + Pb - 1));
+        a.meta[b] = make_int2(part_worker_of(Tpages, Wa, Sb),
+                              part_worker_of(Tpages, Wa, Sb + Pb - 1));
       const int tok0 = j0 * kPage;
       const int tok1 = min(j1 * kPage, L);
 

@@ -168,12 +168,13 @@ int mla_decode_split_plan(const int32_t* seqlens_host, int B, int T_q, int max_b
     if (L >= T_q && L <= cap) T += (L + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
   }
   long long S = 0;
+  const int Wa = mla::part_active(T, num_workers);
   for (int b = 0; b < B; ++b) {
     const long long L = seqlens_host[b];
     if (L >= T_q && L <= cap) {
       const long long P = (L + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
-      first_worker[b] = mla::part_worker_of(T, num_workers, S);
-      last_worker[b] = mla::part_worker_of(T, num_workers, S + P - 1);
+      first_worker[b] = mla::part_worker_of(T, Wa, S);
+      last_worker[b] = mla::part_worker_of(T, Wa, S + P - 1);
       S += P;
     } else {
       first_worker[b] = last_worker[b] = -1;

@@ -209,8 +209,8 @@ int mla_absorb_output(const float* o_lat, const void* w_uv, const void* w_o, int
  * assigns to each sequence, for a given worker count (no device needed).
  *
  * The pages of all valid sequences are laid end to end (sequence b owns
- * ceil(L_b / 64) pages) and cut into num_workers ranges whose sizes differ
- * by at most one page.  For each b, first_worker[b] / last_worker[b] get the
+ * ceil(L_b / 64) pages, T pages in all) and cut into min(num_workers, T)
+ * non-empty ranges whose sizes differ by at most one page.  For each b, first_worker[b] / last_worker[b] get the
  * first and last worker whose range meets sequence b (-1 for a sequence
  * whose length is outside [T_q, 64 * max_blocks_per_seq]).  A sequence with
  * first == last is finished by one worker; otherwise its partial results are

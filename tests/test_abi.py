@@ -70,8 +70,8 @@ def test_other_calls_reject_bad_arguments_on_host():
 
 
 def brute_force_plan(seqlens, T_q, max_blocks, W):
-    """Explicit page list: page p goes to the worker w with
-    floor(T w / W) <= p < floor(T (w+1) / W)."""
+    """Explicit page list: with W' = min(W, T) active workers, page p goes to
+    the worker w with floor(T w / W') <= p < floor(T (w+1) / W')."""
     cap = max_blocks * 64
     owners = []
     seq_of_page = []
@@ -79,8 +79,11 @@ def brute_force_plan(seqlens, T_q, max_blocks, W):
         if T_q <= L <= cap:
             seq_of_page += [b] * ((L + 63) // 64)
     T = len(seq_of_page)
-    for w in range(W):
-        owners += [w] * ((T * (w + 1)) // W - (T * w) // W)
+    Wa = min(W, T)
+    for w in range(Wa):
+        cnt = (T * (w + 1)) // Wa - (T * w) // Wa
+        assert cnt >= 1                     # no active worker is empty
+        owners += [w] * cnt
     first = [-1] * len(seqlens)
     last = [-1] * len(seqlens)
     for p, b in enumerate(seq_of_page):
@@ -102,8 +105,16 @@ def test_split_plan_matches_brute_force(W):
         assert T == bT
         np.testing.assert_array_equal(f, bf)
         np.testing.assert_array_equal(l, bl)
-        # partial slots b + w are distinct over all (sequence, worker) pairs
+        # partial slots b + w are distinct over all (sequence, worker) pairs,
+        # and every worker between a sequence's first and last holds part of it
         slots = [b + w for b in range(B) if f[b] >= 0 and f[b] != l[b]
                  for w in range(f[b], l[b] + 1)]
         assert len(slots) == len(set(slots))
         assert all(s < B + W for s in slots)
+        valid = [b for b in range(B) if f[b] >= 0]
+        for b0, b1 in zip(valid, valid[1:]):
+            assert f[b1] in (l[b0], l[b0] + 1)   # contiguous, no skipped worker
+
+    # few pages, many workers: the case where idle workers would leave holes
+    f, l, T = mla.mla_decode_split_plan(np.array([300, 129], np.int32), 1, 8, W)
+    assert T == 8 and f[0] == 0 and l[1] == min(W, 8) - 1

@@ -26,9 +26,11 @@ def test_cache_append_matches_oracle(cache_dtype, in_dtype):
     d_c, d_r, B, maxb, nb = 512, 64, 3, 4, 16
     n_new = 37
     bt = rng.permutation(nb)[: B * maxb].reshape(B, maxb).astype(np.int32)
-    seq_ids = rng.integers(0, B, n_new).astype(np.int32)
-    positions = rng.choice(maxb * 64, n_new, replace=False).astype(np.int32)
-    positions[:3] = [0, 63, maxb * 64 - 1]
+    # distinct (sequence, position) pairs, including both ends of the table
+    flat = rng.choice(B * maxb * 64 - 3, n_new - 3, replace=False) + 3
+    flat = np.concatenate([[0, 63, maxb * 64 - 1], flat]).astype(np.int64)
+    seq_ids = (flat // (maxb * 64)).astype(np.int32)
+    positions = (flat % (maxb * 64)).astype(np.int32)
     c = rng.standard_normal((n_new, d_c)).astype(np.float32)
     kr = rng.standard_normal((n_new, d_r)).astype(np.float32)
     if in_dtype == torch.bfloat16:
