@@ -415,12 +415,14 @@ def run_mla(args, spec):
     tc = mla.lib().mla_decode_path(T_q, H, spec.d_c, spec.d_r, mla.MLA_BF16) == 1
     kernel_file = "decode_tc.cu" if tc else "decode_generic.cu"
     achieved_gbs = work["bytes"] / (main_ms / 1e3) / 1e9
+    workers = mla.lib().mla_decode_num_workers(B, T_q, H, spec.d_c, spec.d_r, mla.MLA_BF16)
     roofline = {"bound": "hbm" if t_mem >= t_tc else "tensor",
                 "achieved": achieved_gbs if t_mem >= t_tc else work["flops"] / (main_ms / 1e3) / 1e12,
                 "peak": peaks["hbm_gbs"] if t_mem >= t_tc else peaks["bf16_tflops"],
                 "unit": "GB/s" if t_mem >= t_tc else "TFLOP/s",
                 "traffic": profiled_traffic(kernel_file, spec.name),
                 "kernel": kernel_file, "kernel_ms": main_ms, "combine_ms": comb_ms,
+                "split_workers": workers,
                 "peak_source": peak_src + " (burst; kernel timed alone)",
                 "achieved_tflops": work["flops"] / (main_ms / 1e3) / 1e12,
                 "tensor_peak_tflops": peaks["bf16_tflops"],

@@ -147,8 +147,10 @@ def test_layout_invariance_bitwise():
 
 def test_batch_order_invariance():
     """A sequence's output does not depend on its neighbours beyond the
-    split plan: moving it inside the batch changes nothing beyond float
-    rounding of the partial merge."""
+    split plan: running it alone changes only rounding.  (On the tensor-core
+    path the probabilities are rounded to bf16 relative to each worker's
+    running max, so a different split rounds differently: the bf16 decode
+    tolerance applies, not a float one.)"""
     spec = mi.DecodeSpec("order", seed=22, B=3, H=128, seqlens=(5000, 100, 2500))
     inp = mi.make_decode_inputs(spec)
     o, _ = run_decode(inp)
@@ -158,7 +160,7 @@ def test_batch_order_invariance():
                               inp.block_table[b:b + 1], inp.q_bits[b:b + 1],
                               inp.seq_rows(b), inp.pool_bits)
         ob, _ = run_decode(one)
-        np.testing.assert_allclose(ob[0], o[b], rtol=0, atol=2e-5)
+        assert_decode_close(ob[0], o[b], what=f"seq {b} alone vs in batch")
 
 
 # --------------------------------------------------------------------------
