@@ -8,24 +8,29 @@
 // the value is the first d_c numbers of the cached row).
 //
 // How (B300-specific).  One split worker is a cluster of two CTAs on two SMs:
-//  * CTA 0, the score CTA, keeps the whole 128 x 576 latent query in tensor
-//    memory (A operand), streams full 64-token pages with TMA and computes
-//    S = Q . C^T (M=128 rows, N=64 tokens, K=576) with tcgen05.mma into one of
-//    three TMEM score buffers.  Eight softmax warps (two per row, 32 tokens
-//    each) run a base-2 online softmax with a lazy running max (the output is
-//    rescaled only when a row max grows by more than 2^8; exact after the
-//    final division), round the probabilities to bf16 and ship them, with the
-//    per-row rescale factors, to the value CTA as one 17 KB bulk copy through
-//    distributed shared memory.
+//  * CTA 0, the score CTA, streams its pages from HBM two at a time through a
+//    ring of ten 16 KB cells (cell c of a page pair = the 64-dim box c of
+//    both pages, so one N=128 MMA covers both pages), and computes
+//    S = Q . C^T (M=128 rows, N=128 tokens, K=576) with tcgen05.mma into one of
+//    two TMEM score buffers.  The latent part of the query (K 0..511) is the A
+//    operand in tensor memory, the rotary part (K 512..575) sits in shared
+//    memory.  Eight softmax warps (one page of the pair per half) run a
+//    base-2 online softmax with a lazy running max (the output is rescaled
+//    only when a row max grows by more than 2^8; exact after the final
+//    division) and round the probabilities to bf16.  Each page's probabilities
+//    and per-row rescale factors are staged in shared memory in the layout the
+//    value CTA's MMA reads and moved there with one bulk copy (a contiguous
+//    copy runs at twice the rate of per-row remote stores; its bytes complete
+//    the receiver's barrier).
 //  * CTA 1, the value CTA, keeps the full 128 x 512 fp32 output in tensor
 //    memory (all 512 columns), streams the 512 latent dims of the same pages
-//    (the second read of a page is an L2 hit) and accumulates O += P . V with
-//    tcgen05.mma (A = P from shared memory, B = V MN-major, N = 2 x 256).
-//    Four warps apply row rescales, zero the rows of a last page past the
-//    sequence end (0 x NaN would poison O), and write the normalised output.
+//    in half-page units through a 4-deep ring (the second read of a page is
+//    an L2 hit) and accumulates O += P . V with tcgen05.mma (A = P from shared
+//    memory, B = V MN-major, N = 256 per half).  Four warps apply row
+//    rescales and zero the rows of a last page past the sequence end (0 x NaN
+//    would poison O); eight warps write the normalised output.
 // The data flow is one-way (score CTA -> value CTA), so the distributed-
-// shared-memory latency is pipelined, never on a round trip.  Both CTAs carry
-// 1024-1152 MMA cycles per page: the pair is balanced.
+// shared-memory latency is pipelined, never on a round trip.
 // Every mbarrier wait is bounded (2 s): on expiry the kernel records
 // MLA_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -43,21 +48,37 @@ using namespace sm100;
 constexpr int kThreads = 320;            // 10 warps
 constexpr int kRows = 128;               // query rows per sequence handled here
 constexpr int kBox = 8192;               // 64 tokens x 64 dims x bf16
-constexpr int kSStageBytes = 9 * kBox;   // score CTA: full 576-dim page
-constexpr int kVStageBytes = 8 * kBox;   // value CTA: 512 latent dims
-constexpr int kStagesBytes = 2 * kSStageBytes;   // two stages (both roles fit)
+constexpr int kCell = 2 * kBox;          // score CTA: box c of both pages of a pair
+constexpr int kCells = 10;               // score CTA: ring depth (cells)
+constexpr int kVUnit = 4 * kBox;         // value CTA: 256 latent dims of one page
+constexpr int kVUnits = 4;               // value CTA: ring depth (half pages)
 constexpr int kPBytes = kRows * 64 * 2;  // bf16 probabilities of one page (K-major, SW128)
 constexpr int kInfoBytes = 16 + kRows * 8;       // header + (alpha, l) per row
-constexpr int kPMsgBytes = kPBytes + kInfoBytes; // one bulk copy per page
-constexpr int kPSlotBytes = 34816;       // P + info + room for a second P (34 KB)
-constexpr int kSmemBytes = kStagesBytes + 2 * kPSlotBytes + 1024;
+constexpr int kPMsgBytes = kPBytes + kInfoBytes; // bytes delivered per page (one bulk copy)
+constexpr int kPSlotBytes = 18432;
+constexpr int kPSlots = 4;               // probability slots (pages)
+// shared-memory map (offsets from the 1 KB aligned base)
+constexpr int kOffQr = 0;                // score CTA: rotary query, 128 x 64 bf16 (K-major SW128)
+constexpr int kOffStg = 16384;           // score CTA: the step's two outgoing page messages
+constexpr int kOffCells = kOffStg + 2 * kPSlotBytes;   // score CTA: 10 cells
+constexpr int kOffV = 0;                 // value CTA: 4 half-page units
+constexpr int kOffP = kVUnits * kVUnit;  // value CTA: probability slots (score CTA writes them)
+constexpr int kScoreSmem = kOffCells + kCells * kCell;
+constexpr int kValueSmem = kOffP + kPSlots * kPSlotBytes;
+constexpr int kSmemBytes = (kScoreSmem > kValueSmem ? kScoreSmem : kValueSmem) + 1024;
 constexpr int kMaxItems = 64;            // work items planned per batch
-// TMEM columns
-constexpr uint32_t kTmemQ = 192;         // score CTA: 288 columns = 576 bf16 query dims
+// TMEM columns (score CTA): score buffers 2 x 128 at [0, 256), latent query at [256, 512)
+constexpr uint32_t kTmemQ = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr uint64_t kWaitNs = 2000000000ull;
+
+static_assert(kPMsgBytes <= kPSlotBytes, "probability slot too small");
+static_assert(kPMsgBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
+static_assert(kOffCells % 1024 == 0, "SW128 operands need 1 KB alignment");
+static_assert(kOffP % 1024 == 0 && kPSlotBytes % 1024 == 0, "SW128 operands need 1 KB alignment");
+static_assert(8 * 2048 <= kPBytes, "epilogue staging lives in a probability slot");
 
 struct Item {
   int b, j0, j1;            // sequence, page range [j0, j1)
@@ -67,14 +88,17 @@ struct Item {
 
 struct SmemCtl {
   // score CTA
-  uint64_t stage_full[2], stage_empty[2];
-  uint64_t s_full[3], s_free[3];
-  uint64_t q_ready, pfree[2];
+  uint64_t cell_full[kCells], cell_empty[kCells];
+  uint64_t s_full[2], s_free[2];
+  uint64_t q_ready, pfree[kPSlots];
   // value CTA
-  uint64_t v_full[2], v_empty[2];
-  uint64_t p_recv[2], pv_done[2];
+  uint64_t v_full[kVUnits], v_empty[kVUnits];
+  uint64_t p_recv[kPSlots], pv_done[kPSlots];
   uint64_t resc_done, vz_done;
   uint64_t o_free;          // the epilogue has read O: the next item may overwrite it
+  uint64_t epi_go;          // O of the item is final (value row warps -> other warps)
+  uint64_t epi_done;        // all epilogue warps are done with the staging slot
+  uint64_t rows_seen[kPSlots];   // all row warps have read the header and factors in a slot
   // both
   uint64_t grp, mma_final;
   uint32_t tmem_base;
@@ -82,8 +106,9 @@ struct SmemCtl {
   int never;                // stays 0: abort flag for the final drain waits
   int n_batch, n_total;
   int scan[kThreads / 32];
-  float rowx[2][kRows];     // score CTA: per-half row maxima
-  float rowl[2][kRows];     // score CTA: per-half row sums (last page of an item)
+  float rowx[2][kRows];     // score CTA: per-half row maxima of a step
+  float rowl[2][kRows];     // score CTA: per-half row sums (last step of an item)
+  uint32_t pflags[kPSlots]; // score CTA: header flags of the page in flight per slot
   Item items[kMaxItems];
 };
 
@@ -180,6 +205,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, kWaitNs));
 }
 
+// the same, with acquire at cluster scope (bytes or arrivals from the peer CTA)
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, abort, kWaitNs));
+}
+
 // barrier among the warps of a role, with a bounded wait (a plain bar.sync
 // could not give up if a warp left after a timeout)
 __device__ __forceinline__ bool group_sync(uint64_t* grp, uint32_t& phase, volatile int* abort) {
@@ -202,8 +232,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
   __shared__ SmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stages = smem;                          // 2 page stages
-  uint8_t* pslots = smem + kStagesBytes;           // 2 probability slots
+  uint8_t* pslots = smem + kOffP;                  // value CTA: probability slots
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();         // 0: score CTA, 1: value CTA
@@ -213,29 +242,35 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
   if (threadIdx.x == 0) {
     ctl.abort = 0;
     ctl.never = 0;
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&ctl.stage_full[i], 1);
-      mbar_init(&ctl.stage_empty[i], 1);
-      mbar_init(&ctl.pfree[i], 1);
-      mbar_init(&ctl.v_full[i], 1);
-      mbar_init(&ctl.v_empty[i], 1);
-      mbar_init(&ctl.p_recv[i], 1);
-      mbar_init(&ctl.pv_done[i], 1);
+    for (int i = 0; i < kCells; ++i) {
+      mbar_init(&ctl.cell_full[i], 1);
+      mbar_init(&ctl.cell_empty[i], 1);
     }
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.s_full[i], 1);
       mbar_init(&ctl.s_free[i], 8);
+    }
+    for (int i = 0; i < kVUnits; ++i) {
+      mbar_init(&ctl.v_full[i], 1);
+      mbar_init(&ctl.v_empty[i], 1);
+    }
+    for (int i = 0; i < kPSlots; ++i) {
+      mbar_init(&ctl.pfree[i], 1);
+      mbar_init(&ctl.p_recv[i], 1);
+      mbar_init(&ctl.pv_done[i], 1);
+      ctl.pflags[i] = 0;
     }
     mbar_init(&ctl.q_ready, 8);
     mbar_init(&ctl.resc_done, 4);
     mbar_init(&ctl.vz_done, 4);
-    mbar_init(&ctl.o_free, 4);
-    mbar_init(&ctl.grp, rank == 0 ? 8 : 4);
+    mbar_init(&ctl.o_free, 8);
+    mbar_init(&ctl.epi_go, 4);
+    mbar_init(&ctl.epi_done, 8);
+    for (int i = 0; i < kPSlots; ++i) mbar_init(&ctl.rows_seen[i], 4);
+    mbar_init(&ctl.grp, 8);
     mbar_init(&ctl.mma_final, 1);
-    if (rank == 1) {   // the first two pages' probabilities will arrive
-      mbar_arrive_expect_tx(&ctl.p_recv[0], kPMsgBytes);
-      mbar_arrive_expect_tx(&ctl.p_recv[1], kPMsgBytes);
-    }
+    if (rank == 1)     // the first pages' probabilities will arrive
+      for (int i = 0; i < kPSlots; ++i) mbar_arrive_expect_tx(&ctl.p_recv[i], kPMsgBytes);
     fence_mbar_init_cluster();
   }
   if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_pool);
@@ -251,8 +286,11 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
   const int rows = a.T_q * a.H;   // == kRows
   const int cap = a.max_blocks * kPage;
 
-  uint32_t g_prod = 0, g_issue = 0, g_mma = 0, g_sm = 0;   // page counters per role
-  uint32_t it_mma = 0;                                     // items (score MMA)
+  uint32_t g_prod = 0, g_issue = 0;    // producer: cells (score) or units (value) issued
+  uint32_t g_cell = 0;                 // score MMA: cells consumed
+  uint32_t g_step = 0;                 // score CTA: page-pair steps (MMA and softmax)
+  uint32_t g_page = 0;                 // pages (score softmax, value MMA and warps)
+  uint32_t it_cnt = 0;                 // items (MMA issuers, value warps)
   uint32_t grp_phase = 0, n_resc = 0, n_vz = 0;
 
   for (int offset = 0;; offset += kMaxItems) {
@@ -264,10 +302,6 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
       // ============================================================ producer
       // (the whole warp walks the loop; lane 0 issues barriers and copies)
       const uint64_t pol = policy_evict_first();
-      const int nbox = rank == 0 ? 9 : 8;
-      const int stage_bytes = rank == 0 ? kSStageBytes : kVStageBytes;
-      uint64_t* full = rank == 0 ? ctl.stage_full : ctl.v_full;
-      uint64_t* empty = rank == 0 ? ctl.stage_empty : ctl.v_empty;
       for (int ii = 0; ii < n_items; ++ii) {
         if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
         const Item it = ctl.items[ii];
@@ -277,27 +311,61 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
           int blk = -1;
           if (jj < it.j1) blk = a.block_table[(size_t)it.b * a.max_blocks + jj];
           const int nj = min(32, it.j1 - jb);
-          for (int k = 0; k < nj; ++k) {
-            const int bk = __shfl_sync(0xffffffffu, blk, k);
-            if (lane == 0 && !*abort_flag) {
-              const uint32_t st = g_prod & 1;
-              bool ok = true;
-              if (g_prod >= 2) ok = mbar_wait(&empty[st], ((g_prod >> 1) - 1) & 1, abort_flag, kWaitNs);
-              if (!ok) fail(&ctl, a.err);
-              else {
-                const bool valid = bk >= 0 && bk < a.num_blocks;
-                if (!valid && rank == 0) atomicOr(a.err, kErrBadIndex);
+          if (rank == 0) {
+            // page pairs (pairs start at j0, so they never straddle a 32-page chunk)
+            for (int k = 0; k < nj; k += 2) {
+              const bool two = k + 1 < nj;
+              const int bA = __shfl_sync(0xffffffffu, blk, k);
+              const int bB = __shfl_sync(0xffffffffu, blk, two ? k + 1 : k);
+              if (lane == 0) {
+                const bool okA = bA >= 0 && bA < a.num_blocks;
+                const bool okB = bB >= 0 && bB < a.num_blocks;
+                if (!okA || (two && !okB)) atomicOr(a.err, kErrBadIndex);
                 // an invalid block is read past the pool's end: TMA fills zeros
-                const int y = valid ? bk * kPage : a.num_blocks * kPage;
-                uint8_t* dst = stages + st * kSStageBytes;
-                mbar_arrive_expect_tx(&full[st], stage_bytes);
-                for (int bx = 0; bx < nbox; ++bx)
-                  tma_load_2d(dst + bx * kBox, &tm_pool, &full[st], 64 * bx, y, pol);
-                ++g_issue;
+                const int yA = okA ? bA * kPage : a.num_blocks * kPage;
+                const int yB = okB ? bB * kPage : a.num_blocks * kPage;
+                for (int c = 0; c < 9; ++c) {
+                  if (*abort_flag) break;
+                  const uint32_t sl = g_prod % kCells;
+                  if (g_prod >= (uint32_t)kCells &&
+                      !mbar_wait(&ctl.cell_empty[sl], ((g_prod / kCells) - 1) & 1, abort_flag, kWaitNs)) {
+                    fail(&ctl, a.err);
+                    break;
+                  }
+                  uint8_t* dst = smem + kOffCells + sl * kCell;
+                  mbar_arrive_expect_tx(&ctl.cell_full[sl], two ? kCell : kBox);
+                  tma_load_2d(dst, &tm_pool, &ctl.cell_full[sl], 64 * c, yA, pol);
+                  if (two) tma_load_2d(dst + kBox, &tm_pool, &ctl.cell_full[sl], 64 * c, yB, pol);
+                  ++g_prod;
+                  ++g_issue;
+                }
               }
+              __syncwarp();
             }
-            ++g_prod;
-            __syncwarp();
+          } else {
+            for (int k = 0; k < nj; ++k) {
+              const int bk = __shfl_sync(0xffffffffu, blk, k);
+              if (lane == 0) {
+                const bool valid = bk >= 0 && bk < a.num_blocks;
+                const int y = valid ? bk * kPage : a.num_blocks * kPage;
+                for (int nh = 0; nh < 2; ++nh) {
+                  if (*abort_flag) break;
+                  const uint32_t sl = g_prod % kVUnits;
+                  if (g_prod >= (uint32_t)kVUnits &&
+                      !mbar_wait(&ctl.v_empty[sl], ((g_prod / kVUnits) - 1) & 1, abort_flag, kWaitNs)) {
+                    fail(&ctl, a.err);
+                    break;
+                  }
+                  uint8_t* dst = smem + kOffV + sl * kVUnit;
+                  mbar_arrive_expect_tx(&ctl.v_full[sl], kVUnit);
+                  for (int bx = 0; bx < 4; ++bx)
+                    tma_load_2d(dst + bx * kBox, &tm_pool, &ctl.v_full[sl], 64 * (4 * nh + bx), y, pol);
+                  ++g_prod;
+                  ++g_issue;
+                }
+              }
+              __syncwarp();
+            }
           }
         }
       }
@@ -305,28 +373,41 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
       // ============================================================ MMA issuer
       if (lane == 0) {
         if (rank == 0) {
-          const uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);
+          const uint32_t idS2 = idesc_bf16_f32(128, 128, 0, 0);
+          const uint32_t idS1 = idesc_bf16_f32(128, 64, 0, 0);
+          const uint8_t* qr = smem + kOffQr;
           for (int ii = 0; ii < n_items && !*abort_flag; ++ii) {
             const Item it = ctl.items[ii];
-            bool ok = mbar_wait(&ctl.q_ready, it_mma & 1, abort_flag, kWaitNs);
-            for (int i = 0; ok && i < it.j1 - it.j0; ++i) {
-              const uint32_t g = g_mma + i, sb = g % 3;
-              if (g >= 3) ok = mbar_wait(&ctl.s_free[sb], ((g / 3) - 1) & 1, abort_flag, kWaitNs);
-              if (ok) ok = mbar_wait(&ctl.stage_full[g & 1], (g >> 1) & 1, abort_flag, kWaitNs);
-              if (!ok) break;
-              tc_fence_after();
-              const uint8_t* st = stages + (g & 1) * kSStageBytes;
-              for (int kk = 0; kk < 36; ++kk) {   // K = 576: query in TMEM, page in smem
-                const uint64_t bd =
-                    sdesc_sw128(smem_u32(st + (kk >> 2) * kBox + (kk & 3) * 32), 16, 1024);
-                mma_ts(tmem + sb * 64, tmem + kTmemQ + kk * 8, bd, idS, kk > 0);
+            const int n = it.j1 - it.j0;
+            bool ok = mbar_wait(&ctl.q_ready, it_cnt & 1, abort_flag, kWaitNs);
+            for (int k = 0; ok && k < n; k += 2) {
+              const uint32_t sb = g_step & 1;
+              const uint32_t id = (k + 1 < n) ? idS2 : idS1;
+              if (g_step >= 2) ok = mbar_wait(&ctl.s_free[sb], ((g_step >> 1) - 1) & 1, abort_flag, kWaitNs);
+              for (int c = 0; ok && c < 9; ++c) {
+                const uint32_t sl = g_cell % kCells;
+                ok = mbar_wait(&ctl.cell_full[sl], (g_cell / kCells) & 1, abort_flag, kWaitNs);
+                if (!ok) break;
+                tc_fence_after();
+                const uint8_t* cp = smem + kOffCells + sl * kCell;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const int kk = 4 * c + q;
+                  const uint64_t bd = sdesc_sw128(smem_u32(cp + q * 32), 16, 1024);
+                  if (c < 8)
+                    mma_ts(tmem + sb * 128, tmem + kTmemQ + kk * 8, bd, id, kk > 0);
+                  else
+                    mma_ss(tmem + sb * 128, sdesc_sw128(smem_u32(qr + q * 32), 16, 1024), bd, id, 1);
+                }
+                mma_commit(&ctl.cell_empty[sl]);
+                ++g_cell;
               }
+              if (!ok) break;
               mma_commit(&ctl.s_full[sb]);
-              mma_commit(&ctl.stage_empty[g & 1]);
+              ++g_step;
             }
             if (!ok) { fail(&ctl, a.err); break; }
-            g_mma += it.j1 - it.j0;
-            ++it_mma;
+            ++it_cnt;
           }
         } else {
           const uint32_t idPV = idesc_bf16_f32(128, 256, 0, 1);
@@ -335,12 +416,13 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
             const int L = a.seqlens[it.b];
             const int Pb = pages_of(L, a.T_q, cap);
             // the previous item's epilogue must have read O before it is overwritten
-            bool ok = it_mma == 0 || mbar_wait(&ctl.o_free, (it_mma - 1) & 1, abort_flag, kWaitNs);
+            bool ok = it_cnt == 0 || mbar_wait(&ctl.o_free, (it_cnt - 1) & 1, abort_flag, kWaitNs);
             for (int i = 0; ok && i < it.j1 - it.j0; ++i) {
-              const uint32_t g = g_mma + i, slot = g & 1;
+              const uint32_t g = g_page + i, slot = g % kPSlots;
               const int j = it.j0 + i;
-              ok = mbar_wait(&ctl.p_recv[slot], (g >> 1) & 1, abort_flag, kWaitNs);
+              ok = mbar_wait_cluster(&ctl.p_recv[slot], (g / kPSlots) & 1, abort_flag, kWaitNs);
               if (!ok) break;
+              fence_proxy_async_smem();   // the probabilities came in as generic stores
               const uint8_t* ps = pslots + slot * kPSlotBytes;
               const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(ps + kPBytes);
               if ((flags & 1u) && i > 0) {          // rows rescaled by the value warps
@@ -351,58 +433,70 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
                 ok = mbar_wait(&ctl.vz_done, n_vz & 1, abort_flag, kWaitNs);
                 ++n_vz;
               }
-              if (ok) ok = mbar_wait(&ctl.v_full[g & 1], (g >> 1) & 1, abort_flag, kWaitNs);
-              if (!ok) break;
-              tc_fence_after();
-              const uint8_t* vs = stages + (g & 1) * kSStageBytes;
-              for (int nh = 0; nh < 2; ++nh) {
+              for (int nh = 0; ok && nh < 2; ++nh) {
+                const uint32_t u = 2 * g + nh, vs = u % kVUnits;
+                ok = mbar_wait(&ctl.v_full[vs], (u / kVUnits) & 1, abort_flag, kWaitNs);
+                if (!ok) break;
+                tc_fence_after();
+                const uint8_t* vp = smem + kOffV + vs * kVUnit;
+#pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {   // 64 tokens, K-step 16
                   const uint64_t ad = sdesc_sw128(smem_u32(ps + kk * 32), 16, 1024);
-                  const uint64_t bd = sdesc_sw128(smem_u32(vs + nh * 4 * kBox + kk * 2048), kBox, 1024);
+                  const uint64_t bd = sdesc_sw128(smem_u32(vp + kk * 2048), kBox, 1024);
                   mma_ss(tmem + nh * 256, ad, bd, idPV, (i > 0 || kk > 0) ? 1 : 0);
                 }
+                mma_commit(&ctl.v_empty[vs]);
               }
-              mma_commit(&ctl.v_empty[g & 1]);
+              if (!ok) break;
               mma_commit(&ctl.pv_done[slot]);
             }
             if (!ok) { fail(&ctl, a.err); break; }
-            g_mma += it.j1 - it.j0;
-            ++it_mma;
+            g_page += it.j1 - it.j0;
+            ++it_cnt;
           }
         }
       }
       __syncwarp();
     } else if (rank == 0) {
       // ============================================================ softmax (score CTA)
+      // warp w: TMEM lane quarter w & 3 (32 rows); half 0 (warps 2-5) takes the
+      // first page of each pair, half 1 (warps 6-9) the second
       const int q4 = warp & 3;
-      const int half = warp >= 6 ? 1 : 0;          // tokens [32*half, 32*half + 32)
+      const int half = warp >= 6 ? 1 : 0;
       const int r = 32 * q4 + lane;
       const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-      const uint32_t peer_pslots = mapa(smem_u32(pslots), 1);
-      const uint32_t peer_precv0 = mapa(smem_u32(&ctl.p_recv[0]), 1);
-      const uint32_t peer_precv1 = mapa(smem_u32(&ctl.p_recv[1]), 1);
+      const uint32_t peer_p = mapa(smem_u32(pslots), 1);               // value CTA's slots
+      const uint32_t peer_precv = mapa(smem_u32(&ctl.p_recv[0]), 1);   // + 8 * slot
+      const bool leader = threadIdx.x == 64;
       const int t = r / a.H;
+      uint8_t* qr = smem + kOffQr;
       for (int ii = 0; ii < n_items; ++ii) {
         if (__any_sync(0xffffffffu, *abort_flag)) break;
         const Item it = ctl.items[ii];
         const int L = a.seqlens[it.b];
         const int lim = a.causal ? (L - a.T_q + t) : (L - 1);
         const int n = it.j1 - it.j0;
-        // the whole latent query row -> TMEM (A operand of the score MMA);
-        // half 0 writes dims [0, 320), half 1 dims [320, 576)
+        // the query row: latent dims -> TMEM (half 0: [0, 256), half 1: [256, 512)),
+        // rotary dims -> shared memory (K-major SW128; half h: 16-byte chunks 4h..4h+3)
         {
           const uint4* src = reinterpret_cast<const uint4*>(
-              static_cast<const __nv_bfloat16*>(a.q) + ((size_t)it.b * rows + r) * a.D) + half * 40;
-          const int nchunk = half ? 4 : 5;
-          for (int c = 0; c < nchunk; ++c) {
+              static_cast<const __nv_bfloat16*>(a.q) + ((size_t)it.b * rows + r) * a.D);
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
             uint32_t v[32];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              const uint4 x = __ldg(src + c * 8 + u);
+              const uint4 x = __ldg(src + half * 32 + c * 8 + u);
               v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
             }
-            tmem_st32(tmem + lane_off + kTmemQ + half * 160 + 32 * c, v);
+            tmem_st32(tmem + lane_off + kTmemQ + half * 128 + 32 * c, v);
           }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int ch = 4 * half + c;
+            *reinterpret_cast<uint4*>(qr + r * 128 + ((ch ^ (r & 7)) << 4)) = __ldg(src + 64 + ch);
+          }
+          fence_proxy_async_smem();
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
@@ -410,41 +504,49 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
         }
         float m_run = -INFINITY, l_half = 0.f;
         bool ok = true;
-        for (int i = 0; i < n; ++i) {
-          const uint32_t g = g_sm + i, sb = g % 3, slot = g & 1;
-          const int j = it.j0 + i;
-          const bool last = (i == n - 1);
-          const int bk = __ldg(a.block_table + (size_t)it.b * a.max_blocks + j);
-          const bool page_ok = bk >= 0 && bk < a.num_blocks;
-          if (!warp_wait(&ctl.s_full[sb], (g / 3) & 1, abort_flag)) { ok = false; break; }
+        for (int k = 0; k < n; k += 2) {
+          const bool two = k + 1 < n;
+          const bool has = half == 0 || two;           // this half's page exists
+          const uint32_t sb = g_step & 1;
+          const uint32_t gA = g_page, slotA = gA % kPSlots;
+          const int jh = it.j0 + k + half;
+          const bool last_step = k + 2 >= n;
+          int bk = -1;
+          if (has) bk = __ldg(a.block_table + (size_t)it.b * a.max_blocks + jh);
+          const bool page_ok = has && bk >= 0 && bk < a.num_blocks;
+          if (!warp_wait(&ctl.s_full[sb], (g_step >> 1) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          float x[32];
-          tmem_ld32(tmem + lane_off + sb * 64 + 32 * half, x);
+          float x[64];
+          tmem_ld64(tmem + lane_off + sb * 128 + 64 * half, x);
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl.s_free[sb]);     // score buffer reusable
-          // mask (tokens past the visible range, or a page with a bad block id)
-          const int tok0 = j * kPage + 32 * half;
-          if (!page_ok || tok0 + 31 > L - a.T_q) {
+          // mask (tokens past the visible range, a missing page, a bad block id)
+          const int tok0 = jh * kPage;
+          if (!page_ok || tok0 + 63 > L - a.T_q) {
             const int lim_page = page_ok ? lim : -1;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) x[k] = (tok0 + k <= lim_page) ? x[k] : -INFINITY;
+            for (int q = 0; q < 64; ++q) x[q] = (tok0 + q <= lim_page) ? x[q] : -INFINITY;
           }
           float mx = x[0];
 #pragma unroll
-          for (int k = 1; k < 32; ++k) mx = fmaxf(mx, x[k]);
+          for (int q = 1; q < 64; ++q) mx = fmaxf(mx, x[q]);
           ctl.rowx[half][r] = mx;
-          uint8_t* ps = pslots + slot * kPSlotBytes;          // our staging for this page
-          if (threadIdx.x == 64) {
+          if (leader) {
+            // the value CTA must have finished with the pages that last used these slots
             bool fr = true;
-            if (g >= 2) fr = mbar_wait_cluster(&ctl.pfree[slot], ((g >> 1) - 1) & 1, abort_flag, kWaitNs);
+            for (uint32_t e = 0; e < (two ? 2u : 1u) && fr; ++e) {
+              const uint32_t ge = gA + e;
+              if (ge >= (uint32_t)kPSlots)
+                fr = mbar_wait_cluster(&ctl.pfree[ge % kPSlots], ((ge / kPSlots) - 1) & 1, abort_flag, kWaitNs);
+            }
             if (!fr) fail(&ctl, a.err);
-            *reinterpret_cast<uint32_t*>(ps + kPBytes) = 0u;   // header flags
+            bulk_wait_read0();   // the previous step's copies have read the staging
+            ctl.pflags[slotA] = 0u;
           }
           if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { ok = false; break; }   // [A]
-          const float mo = ctl.rowx[half ^ 1][r];
-          const float m_page = fmaxf(mx, mo) * sl2;
+          const float m_page = fmaxf(mx, ctl.rowx[half ^ 1][r]) * sl2;
           const float m_new = fmaxf(m_run, m_page);
           const bool need = m_new > m_run + kRescaleThreshold;
           float alpha = 1.f;
@@ -453,34 +555,36 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
             m_run = m_new;
             l_half *= alpha;
           }
-          // probabilities, rounded to bf16 once; l sums the rounded values
-          uint32_t pk[16];
-          float psum = 0.f;
-          const float neg_m = -m_run;
+          uint8_t* stg = smem + kOffStg + half * kPSlotBytes;   // this half's page message
+          if (has) {
+            // probabilities, rounded to bf16 once; l sums the rounded values.
+            // This row's 128 bytes are staged in the layout the value CTA's
+            // MMA reads (K-major SW128: 16-byte chunk c of row r at c ^ (r & 7)).
+            float psum = 0.f;
+            const float neg_m = -m_run;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float p0 = x[2 * k] == -INFINITY ? 0.f : ex2(fmaf(x[2 * k], sl2, neg_m));
-            const float p1 = x[2 * k + 1] == -INFINITY ? 0.f : ex2(fmaf(x[2 * k + 1], sl2, neg_m));
-            pk[k] = pack_bf16x2(p0, p1);
-            psum += __uint_as_float(lo_half_f(pk[k])) + __uint_as_float(hi_half_f(pk[k]));
-          }
-          l_half += psum;
-          {
-            uint4* prow = reinterpret_cast<uint4*>(ps + r * 128);
+            for (int c = 0; c < 8; ++c) {
+              uint32_t pk[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              prow[(4 * half + c) ^ (r & 7)] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+              for (int e = 0; e < 4; ++e) {
+                const float x0 = x[8 * c + 2 * e], x1 = x[8 * c + 2 * e + 1];
+                const float p0 = x0 == -INFINITY ? 0.f : ex2(fmaf(x0, sl2, neg_m));
+                const float p1 = x1 == -INFINITY ? 0.f : ex2(fmaf(x1, sl2, neg_m));
+                pk[e] = pack_bf16x2(p0, p1);
+                psum += __uint_as_float(lo_half_f(pk[e])) + __uint_as_float(hi_half_f(pk[e]));
+              }
+              *reinterpret_cast<uint4*>(stg + r * 128 + ((c ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            l_half += psum;
           }
-          float* info = reinterpret_cast<float*>(ps + kPBytes + 16);
-          if (half == 0) info[2 * r] = alpha;
-          if (__any_sync(0xffffffffu, need) && i > 0 && lane == 0)
-            atomicOr(reinterpret_cast<uint32_t*>(ps + kPBytes), 1u);
-          if (last) {
+          if (__any_sync(0xffffffffu, need) && k > 0 && lane == 0 && half == 0)
+            atomicOr(&ctl.pflags[slotA], 1u);
+          float l_tot = 0.f;
+          if (last_step) {
             ctl.rowl[half][r] = l_half;
             if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { ok = false; break; }
-            const float l_tot = ctl.rowl[0][r] + ctl.rowl[1][r];
+            l_tot = ctl.rowl[0][r] + ctl.rowl[1][r];
             if (half == 0) {
-              info[2 * r + 1] = l_tot;
               const float lse = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
               const int wslot = it.b + w;
               if (it.flags & 1) { if (a.lse) a.lse[(size_t)it.b * rows + r] = lse; }
@@ -488,123 +592,187 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
               if (r == 0 && it.j0 == 0) a.meta[it.b] = make_int2(it.w_first, it.w_last);
             }
           }
-          fence_proxy_async_smem();
+          // per-row (alpha, l): the rescale factor rides on the pair's first
+          // page; l (the row sum) on the item's last page
+          if (has) {
+            const bool last_page = last_step && half == (two ? 1 : 0);
+            *reinterpret_cast<float2*>(stg + kPBytes + 16 + r * 8) =
+                make_float2(half == 0 ? alpha : 1.f, last_page ? l_tot : 0.f);
+            fence_proxy_async_smem();      // the bulk copy reads the staging
+          }
           if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { ok = false; break; }   // [B]
-          if (threadIdx.x == 64 && !*abort_flag)
-            bulk_copy_to_peer(peer_pslots + slot * kPSlotBytes, ps, kPMsgBytes,
-                              slot ? peer_precv1 : peer_precv0);
+          // headers (flags gathered from all warps of the first page; none on the
+          // second), then one bulk copy per page into the value CTA's slot; the
+          // bytes complete its barrier
+          if (leader) {
+            uint8_t* stg0 = smem + kOffStg;
+            *reinterpret_cast<uint4*>(stg0 + kPBytes) = make_uint4(ctl.pflags[slotA], 0u, 0u, 0u);
+            if (two) *reinterpret_cast<uint4*>(stg0 + kPSlotBytes + kPBytes) = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+            bulk_copy_to_peer(peer_p + slotA * kPSlotBytes, stg0, kPMsgBytes, peer_precv + 8 * slotA);
+            if (two) {
+              const uint32_t slotB = (gA + 1) % kPSlots;
+              bulk_copy_to_peer(peer_p + slotB * kPSlotBytes, stg0 + kPSlotBytes, kPMsgBytes,
+                                peer_precv + 8 * slotB);
+            }
+            bulk_commit();
+          }
+          g_page += two ? 2 : 1;
+          ++g_step;
         }
         if (!ok) { fail(&ctl, a.err); break; }
-        g_sm += n;
       }
-    } else if (warp < 6) {
-      // ============================================================ value CTA rows
+    } else {
+      // ============================================================ value CTA warps
+      // warps 2-5 ("row warps"): page bookkeeping, row rescales, tail zeroing;
+      // all eight: the epilogue, warp w writing rows 32 (w & 3) .. + 31 and
+      // output columns [256 * (w >= 6), + 256)
       const int q4 = warp & 3;
+      const int ch = warp >= 6 ? 1 : 0;
+      const bool row_warp = warp < 6;
       const int r = 32 * q4 + lane;
-      const int tq = threadIdx.x - 64;             // 0..127
+      const int tq = threadIdx.x - 64;             // 0..127 (row warps)
       const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-      const uint32_t peer_pfree0 = mapa(smem_u32(&ctl.pfree[0]), 0);
-      const uint32_t peer_pfree1 = mapa(smem_u32(&ctl.pfree[1]), 0);
+      const uint32_t peer_pfree = mapa(smem_u32(&ctl.pfree[0]), 0);   // + 8 * slot
       for (int ii = 0; ii < n_items; ++ii) {
         if (__any_sync(0xffffffffu, *abort_flag)) break;
         const Item it = ctl.items[ii];
         const int L = a.seqlens[it.b];
         const int Pb = pages_of(L, a.T_q, cap);
         const int n = it.j1 - it.j0;
+        const uint32_t g_last = g_page + n - 1, slot_last = g_last % kPSlots;
         bool ok = true;
-        float l_row = 0.f;
-        for (int i = 0; i < n; ++i) {
-          const uint32_t g = g_sm + i, slot = g & 1;
-          const int j = it.j0 + i;
-          uint8_t* ps = pslots + slot * kPSlotBytes;
-          if (!warp_wait(&ctl.p_recv[slot], (g >> 1) & 1, abort_flag)) { ok = false; break; }
-          const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(ps + kPBytes);
-          const float* info = reinterpret_cast<const float*>(ps + kPBytes + 16);
-          if (j == Pb - 1 && (L & (kPage - 1)) != 0) {
-            // last page: zero the V rows past the sequence end (they may hold NaN)
-            if (!warp_wait(&ctl.v_full[g & 1], (g >> 1) & 1, abort_flag)) { ok = false; break; }
-            const int nv = L & (kPage - 1);
-            uint4* vs = reinterpret_cast<uint4*>(stages + (g & 1) * kSStageBytes);
-            const int per_box = (kPage - nv) * 8;
-            for (int q = tq; q < 8 * per_box; q += kRows) {
-              const int bx = q / per_box, rem = q - bx * per_box;
-              vs[(bx * kBox + (nv + rem / 8) * 128) / 16 + (rem & 7)] = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.vz_done);
-          }
-          if ((flags & 1u) && i > 0) {
-            // rescale O rows before this page's value MMA: O holds pages < j
-            if (!warp_wait(&ctl.pv_done[slot ^ 1], ((g - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            const float alpha = info[2 * r];
-#pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-              float o[64];
-              tmem_ld64(tmem + lane_off + 64 * c, o);
-              tmem_ld_wait();
-              uint32_t u0[32], u1[32];
-#pragma unroll
-              for (int k = 0; k < 32; ++k) {
-                u0[k] = __float_as_uint(o[k] * alpha);
-                u1[k] = __float_as_uint(o[32 + k] * alpha);
+        if (row_warp) {
+          for (int i = 0; i < n; ++i) {
+            const uint32_t g = g_page + i, slot = g % kPSlots;
+            const int j = it.j0 + i;
+            uint8_t* ps = pslots + slot * kPSlotBytes;
+            if (!warp_wait_cluster(&ctl.p_recv[slot], (g / kPSlots) & 1, abort_flag)) { ok = false; break; }
+            const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(ps + kPBytes);
+            const float* info = reinterpret_cast<const float*>(ps + kPBytes + 16);
+            if (j == Pb - 1 && (L & (kPage - 1)) != 0) {
+              // last page: zero the V rows past the sequence end (they may hold NaN)
+              const int nv = L & (kPage - 1);
+              const int per_box = (kPage - nv) * 8;    // 16-byte chunks per box
+              for (int nh = 0; nh < 2 && ok; ++nh) {
+                const uint32_t u = 2 * g + nh, vs = u % kVUnits;
+                if (!warp_wait(&ctl.v_full[vs], (u / kVUnits) & 1, abort_flag)) { ok = false; break; }
+                uint4* vp = reinterpret_cast<uint4*>(smem + kOffV + vs * kVUnit);
+                for (int q = tq; q < 4 * per_box; q += kRows) {
+                  const int bx = q / per_box, rem = q - bx * per_box;
+                  vp[(bx * kBox + (nv + rem / 8) * 128) / 16 + (rem & 7)] = make_uint4(0, 0, 0, 0);
+                }
               }
-              tmem_st32(tmem + lane_off + 64 * c, u0);
-              tmem_st32(tmem + lane_off + 64 * c + 32, u1);
+              if (!ok) break;
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&ctl.vz_done);
             }
-            tmem_st_wait();
-            tc_fence_before();
+            if ((flags & 1u) && i > 0) {
+              // rescale O rows before this page's value MMA: O holds pages < j
+              if (!warp_wait(&ctl.pv_done[(g - 1) % kPSlots], ((g - 1) / kPSlots) & 1, abort_flag)) { ok = false; break; }
+              tc_fence_after();
+              const float alpha = info[2 * r];
+#pragma unroll 1
+              for (int c = 0; c < 8; ++c) {
+                float o[64];
+                tmem_ld64(tmem + lane_off + 64 * c, o);
+                tmem_ld_wait();
+                uint32_t u0[32], u1[32];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                  u0[q] = __float_as_uint(o[q] * alpha);
+                  u1[q] = __float_as_uint(o[32 + q] * alpha);
+                }
+                tmem_st32(tmem + lane_off + 64 * c, u0);
+                tmem_st32(tmem + lane_off + 64 * c + 32, u1);
+              }
+              tmem_st_wait();
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&ctl.resc_done);
+            }
+            // header and factors read by this warp (one barrier per slot: a warp
+            // may run up to three pages ahead of the releasing warp, never four,
+            // since page g + 4 arrives only after slot g is released)
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.resc_done);
-          }
-          if (i == n - 1) l_row = info[2 * r + 1];
-          // this page's value MMA done: the slot may be refilled (the last
-          // page's slot is released after the epilogue, which reuses it)
-          if (!warp_wait(&ctl.pv_done[slot], (g >> 1) & 1, abort_flag)) { ok = false; break; }
-          if (i < n - 1 && threadIdx.x == 64) {
-            mbar_arrive_expect_tx(&ctl.p_recv[slot], kPMsgBytes);
-            mbar_arrive_remote(slot ? peer_pfree1 : peer_pfree0);
+            if (lane == 0) mbar_arrive(&ctl.rows_seen[slot]);
+            // this page's value MMA done
+            if (!warp_wait(&ctl.pv_done[slot], (g / kPSlots) & 1, abort_flag)) { ok = false; break; }
+            if (i < n - 1) {
+              // the slot may be refilled once every row warp is past its header
+              if (threadIdx.x == 64) {
+                if (mbar_wait(&ctl.rows_seen[slot], (g / kPSlots) & 1, abort_flag, kWaitNs)) {
+                  mbar_arrive_expect_tx(&ctl.p_recv[slot], kPMsgBytes);
+                  mbar_arrive_remote(peer_pfree + 8 * slot);
+                } else {
+                  fail(&ctl, a.err);
+                }
+              }
+              __syncwarp();
+            } else {
+              // O is final; the last page's slot becomes the epilogue staging
+              // buffer and is handed back only after the epilogue
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&ctl.epi_go);
+            }
           }
         }
+        if (ok && !warp_wait(&ctl.epi_go, it_cnt & 1, abort_flag)) ok = false;
         if (!ok) { fail(&ctl, a.err); break; }
-        const uint32_t g_last = g_sm + n - 1, slot = g_last & 1;
-        g_sm += n;
-        // ---- epilogue: normalise and write the item's 128 x 512 output,
-        // staged through the last page's slot for coalesced row writes
+        // ---- epilogue: normalise and write the item's 128 x 512 output, each
+        // warp staging 32 rows x 16 columns at a time for full-sector writes
         tc_fence_after();
+        uint8_t* ps_last = pslots + slot_last * kPSlotBytes;
+        const float l_row = reinterpret_cast<const float*>(ps_last + kPBytes + 16)[2 * r + 1];
         const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
         const bool whole = it.flags & 1;
-        float* out_base = whole ? a.o + (size_t)it.b * rows * a.d_c
-                                : a.ws_o + (size_t)(it.b + w) * rows * a.d_c;
-        float4* stage_o = reinterpret_cast<float4*>(pslots + slot * kPSlotBytes);
-        if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { fail(&ctl, a.err); break; }  // l read
+        float* out_base = (whole ? a.o + (size_t)it.b * rows * a.d_c
+                                 : a.ws_o + (size_t)(it.b + w) * rows * a.d_c) +
+                          (size_t)(32 * q4) * a.d_c + 256 * ch;
+        float4* stg = reinterpret_cast<float4*>(ps_last + (warp - 2) * 2048);   // 32 rows x 4 float4
+        // every thread must have read l before the staging writes below
+        __syncwarp();
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
           float o[64];
-          tmem_ld64(tmem + lane_off + 64 * c, o);
+          tmem_ld64(tmem + lane_off + 256 * ch + 64 * c, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
-            stage_o[r * 16 + (k ^ (r & 7))] =
-                make_float4(o[4 * k] * inv, o[4 * k + 1] * inv, o[4 * k + 2] * inv, o[4 * k + 3] * inv);
-          if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { ok = false; break; }
-#pragma unroll 4
-          for (int idx = tq; idx < kRows * 16; idx += kRows) {
-            const int row = idx >> 4, c16 = idx & 15;
-            reinterpret_cast<float4*>(out_base + (size_t)row * a.d_c + 64 * c)[c16] =
-                stage_o[row * 16 + (c16 ^ (row & 7))];
+          for (int sr = 0; sr < 4; ++sr) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              stg[lane * 4 + (e ^ ((lane >> 1) & 3))] =
+                  make_float4(o[16 * sr + 4 * e] * inv, o[16 * sr + 4 * e + 1] * inv,
+                              o[16 * sr + 4 * e + 2] * inv, o[16 * sr + 4 * e + 3] * inv);
+            __syncwarp();
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt) {
+              const int row = lane / 4 + 8 * tt, e = lane & 3;
+              reinterpret_cast<float4*>(out_base + (size_t)row * a.d_c + 64 * c + 16 * sr)[e] =
+                  stg[row * 4 + (e ^ ((row >> 1) & 3))];
+            }
+            __syncwarp();
           }
-          if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { ok = false; break; }
         }
-        if (!ok) { fail(&ctl, a.err); break; }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.o_free);      // O may be overwritten now
-        if (threadIdx.x == 64) {
-          mbar_arrive_expect_tx(&ctl.p_recv[slot], kPMsgBytes);
-          mbar_arrive_remote(slot ? peer_pfree1 : peer_pfree0);
+        if (lane == 0) {
+          mbar_arrive(&ctl.o_free);      // O may be overwritten now
+          mbar_arrive(&ctl.epi_done);
         }
+        if (threadIdx.x == 64) {
+          // hand the staging slot back once every epilogue warp is done with it
+          if (mbar_wait(&ctl.epi_done, it_cnt & 1, abort_flag, kWaitNs)) {
+            mbar_arrive_expect_tx(&ctl.p_recv[slot_last], kPMsgBytes);
+            mbar_arrive_remote(peer_pfree + 8 * slot_last);
+          } else {
+            fail(&ctl, a.err);
+          }
+        }
+        __syncwarp();
+        g_page += n;
+        ++it_cnt;
       }
     }
     __syncthreads();
@@ -612,16 +780,18 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
     if (offset + kMaxItems >= ctl.n_total) break;
   }
 
-  // ---- drain: all MMAs complete, all TMA loads landed, then free TMEM
+  // ---- drain: all MMAs complete, all TMA loads and bulk copies done, then free TMEM
+  if (rank == 0 && threadIdx.x == 64) bulk_wait0();
   if (warp == 1 && lane == 0) {
     mma_commit(&ctl.mma_final);
     if (!mbar_wait(&ctl.mma_final, 0, &ctl.never, kWaitNs)) atomicOr(a.err, kErrTimeout);
   }
   if (warp == 0 && lane == 0) {
-    uint64_t* full = rank == 0 ? ctl.stage_full : ctl.v_full;
-    for (uint32_t k = 0; k < 2u && k < g_issue; ++k) {
+    const uint32_t nring = rank == 0 ? kCells : kVUnits;
+    uint64_t* full = rank == 0 ? ctl.cell_full : ctl.v_full;
+    for (uint32_t k = 0; k < nring && k < g_issue; ++k) {
       const uint32_t g = g_issue - 1 - k;
-      if (!mbar_wait(&full[g & 1], (g >> 1) & 1, &ctl.never, kWaitNs)) atomicOr(a.err, kErrTimeout);
+      if (!mbar_wait(&full[g % nring], (g / nring) & 1, &ctl.never, kWaitNs)) atomicOr(a.err, kErrTimeout);
     }
   }
   tc_fence_before();

@@ -159,12 +159,37 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const vo
       "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
       : "memory");
 }
+// bulk-copy groups of this thread: close the current group; wait until at
+// most 0 groups are still reading their source / have not completed
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 __device__ __forceinline__ void st_async_v4u(uint32_t addr, uint4 v, uint32_t remote_bar) {
   asm volatile(
       "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
           addr),
       "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
       : "memory");
+}
+// plain (weak) 16- and 8-byte stores into a peer CTA's shared memory
+__device__ __forceinline__ void st_cluster_v4u(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_v2f(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+// order this thread's generic-proxy writes to cluster shared memory before
+// later async-proxy reads of it (tensor-core operands)
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 __device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uint32_t remote_bar) {
   asm volatile(
