@@ -104,7 +104,10 @@ def profiled_traffic(kernel_file: str, workload: str):
 
 class ClockSampler:
     """Samples the SM clock and the clock-event reasons of one GPU in the
-    background (NVML if importable, else `nvidia-smi -lms`)."""
+    background (NVML if importable, else `nvidia-smi -lms`), timestamping
+    every sample on the host clock.  `mark(start|end)` brackets the timed
+    region; the summary keeps the samples inside it (the nearest ones when the
+    region is shorter than the sampling period, flagged as such)."""
     REASONS = {  # NVML clocks-event reason bits
         0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
         0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
@@ -112,10 +115,13 @@ class ClockSampler:
     SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                   "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                   "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    SMI_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, device_index: int, period_s: float = 0.01):
+    def __init__(self, device_index: int, period_s: float = 0.005):
         self.dev, self.period = device_index, period_s
-        self.samples, self.reasons, self.max_mhz, self.err = [], set(), None, None
+        self.samples = []          # (host time, sm MHz, set of reasons)
+        self.max_mhz, self.err = None, None
+        self.t_start = self.t_end = None
         self._stop = threading.Event()
         self.mode = None
         try:
@@ -134,12 +140,25 @@ class ClockSampler:
         nv = self.nv
         while not self._stop.is_set():
             try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
                 bits = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                self.reasons.update(n for b, n in self.REASONS.items() if bits & b)
+                self.samples.append((time.monotonic(), float(mhz),
+                                     {n for b, n in self.REASONS.items() if bits & b}))
             except Exception:  # noqa: BLE001
                 pass
             time.sleep(self.period)
+
+    def _read_smi(self):
+        for line in self.proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                mhz, self.max_mhz = float(f[0]), float(f[1])
+            except ValueError:
+                continue
+            self.samples.append((time.monotonic(), mhz,
+                                 {n for n, v in zip(self.SMI_REASONS, f[4:8]) if v.lower() == "active"}))
 
     def __enter__(self):
         if self.mode == "nvml":
@@ -148,37 +167,51 @@ class ClockSampler:
         elif self.mode == "nvidia-smi":
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.SMI_FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", str(int(self.period * 1000))],
+                 "--format=csv,noheader,nounits", "-lms", str(max(1, int(self.period * 1000)))],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read_smi, daemon=True)
+            self.t.start()
+        # the sampler is live before the timed region starts
+        t0 = time.monotonic()
+        while self.mode and not self.samples and time.monotonic() - t0 < 5.0:
+            time.sleep(0.01)
         return self
 
+    def mark(self, which: str):
+        if which == "start":
+            self.t_start = time.monotonic()
+        else:
+            self.t_end = time.monotonic()
+
     def __exit__(self, *a):
+        time.sleep(2 * self.period)
         if self.mode == "nvml":
             self._stop.set()
             self.t.join()
         elif self.mode == "nvidia-smi":
             self.proc.terminate()
-            out, _ = self.proc.communicate(timeout=10)
-            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-            for line in out.splitlines():
-                f = [x.strip() for x in line.split(",")]
-                if len(f) < 8:
-                    continue
-                try:
-                    self.samples.append(float(f[0]))
-                    self.max_mhz = float(f[1])
-                except ValueError:
-                    continue
-                for name, v in zip(names, f[4:8]):
-                    if v.lower() == "active":
-                        self.reasons.add(name)
+            try:
+                self.proc.wait(timeout=10)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=5)
 
     def summary(self):
         if self.mode is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.err}
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples), "source": self.mode}
+        inside = [x for x in self.samples
+                  if self.t_start is not None and self.t_start <= x[0] <= (self.t_end or x[0])]
+        where = "timed region"
+        if not inside and self.samples and self.t_start is not None:
+            mid = 0.5 * (self.t_start + (self.t_end or self.t_start))
+            inside = sorted(self.samples, key=lambda x: abs(x[0] - mid))[:2]
+            where = "nearest to the timed region (shorter than the sampling period)"
+        reasons = set()
+        for x in inside:
+            reasons |= x[2]
+        return {"sm_mhz": statistics.median(x[1] for x in inside) if inside else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(inside), "window": where, "source": self.mode}
 
 
 # --------------------------------------------------------------------------
@@ -343,11 +376,13 @@ def run_mla(args, spec):
     barrier(dist, local)
     torch.cuda.synchronize(dev)
     with sampler:
+        sampler.mark("start")
         ev0.record(stream)
         for i in range(args.steps):
             step(i)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
+        sampler.mark("end")
     barrier(dist, local)
     ms = ev0.elapsed_time(ev1)
     ms_max = max_over_ranks(dist, ms)

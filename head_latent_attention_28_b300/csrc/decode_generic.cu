@@ -249,47 +249,114 @@ __global__ void __launch_bounds__(GT) decode_generic_kernel(DecodeArgs a) {
   }
 }
 
-constexpr int CT = 128;  // combine threads
+constexpr int CT = 256;  // combine threads
 constexpr int CR = 4;    // rows per combine CTA
 
 // Merge the partial softmax results of sequences split across workers:
 // lse* = max_i lse_i, w_i = exp(lse_i - lse*) (0 for an empty part),
 // o = sum_i w_i o_i / sum_i w_i, lse = lse* + ln sum_i w_i.
+// The normalised weights of the CTA's rows are computed once into shared
+// memory; the output is then a weighted sum of VEC-wide column groups
+// (float4 when d_c and the output allow it; coalesced either way).
 // Sequences with an invalid length get zero outputs here.
+template <int VEC>
+struct VecT { using T = float; };
+template <>
+struct VecT<4> { using T = float4; };
+__device__ __forceinline__ void fma_vec(float w, float v, float& acc) { acc = fmaf(w, v, acc); }
+__device__ __forceinline__ void fma_vec(float w, const float4& v, float4& acc) {
+  acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
+  acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
+}
+__device__ __forceinline__ void zero_vec(float& v) { v = 0.f; }
+__device__ __forceinline__ void zero_vec(float4& v) { v = make_float4(0.f, 0.f, 0.f, 0.f); }
+
+template <int VEC>
 __global__ void __launch_bounds__(CT) combine_kernel(DecodeArgs a) {
+  using V = typename VecT<VEC>::T;
+  // launched as a programmatic dependent of the partial pass: wait until that
+  // grid has completed and its writes are visible (no-op otherwise)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  extern __shared__ float wts[];            // [CR][nw] normalised weights
   const int b = blockIdx.x;
   const int rows = a.T_q * a.H;
+  const int r0 = blockIdx.y * CR;
+  const int nr = min(CR, rows - r0);
   const int L = a.seqlens[b];
   const bool valid = L >= a.T_q && L <= a.max_blocks * kPage;
-  int2 m = make_int2(0, 0);
-  if (valid) m = a.meta[b];
-  if (valid && m.x == m.y) return;  // finished by its only worker
-  for (int r = blockIdx.y * CR; r < min(rows, (blockIdx.y + 1) * CR); ++r) {
-    const size_t orow = ((size_t)b * rows + r) * a.d_c;
-    if (!valid) {
-      for (int c = threadIdx.x; c < a.d_c; c += CT) a.o[orow + c] = 0.f;
-      if (threadIdx.x == 0 && a.lse) a.lse[(size_t)b * rows + r] = 0.f;
-      continue;
+  const int dc4 = a.d_c / VEC;
+  if (!valid) {
+    V z;
+    zero_vec(z);
+    for (int idx = threadIdx.x; idx < nr * dc4; idx += CT) {
+      const int rr = idx / dc4, c4 = idx - rr * dc4;
+      reinterpret_cast<V*>(a.o + ((size_t)b * rows + r0 + rr) * a.d_c)[c4] = z;
     }
+    if (threadIdx.x < nr && a.lse) a.lse[(size_t)b * rows + r0 + threadIdx.x] = 0.f;
+    return;
+  }
+  const int2 m = a.meta[b];
+  if (m.x == m.y) return;  // finished by its only worker
+  const int nw = m.y - m.x + 1;
+  // weights: one warp per row
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int rr = warp; rr < nr; rr += CT / 32) {
+    const int r = r0 + rr;
     float lmax = -INFINITY;
-    for (int w = m.x; w <= m.y; ++w) lmax = fmaxf(lmax, a.ws_lse[(size_t)(b + w) * rows + r]);
+    for (int k = lane; k < nw; k += 32) lmax = fmaxf(lmax, a.ws_lse[(size_t)(b + m.x + k) * rows + r]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
     float sumw = 0.f;
-    for (int w = m.x; w <= m.y; ++w) {
-      float lw = a.ws_lse[(size_t)(b + w) * rows + r];
-      sumw += (lw == -INFINITY) ? 0.f : expf(lw - lmax);
+    for (int k = lane; k < nw; k += 32) {
+      const float lw = a.ws_lse[(size_t)(b + m.x + k) * rows + r];
+      const float wt = (lw == -INFINITY) ? 0.f : expf(lw - lmax);
+      wts[rr * nw + k] = wt;
+      sumw += wt;
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sumw += __shfl_xor_sync(0xffffffffu, sumw, o);
     const float inv = sumw > 0.f ? 1.f / sumw : 0.f;
-    for (int c = threadIdx.x; c < a.d_c; c += CT) {
-      float acc = 0.f;
-      for (int w = m.x; w <= m.y; ++w) {
-        float lw = a.ws_lse[(size_t)(b + w) * rows + r];
-        float wt = (lw == -INFINITY) ? 0.f : expf(lw - lmax);
-        acc = fmaf(wt, a.ws_o[((size_t)(b + w) * rows + r) * a.d_c + c], acc);
-      }
-      a.o[orow + c] = acc * inv;
+    __syncwarp();
+    for (int k = lane; k < nw; k += 32) wts[rr * nw + k] *= inv;
+    if (lane == 0 && a.lse) a.lse[(size_t)b * rows + r] = sumw > 0.f ? lmax + logf(sumw) : -INFINITY;
+  }
+  __syncthreads();
+  // each thread keeps kOut outputs in registers and issues the loads of up
+  // to kParts parts for all of them together (the parts are L2-resident:
+  // this kernel is latency-bound, so loads in flight decide its time)
+  constexpr int kOut = 2, kParts = 4;
+  const int total = nr * dc4;
+  for (int base = threadIdx.x; base < total; base += CT * kOut) {
+    V acc[kOut];
+    int off[kOut], wrow[kOut];
+#pragma unroll
+    for (int t = 0; t < kOut; ++t) {
+      zero_vec(acc[t]);
+      const int idx = min(base + t * CT, total - 1);
+      const int rr = idx / dc4, c4 = idx - rr * dc4;
+      off[t] = (r0 + rr) * dc4 + c4;   // V index within a [rows, d_c] slab
+      wrow[t] = rr * nw;
     }
-    if (threadIdx.x == 0 && a.lse)
-      a.lse[(size_t)b * rows + r] = sumw > 0.f ? lmax + logf(sumw) : -INFINITY;
+    for (int k0 = 0; k0 < nw; k0 += kParts) {
+      V v[kParts][kOut];
+#pragma unroll
+      for (int kk = 0; kk < kParts; ++kk) {
+        const int k = min(k0 + kk, nw - 1);
+        const V* part = reinterpret_cast<const V*>(a.ws_o + (size_t)(b + m.x + k) * rows * a.d_c);
+#pragma unroll
+        for (int t = 0; t < kOut; ++t) v[kk][t] = part[off[t]];
+      }
+#pragma unroll
+      for (int kk = 0; kk < kParts; ++kk)
+        if (k0 + kk < nw) {
+#pragma unroll
+          for (int t = 0; t < kOut; ++t) fma_vec(wts[wrow[t] + k0 + kk], v[kk][t], acc[t]);
+        }
+    }
+    V* out = reinterpret_cast<V*>(a.o + (size_t)b * rows * a.d_c);
+#pragma unroll
+    for (int t = 0; t < kOut; ++t)
+      if (base + t * CT < total) out[off[t]] = acc[t];
   }
 }
 
@@ -323,8 +390,26 @@ cudaError_t launch_decode_generic(const DecodeArgs& a, cudaStream_t s) {
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s) {
   const int rows = a.T_q * a.H;
   dim3 grid(a.B, (rows + CR - 1) / CR);
-  combine_kernel<<<grid, CT, 0, s>>>(a);
-  return cudaGetLastError();
+  // a sequence's parts come from at most W workers
+  const size_t smem = sizeof(float) * (size_t)CR * (size_t)(a.W > 0 ? a.W : 1);
+  const bool vec4 = a.d_c % 4 == 0 && (reinterpret_cast<uintptr_t>(a.o) & 15u) == 0 &&
+                    (reinterpret_cast<uintptr_t>(a.ws_o) & 15u) == 0;
+  auto kern = vec4 ? combine_kernel<4> : combine_kernel<1>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(CT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace mla

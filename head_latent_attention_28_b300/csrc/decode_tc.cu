@@ -780,6 +780,8 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
     if (offset + kMaxItems >= ctl.n_total) break;
   }
 
+  // the merge pass may start launching now (it waits for this grid's completion)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // ---- drain: all MMAs complete, all TMA loads and bulk copies done, then free TMEM
   if (rank == 0 && threadIdx.x == 64) bulk_wait0();
   if (warp == 1 && lane == 0) {
