@@ -49,19 +49,20 @@ constexpr int kThreads = 320;            // 10 warps
 constexpr int kRows = 128;               // query rows per sequence handled here
 constexpr int kBox = 8192;               // 64 tokens x 64 dims x bf16
 constexpr int kCell = 2 * kBox;          // score CTA: box c of both pages of a pair
-constexpr int kCells = 10;               // score CTA: ring depth (cells)
+constexpr int kCells = 8;                // score CTA: ring depth (cells)
 constexpr int kVUnit = 4 * kBox;         // value CTA: 256 latent dims of one page
-constexpr int kVUnits = 4;               // value CTA: ring depth (half pages)
+constexpr int kVUnits = 3;               // value CTA: ring depth (half pages)
 constexpr int kPBytes = kRows * 64 * 2;  // bf16 probabilities of one page (K-major, SW128)
 constexpr int kInfoBytes = 16 + kRows * 8;       // header + (alpha, l) per row
 constexpr int kPMsgBytes = kPBytes + kInfoBytes; // bytes delivered per page (one bulk copy)
-constexpr int kPSlotBytes = 18432;
-constexpr int kPSlots = 4;               // probability slots (pages)
+constexpr int kLoOff = 18432;            // low bf16 parts of a page's probabilities (when sent)
+constexpr int kPSlotBytes = kLoOff + kPBytes;
+constexpr int kPSlots = 3;               // probability slots (pages)
 // shared-memory map (offsets from the 1 KB aligned base)
 constexpr int kOffQr = 0;                // score CTA: rotary query, 128 x 64 bf16 (K-major SW128)
 constexpr int kOffStg = 16384;           // score CTA: the step's two outgoing page messages
-constexpr int kOffCells = kOffStg + 2 * kPSlotBytes;   // score CTA: 10 cells
-constexpr int kOffV = 0;                 // value CTA: 4 half-page units
+constexpr int kOffCells = kOffStg + 2 * kPSlotBytes;   // score CTA: 8 cells
+constexpr int kOffV = 0;                 // value CTA: 3 half-page units
 constexpr int kOffP = kVUnits * kVUnit;  // value CTA: probability slots (score CTA writes them)
 constexpr int kScoreSmem = kOffCells + kCells * kCell;
 constexpr int kValueSmem = kOffP + kPSlots * kPSlotBytes;
@@ -72,6 +73,9 @@ constexpr uint32_t kTmemQ = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+// header flag bits of a page message
+constexpr uint32_t kFlagRescale = 1u;    // rows rescaled before this page's value MMA
+constexpr uint32_t kFlagLo = 2u;         // the low bf16 parts of the probabilities follow
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 static_assert(kPMsgBytes <= kPSlotBytes, "probability slot too small");
@@ -79,6 +83,7 @@ static_assert(kPMsgBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
 static_assert(kOffCells % 1024 == 0, "SW128 operands need 1 KB alignment");
 static_assert(kOffP % 1024 == 0 && kPSlotBytes % 1024 == 0, "SW128 operands need 1 KB alignment");
 static_assert(8 * 2048 <= kPBytes, "epilogue staging lives in a probability slot");
+static_assert(kLoOff >= kPMsgBytes && kLoOff % 1024 == 0, "low parts after the header, SW128-aligned");
 
 struct Item {
   int b, j0, j1;            // sequence, page range [j0, j1)
@@ -94,6 +99,7 @@ struct SmemCtl {
   // value CTA
   uint64_t v_full[kVUnits], v_empty[kVUnits];
   uint64_t p_recv[kPSlots], pv_done[kPSlots];
+  uint64_t lo_recv[kPSlots];   // the low parts of a slot's probabilities arrived (armed on demand)
   uint64_t resc_done, vz_done;
   uint64_t o_free;          // the epilogue has read O: the next item may overwrite it
   uint64_t epi_go;          // O of the item is final (value row warps -> other warps)
@@ -108,7 +114,10 @@ struct SmemCtl {
   int scan[kThreads / 32];
   float rowx[2][kRows];     // score CTA: per-half row maxima of a step
   float rowl[2][kRows];     // score CTA: per-half row sums (last step of an item)
-  uint32_t pflags[kPSlots]; // score CTA: header flags of the page in flight per slot
+  // score CTA: header flags of a page, indexed by page mod 2 x slots: a word
+  // is reset by the leader after the step that sent it and written again three
+  // steps later, so the two never race
+  uint32_t pflags[2 * kPSlots];
   Item items[kMaxItems];
 };
 
@@ -258,7 +267,9 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
       mbar_init(&ctl.pfree[i], 1);
       mbar_init(&ctl.p_recv[i], 1);
       mbar_init(&ctl.pv_done[i], 1);
-      ctl.pflags[i] = 0;
+      mbar_init(&ctl.lo_recv[i], 1);
+      ctl.pflags[2 * i] = 0;
+      ctl.pflags[2 * i + 1] = 0;
     }
     mbar_init(&ctl.q_ready, 8);
     mbar_init(&ctl.resc_done, 4);
@@ -411,6 +422,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
           }
         } else {
           const uint32_t idPV = idesc_bf16_f32(128, 256, 0, 1);
+          uint32_t lo_par = 0;   // per slot: parity of the next low-parts phase
           for (int ii = 0; ii < n_items && !*abort_flag; ++ii) {
             const Item it = ctl.items[ii];
             const int L = a.seqlens[it.b];
@@ -433,6 +445,15 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
                 ok = mbar_wait(&ctl.vz_done, n_vz & 1, abort_flag, kWaitNs);
                 ++n_vz;
               }
+              const bool lo = (flags & kFlagLo) != 0;
+              if (ok && lo) {
+                // the low parts may already be here (the count then goes below
+                // zero until this expectation is added)
+                mbar_arrive_expect_tx(&ctl.lo_recv[slot], kPBytes);
+                ok = mbar_wait_cluster(&ctl.lo_recv[slot], (lo_par >> slot) & 1, abort_flag, kWaitNs);
+                lo_par ^= 1u << slot;
+                fence_proxy_async_smem();
+              }
               for (int nh = 0; ok && nh < 2; ++nh) {
                 const uint32_t u = 2 * g + nh, vs = u % kVUnits;
                 ok = mbar_wait(&ctl.v_full[vs], (u / kVUnits) & 1, abort_flag, kWaitNs);
@@ -444,6 +465,14 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
                   const uint64_t ad = sdesc_sw128(smem_u32(ps + kk * 32), 16, 1024);
                   const uint64_t bd = sdesc_sw128(smem_u32(vp + kk * 2048), kBox, 1024);
                   mma_ss(tmem + nh * 256, ad, bd, idPV, (i > 0 || kk > 0) ? 1 : 0);
+                }
+                if (lo) {
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk) {   // the same V rows, A = low parts
+                    const uint64_t ad = sdesc_sw128(smem_u32(ps + kLoOff + kk * 32), 16, 1024);
+                    const uint64_t bd = sdesc_sw128(smem_u32(vp + kk * 2048), kBox, 1024);
+                    mma_ss(tmem + nh * 256, ad, bd, idPV, 1);
+                  }
                 }
                 mma_commit(&ctl.v_empty[vs]);
               }
@@ -467,6 +496,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
       const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
       const uint32_t peer_p = mapa(smem_u32(pslots), 1);               // value CTA's slots
       const uint32_t peer_precv = mapa(smem_u32(&ctl.p_recv[0]), 1);   // + 8 * slot
+      const uint32_t peer_lorecv = mapa(smem_u32(&ctl.lo_recv[0]), 1); // + 8 * slot
       const bool leader = threadIdx.x == 64;
       const int t = r / a.H;
       uint8_t* qr = smem + kOffQr;
@@ -508,7 +538,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
           const bool two = k + 1 < n;
           const bool has = half == 0 || two;           // this half's page exists
           const uint32_t sb = g_step & 1;
-          const uint32_t gA = g_page, slotA = gA % kPSlots;
+          const uint32_t gA = g_page;
           const int jh = it.j0 + k + half;
           const bool last_step = k + 2 >= n;
           int bk = -1;
@@ -533,6 +563,17 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
 #pragma unroll
           for (int q = 1; q < 64; ++q) mx = fmaxf(mx, x[q]);
           ctl.rowx[half][r] = mx;
+          const uint32_t fh = (gA + half) % (2 * kPSlots);   // this half's page flags
+          {
+            // Precision of the bf16 probabilities: a page whose largest
+            // probability is not small against the row sum so far also sends
+            // the low bf16 parts (p - bf16(p)).  Tested conservatively, before
+            // the rows' maxima are merged: against this half's own running sum
+            // and the previous reference (both can only make the test pass more
+            // often than with the merged values).
+            const bool heavy = has && ex2(mx * sl2 - m_run) >= l_half;
+            if (__any_sync(0xffffffffu, heavy) && lane == 0) atomicOr(&ctl.pflags[fh], kFlagLo);
+          }
           if (leader) {
             // the value CTA must have finished with the pages that last used these slots
             bool fr = true;
@@ -543,7 +584,6 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
             }
             if (!fr) fail(&ctl, a.err);
             bulk_wait_read0();   // the previous step's copies have read the staging
-            ctl.pflags[slotA] = 0u;
           }
           if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { ok = false; break; }   // [A]
           const float m_page = fmaxf(mx, ctl.rowx[half ^ 1][r]) * sl2;
@@ -557,28 +597,37 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
           }
           uint8_t* stg = smem + kOffStg + half * kPSlotBytes;   // this half's page message
           if (has) {
-            // probabilities, rounded to bf16 once; l sums the rounded values.
-            // This row's 128 bytes are staged in the layout the value CTA's
-            // MMA reads (K-major SW128: 16-byte chunk c of row r at c ^ (r & 7)).
+            // probabilities, rounded to bf16 (and, for a heavy page, the
+            // residual rounded again); l sums exactly what the value MMA sees.
+            // Rows are staged in the layout the value CTA's MMA reads
+            // (K-major SW128: 16-byte chunk c of row r at c ^ (r & 7)).
+            const bool lo = (ctl.pflags[fh] & kFlagLo) != 0;
             float psum = 0.f;
             const float neg_m = -m_run;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-              uint32_t pk[4];
+              uint32_t pk[4], pl[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const float x0 = x[8 * c + 2 * e], x1 = x[8 * c + 2 * e + 1];
                 const float p0 = x0 == -INFINITY ? 0.f : ex2(fmaf(x0, sl2, neg_m));
                 const float p1 = x1 == -INFINITY ? 0.f : ex2(fmaf(x1, sl2, neg_m));
                 pk[e] = pack_bf16x2(p0, p1);
-                psum += __uint_as_float(lo_half_f(pk[e])) + __uint_as_float(hi_half_f(pk[e]));
+                const float h0 = __uint_as_float(lo_half_f(pk[e])), h1 = __uint_as_float(hi_half_f(pk[e]));
+                psum += h0 + h1;
+                if (lo) {
+                  pl[e] = pack_bf16x2(p0 - h0, p1 - h1);
+                  psum += __uint_as_float(lo_half_f(pl[e])) + __uint_as_float(hi_half_f(pl[e]));
+                }
               }
-              *reinterpret_cast<uint4*>(stg + r * 128 + ((c ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              const int off = r * 128 + ((c ^ (r & 7)) << 4);
+              *reinterpret_cast<uint4*>(stg + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              if (lo) *reinterpret_cast<uint4*>(stg + kLoOff + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
             }
             l_half += psum;
           }
           if (__any_sync(0xffffffffu, need) && k > 0 && lane == 0 && half == 0)
-            atomicOr(&ctl.pflags[slotA], 1u);
+            atomicOr(&ctl.pflags[gA % (2 * kPSlots)], kFlagRescale);
           float l_tot = 0.f;
           if (last_step) {
             ctl.rowl[half][r] = l_half;
@@ -601,19 +650,23 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
             fence_proxy_async_smem();      // the bulk copy reads the staging
           }
           if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { ok = false; break; }   // [B]
-          // headers (flags gathered from all warps of the first page; none on the
-          // second), then one bulk copy per page into the value CTA's slot; the
-          // bytes complete its barrier
+          // headers (flags gathered from all warps of each page), then per page
+          // one bulk copy of probabilities + header + factors into the value
+          // CTA's slot (its bytes complete the slot's barrier) and, for a heavy
+          // page, one of the low parts (completing the slot's second barrier)
           if (leader) {
-            uint8_t* stg0 = smem + kOffStg;
-            *reinterpret_cast<uint4*>(stg0 + kPBytes) = make_uint4(ctl.pflags[slotA], 0u, 0u, 0u);
-            if (two) *reinterpret_cast<uint4*>(stg0 + kPSlotBytes + kPBytes) = make_uint4(0u, 0u, 0u, 0u);
-            fence_proxy_async_smem();
-            bulk_copy_to_peer(peer_p + slotA * kPSlotBytes, stg0, kPMsgBytes, peer_precv + 8 * slotA);
-            if (two) {
-              const uint32_t slotB = (gA + 1) % kPSlots;
-              bulk_copy_to_peer(peer_p + slotB * kPSlotBytes, stg0 + kPSlotBytes, kPMsgBytes,
-                                peer_precv + 8 * slotB);
+            for (uint32_t e = 0; e < (two ? 2u : 1u); ++e) {
+              const uint32_t sl = (gA + e) % kPSlots;
+              uint8_t* st = smem + kOffStg + e * kPSlotBytes;
+              const uint32_t fi = (gA + e) % (2 * kPSlots);
+              const uint32_t fl = ctl.pflags[fi];
+              ctl.pflags[fi] = 0u;              // ready for page gA + e + 6
+              *reinterpret_cast<uint4*>(st + kPBytes) = make_uint4(fl, 0u, 0u, 0u);
+              fence_proxy_async_smem();
+              bulk_copy_to_peer(peer_p + sl * kPSlotBytes, st, kPMsgBytes, peer_precv + 8 * sl);
+              if (fl & kFlagLo)
+                bulk_copy_to_peer(peer_p + sl * kPSlotBytes + kLoOff, st + kLoOff, kPBytes,
+                                  peer_lorecv + 8 * sl);
             }
             bulk_commit();
           }
