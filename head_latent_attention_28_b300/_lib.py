@@ -35,6 +35,8 @@ SIGNATURES = {
     "mla_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "mla_decode_paged": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                               _P, _SZ, _P, _P, _P]),
+    "mla_decode_paged_noalloc": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
+                                      _I, _P, _P, _P]),
     "mla_decode_paged_partial": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
                                       _I, _P, _SZ, _P, _P, _P]),
     "mla_decode_combine": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I,
@@ -199,6 +201,34 @@ def mla_decode_paged(q_lat, kv_cache, block_table, seqlens, *, d_c, softmax_scal
         _dev(o_lat, "o_lat", torch.float32),
         _dev(lse, "lse", torch.float32) if lse is not None else None, _stream(stream))
     _check(st, "mla_decode_paged" + ("" if stage == "both" else "_" + stage))
+    return o_lat, lse
+
+
+def mla_decode_paged_noalloc(q_lat, kv_cache, block_table, seqlens, *, d_c, softmax_scale,
+                             causal=False, o_lat=None, lse=None, want_lse=True, stream=None):
+    """mla_decode_paged with the library's own 32 MiB device scratch instead of a
+    caller workspace (raises MLAError(MLA_ERR_WORKSPACE) for larger shapes).
+    Returns (o_lat, lse or None)."""
+    B, T_q, H, D = q_lat.shape
+    num_blocks, page, Dc = kv_cache.shape
+    d_r = D - d_c
+    if Dc != D or block_table.shape[0] != B or seqlens.shape != (B,):
+        raise ValueError("shape mismatch")
+    if q_lat.dtype != kv_cache.dtype:
+        raise TypeError("q_lat and kv_cache must share a dtype")
+    dev = q_lat.device
+    if o_lat is None:
+        o_lat = torch.empty((B, T_q, H, d_c), device=dev, dtype=torch.float32)
+    if lse is None and want_lse:
+        lse = torch.empty((B, T_q, H), device=dev, dtype=torch.float32)
+    st = lib().mla_decode_paged_noalloc(
+        _dev(q_lat, "q_lat"), _dev(kv_cache, "kv_cache"), _dtype_code(q_lat),
+        _dev(block_table, "block_table", torch.int32), _dev(seqlens, "seqlens", torch.int32),
+        B, T_q, H, d_c, d_r, page, block_table.shape[1], num_blocks,
+        float(softmax_scale), 1 if causal else 0,
+        _dev(o_lat, "o_lat", torch.float32),
+        _dev(lse, "lse", torch.float32) if lse is not None else None, _stream(stream))
+    _check(st, "mla_decode_paged_noalloc")
     return o_lat, lse
 
 

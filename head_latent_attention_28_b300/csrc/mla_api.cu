@@ -20,6 +20,33 @@ int g_num_sms[kMaxDevices] = {};
 
 thread_local char g_last_cuda[256] = "";
 
+// Scratch of mla_decode_paged_noalloc: the split workspace (merge metadata,
+// partial log-sum-exps and outputs) in a file-scope device array instead of
+// caller memory.  32 MiB holds e.g. B = 32 sequences of 128 query rows with
+// d_c = 512 at 74 split workers (27.9 MB); larger shapes are rejected.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+__device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device (looked up once per
+// device; the lookup may load the module, so make the first call before any
+// stream capture).
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
 int note_cuda(cudaError_t e) {
   snprintf(g_last_cuda, sizeof(g_last_cuda), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
   return MLA_ERR_CUDA;
@@ -257,6 +284,26 @@ int mla_decode_paged(const void* q_lat, const void* kv_cache, int dtype,
   return decode_impl(kStageBoth, q_lat, kv_cache, dtype, block_table, seqlens, B, T_q, H, d_c,
                      d_r, page_size, max_blocks_per_seq, num_blocks, softmax_scale, causal,
                      workspace, workspace_bytes, o_lat, lse, stream);
+}
+
+int mla_decode_paged_noalloc(const void* q_lat, const void* kv_cache, int dtype,
+                             const int32_t* block_table, const int32_t* seqlens,
+                             int B, int T_q, int H, int d_c, int d_r, int page_size,
+                             int max_blocks_per_seq, int num_blocks,
+                             float softmax_scale, int causal,
+                             float* o_lat, float* lse, void* stream) {
+  if (!decode_dims_ok(B, T_q, H, d_c, d_r) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
+  const size_t need = mla_decode_workspace_size(B, T_q, H, d_c, d_r, dtype);
+  if (need == 0) return MLA_ERR_CUDA;
+  if (need > kNoAllocScratchBytes) return MLA_ERR_WORKSPACE;
+  void* ws = nullptr;
+  cudaError_t e = scratch_address(&ws);
+  if (e != cudaSuccess) return note_cuda(e);
+  // nothing in the workspace has to start at zero: the partial pass writes
+  // every merge record and part that the combine reads in the same call
+  return decode_impl(kStageBoth, q_lat, kv_cache, dtype, block_table, seqlens, B, T_q, H, d_c,
+                     d_r, page_size, max_blocks_per_seq, num_blocks, softmax_scale, causal, ws,
+                     kNoAllocScratchBytes, o_lat, lse, stream);
 }
 
 int mla_decode_paged_partial(const void* q_lat, const void* kv_cache, int dtype,

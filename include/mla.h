@@ -145,7 +145,7 @@ size_t mla_decode_workspace_size(int B, int T_q, int H, int d_c, int d_r, int dt
  *   workspace, workspace_bytes           >= mla_decode_workspace_size(...)
  * Long or ragged batches are split into page ranges processed in parallel
  * (partial softmax results in the workspace) and merged by a log-sum-exp
- * combine kernel.  The bf16 shape D = 576, d_c = 512, H*T_q >= 64 runs the
+ * combine kernel.  The bf16 shape d_c = 512, d_r = 64, H*T_q = 128 runs the
  * tensor-core (tcgen05/TMEM) kernel; every other shape a CUDA-core kernel.
  * Host errors: NULL pointers, B/T_q/H < 1, d_c < 1 or > 512, d_r < 0,
  * D > 1024, page_size != 64, max_blocks_per_seq < 1, num_blocks < 1.
@@ -162,6 +162,31 @@ int mla_decode_paged(const void* q_lat, const void* kv_cache, int dtype,
                      float softmax_scale, int causal,
                      void* workspace, size_t workspace_bytes,
                      float* o_lat, float* lse, void* stream);
+
+/*
+ * mla_decode_paged_noalloc -- mla_decode_paged without a caller workspace.
+ * (An engineering variant: the pages have no counterpart of it.)
+ *
+ * Same arguments and results as mla_decode_paged, minus workspace and
+ * workspace_bytes.  The split workspace lives in a file-scope device array
+ * of this library, 32 MiB per device: shapes whose
+ * mla_decode_workspace_size(...) exceeds 32 MiB are rejected with
+ * MLA_ERR_WORKSPACE (nothing launched).  The call allocates nothing (no
+ * cudaMalloc, no library that allocates); nothing in the scratch has to
+ * start at zero, because the partial pass writes every record the merge
+ * reads within the same call.
+ * The scratch is shared by all calls on a device: two calls that may overlap
+ * in time (different streams, or different host threads) race on it; issue
+ * them on one stream.  The first call on a device looks the scratch address
+ * up (cudaGetSymbolAddress; it may load the module), so make it before any
+ * stream capture; later calls can be captured into a graph.
+ */
+int mla_decode_paged_noalloc(const void* q_lat, const void* kv_cache, int dtype,
+                             const int32_t* block_table, const int32_t* seqlens,
+                             int B, int T_q, int H, int d_c, int d_r, int page_size,
+                             int max_blocks_per_seq, int num_blocks,
+                             float softmax_scale, int causal,
+                             float* o_lat, float* lse, void* stream);
 
 /*
  * mla_decode_paged_partial / mla_decode_combine -- the two launches that
