@@ -286,6 +286,7 @@ __global__ void __launch_bounds__(CT) combine_kernel(DecodeArgs a) {
   const bool valid = L >= a.T_q && L <= a.max_blocks * kPage;
   const int dc4 = a.d_c / VEC;
   if (!valid) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(a.err, kErrBadIndex);
     V z;
     zero_vec(z);
     for (int idx = threadIdx.x; idx < nr * dc4; idx += CT) {

@@ -1,5 +1,7 @@
-// Tensor-core MLA decode for sm_103a: 128 query rows (heads x query tokens)
-// per sequence, cached rows of 512 latent + 64 rotary bfloat16 numbers.
+// Tensor-core MLA decode for sm_103a: up to 128 query rows (heads x query
+// tokens) per sequence, cached rows of 512 latent + 64 rotary bfloat16
+// numbers.  The MMAs always run M = 128 rows; fewer rows are zero padding,
+// masked out and never written.
 //
 // What it computes is the latent-space attention of the absorbed MLA path
 // ("Attention, Part 2: MQA, GQA and MLA", the absorbed inference path: score =
@@ -294,7 +296,8 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
   const uint32_t tmem = ctl.tmem_base;
 
   const float sl2 = a.scale * kLog2e;
-  const int rows = a.T_q * a.H;   // == kRows
+  const int rows = a.T_q * a.H;   // query rows of a sequence (<= kRows; the MMAs
+                                  // always run 128 rows, the rest are zero padding)
   const int cap = a.max_blocks * kPage;
 
   uint32_t g_prod = 0, g_issue = 0;    // producer: cells (score) or units (value) issued
@@ -504,19 +507,21 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
         if (__any_sync(0xffffffffu, *abort_flag)) break;
         const Item it = ctl.items[ii];
         const int L = a.seqlens[it.b];
-        const int lim = a.causal ? (L - a.T_q + t) : (L - 1);
+        // padding rows (r >= rows) see no token at all
+        const int lim = r >= rows ? -1 : a.causal ? (L - a.T_q + t) : (L - 1);
         const int n = it.j1 - it.j0;
         // the query row: latent dims -> TMEM (half 0: [0, 256), half 1: [256, 512)),
         // rotary dims -> shared memory (K-major SW128; half h: 16-byte chunks 4h..4h+3)
         {
+          const bool real = r < rows;
           const uint4* src = reinterpret_cast<const uint4*>(
-              static_cast<const __nv_bfloat16*>(a.q) + ((size_t)it.b * rows + r) * a.D);
+              static_cast<const __nv_bfloat16*>(a.q) + ((size_t)it.b * rows + (real ? r : 0)) * a.D);
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t v[32];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              const uint4 x = __ldg(src + half * 32 + c * 8 + u);
+              const uint4 x = real ? __ldg(src + half * 32 + c * 8 + u) : make_uint4(0u, 0u, 0u, 0u);
               v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
             }
             tmem_st32(tmem + lane_off + kTmemQ + half * 128 + 32 * c, v);
@@ -524,7 +529,8 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int ch = 4 * half + c;
-            *reinterpret_cast<uint4*>(qr + r * 128 + ((ch ^ (r & 7)) << 4)) = __ldg(src + 64 + ch);
+            *reinterpret_cast<uint4*>(qr + r * 128 + ((ch ^ (r & 7)) << 4)) =
+                real ? __ldg(src + 64 + ch) : make_uint4(0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
           tmem_st_wait();
@@ -554,7 +560,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
           if (lane == 0) mbar_arrive(&ctl.s_free[sb]);     // score buffer reusable
           // mask (tokens past the visible range, a missing page, a bad block id)
           const int tok0 = jh * kPage;
-          if (!page_ok || tok0 + 63 > L - a.T_q) {
+          if (!page_ok || tok0 + 63 > L - a.T_q || r >= rows) {
             const int lim_page = page_ok ? lim : -1;
 #pragma unroll
             for (int q = 0; q < 64; ++q) x[q] = (tok0 + q <= lim_page) ? x[q] : -INFINITY;
@@ -633,7 +639,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
             ctl.rowl[half][r] = l_half;
             if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { ok = false; break; }
             l_tot = ctl.rowl[0][r] + ctl.rowl[1][r];
-            if (half == 0) {
+            if (half == 0 && r < rows) {
               const float lse = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
               const int wslot = it.b + w;
               if (it.flags & 1) { if (a.lse) a.lse[(size_t)it.b * rows + r] = lse; }
@@ -780,14 +786,15 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
         const float l_row = reinterpret_cast<const float*>(ps_last + kPBytes + 16)[2 * r + 1];
         const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
         const bool whole = it.flags & 1;
+        const int grp_rows = min(32, rows - 32 * q4);   // real rows of this warp's group
         float* out_base = (whole ? a.o + (size_t)it.b * rows * a.d_c
-                                 : a.ws_o + (size_t)(it.b + w) * rows * a.d_c) +
-                          (size_t)(32 * q4) * a.d_c + 256 * ch;
+                                 : a.ws_o + (size_t)(it.b + w) * rows * a.d_c) + 256 * ch;
+        if (grp_rows > 0) out_base += (size_t)(32 * q4) * a.d_c;
         float4* stg = reinterpret_cast<float4*>(ps_last + (warp - 2) * 2048);   // 32 rows x 4 float4
         // every thread must have read l before the staging writes below
         __syncwarp();
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < (grp_rows > 0 ? 4 : 0); ++c) {
           float o[64];
           tmem_ld64(tmem + lane_off + 256 * ch + 64 * c, o);
           tmem_ld_wait();
@@ -802,8 +809,9 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
 #pragma unroll
             for (int tt = 0; tt < 4; ++tt) {
               const int row = lane / 4 + 8 * tt, e = lane & 3;
-              reinterpret_cast<float4*>(out_base + (size_t)row * a.d_c + 64 * c + 16 * sr)[e] =
-                  stg[row * 4 + (e ^ ((row >> 1) & 3))];
+              if (row < grp_rows)
+                reinterpret_cast<float4*>(out_base + (size_t)row * a.d_c + 64 * c + 16 * sr)[e] =
+                    stg[row * 4 + (e ^ ((row >> 1) & 3))];
             }
             __syncwarp();
           }
@@ -894,7 +902,8 @@ int g_max_clusters[64] = {};
 }  // namespace
 
 bool tc_supported(int dtype, int H, int T_q, int d_c, int d_r) {
-  return dtype == BF16 && d_c == 512 && d_r == 64 && H * T_q == kRows;
+  // up to 128 query rows (heads x query tokens); fewer are padded to 128
+  return dtype == BF16 && d_c == 512 && d_r == 64 && H * T_q >= 1 && H * T_q <= kRows;
 }
 
 int tc_workers(int num_sms) {

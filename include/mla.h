@@ -145,7 +145,7 @@ size_t mla_decode_workspace_size(int B, int T_q, int H, int d_c, int d_r, int dt
  *   workspace, workspace_bytes           >= mla_decode_workspace_size(...)
  * Long or ragged batches are split into page ranges processed in parallel
  * (partial softmax results in the workspace) and merged by a log-sum-exp
- * combine kernel.  The bf16 shape d_c = 512, d_r = 64, H*T_q = 128 runs the
+ * combine kernel.  The bf16 shape d_c = 512, d_r = 64, H*T_q <= 128 runs the
  * tensor-core (tcgen05/TMEM) kernel; every other shape a CUDA-core kernel.
  * Host errors: NULL pointers, B/T_q/H < 1, d_c < 1 or > 512, d_r < 0,
  * D > 1024, page_size != 64, max_blocks_per_seq < 1, num_blocks < 1.

@@ -27,8 +27,8 @@ def _inputs(spec):
     # tensor-core path (128 query rows), ragged lengths with a partial last page
     mi.DecodeSpec("noalloc_tc", seed=31, B=6, H=128, d_c=512, d_r=64,
                   seqlens=(1000, 4096, 65, 3000, 130, 2500)),
-    # CUDA-core path, two query tokens with the causal mask
-    mi.DecodeSpec("noalloc_generic", seed=32, B=5, H=16, T_q=2, d_c=512, d_r=64,
+    # 32 query rows (padded to 128 in the MMAs), two query tokens with the causal mask
+    mi.DecodeSpec("noalloc_few_rows", seed=32, B=5, H=16, T_q=2, d_c=512, d_r=64,
                   seqlens=(300, 2049, 64, 1500, 777), causal=True),
 ])
 def test_noalloc_matches_workspace_entry_twice(spec):
