@@ -57,17 +57,20 @@ constexpr int kVUnits = 3;               // value CTA: ring depth (half pages)
 constexpr int kPBytes = kRows * 64 * 2;  // bf16 probabilities of one page (K-major, SW128)
 constexpr int kInfoBytes = 16 + kRows * 8;       // header + (alpha, l) per row
 constexpr int kPMsgBytes = kPBytes + kInfoBytes; // bytes delivered per page (one bulk copy)
-constexpr int kLoOff = 18432;            // low bf16 parts of a page's probabilities (when sent)
-constexpr int kPSlotBytes = kLoOff + kPBytes;
-constexpr int kPSlots = 3;               // probability slots (pages)
+// Probability messages travel in 18 KB units: a page takes one unit (its bf16
+// probabilities, header and per-row factors) or two (then the second one
+// carries the low bf16 parts).  Both CTAs advance the same unit counter.
+constexpr int kPUnitBytes = 18432;
+constexpr int kPUnits = 6;               // units in the value CTA's ring
+constexpr int kStgPageBytes = 2 * kPUnitBytes;   // score CTA staging per page (hi unit, lo unit)
 // shared-memory map (offsets from the 1 KB aligned base)
 constexpr int kOffQr = 0;                // score CTA: rotary query, 128 x 64 bf16 (K-major SW128)
 constexpr int kOffStg = 16384;           // score CTA: the step's two outgoing page messages
-constexpr int kOffCells = kOffStg + 2 * kPSlotBytes;   // score CTA: 8 cells
+constexpr int kOffCells = kOffStg + 2 * kStgPageBytes;   // score CTA: 8 cells
 constexpr int kOffV = 0;                 // value CTA: 3 half-page units
 constexpr int kOffP = kVUnits * kVUnit;  // value CTA: probability slots (score CTA writes them)
 constexpr int kScoreSmem = kOffCells + kCells * kCell;
-constexpr int kValueSmem = kOffP + kPSlots * kPSlotBytes;
+constexpr int kValueSmem = kOffP + kPUnits * kPUnitBytes;
 constexpr int kSmemBytes = (kScoreSmem > kValueSmem ? kScoreSmem : kValueSmem) + 1024;
 constexpr int kMaxItems = 64;            // work items planned per batch
 // TMEM columns (score CTA): score buffers 2 x 128 at [0, 256), latent query at [256, 512)
@@ -80,12 +83,12 @@ constexpr uint32_t kFlagRescale = 1u;    // rows rescaled before this page's val
 constexpr uint32_t kFlagLo = 2u;         // the low bf16 parts of the probabilities follow
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-static_assert(kPMsgBytes <= kPSlotBytes, "probability slot too small");
+static_assert(kPMsgBytes <= kPUnitBytes, "probability unit too small");
 static_assert(kPMsgBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
 static_assert(kOffCells % 1024 == 0, "SW128 operands need 1 KB alignment");
-static_assert(kOffP % 1024 == 0 && kPSlotBytes % 1024 == 0, "SW128 operands need 1 KB alignment");
+static_assert(kOffP % 1024 == 0 && kPUnitBytes % 1024 == 0, "SW128 operands need 1 KB alignment");
 static_assert(8 * 2048 <= kPBytes, "epilogue staging lives in a probability slot");
-static_assert(kLoOff >= kPMsgBytes && kLoOff % 1024 == 0, "low parts after the header, SW128-aligned");
+static_assert(4 * 4096 <= kPBytes, "four epilogue boxes fit in a unit's probability area");
 
 struct Item {
   int b, j0, j1;            // sequence, page range [j0, j1)
@@ -97,16 +100,16 @@ struct SmemCtl {
   // score CTA
   uint64_t cell_full[kCells], cell_empty[kCells];
   uint64_t s_full[2], s_free[2];
-  uint64_t q_ready, pfree[kPSlots];
+  uint64_t q_ready, pfree[kPUnits];
   // value CTA
   uint64_t v_full[kVUnits], v_empty[kVUnits];
-  uint64_t p_recv[kPSlots], pv_done[kPSlots];
-  uint64_t lo_recv[kPSlots];   // the low parts of a slot's probabilities arrived (armed on demand)
+  uint64_t p_recv[kPUnits];    // a unit's bytes arrived
+  uint64_t pv_done[kPUnits];   // value MMAs of the page whose first unit sits here completed
   uint64_t resc_done, vz_done;
   uint64_t o_free;          // the epilogue has read O: the next item may overwrite it
   uint64_t epi_go;          // O of the item is final (value row warps -> other warps)
   uint64_t epi_done;        // all epilogue warps are done with the staging slot
-  uint64_t rows_seen[kPSlots];   // all row warps have read the header and factors in a slot
+  uint64_t rows_seen[kPUnits];  // all row warps have read the header and factors in a unit
   // both
   uint64_t grp, mma_final;
   uint32_t tmem_base;
@@ -119,7 +122,8 @@ struct SmemCtl {
   // score CTA: header flags of a page, indexed by page mod 2 x slots: a word
   // is reset by the leader after the step that sent it and written again three
   // steps later, so the two never race
-  uint32_t pflags[2 * kPSlots];
+  uint32_t pflags[6];
+  uint32_t epi_unit;        // value CTA: first unit of the item's last page (for the epilogue)
   Item items[kMaxItems];
 };
 
@@ -238,7 +242,8 @@ __device__ __forceinline__ uint32_t hi_half_f(uint32_t u) { return u & 0xffff000
 // the kernel
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
-decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool) {
+decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool,
+                 const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_ws) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ SmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -265,13 +270,12 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
       mbar_init(&ctl.v_full[i], 1);
       mbar_init(&ctl.v_empty[i], 1);
     }
-    for (int i = 0; i < kPSlots; ++i) {
+    for (int i = 0; i < kPUnits; ++i) {
       mbar_init(&ctl.pfree[i], 1);
       mbar_init(&ctl.p_recv[i], 1);
       mbar_init(&ctl.pv_done[i], 1);
-      mbar_init(&ctl.lo_recv[i], 1);
-      ctl.pflags[2 * i] = 0;
-      ctl.pflags[2 * i + 1] = 0;
+      mbar_init(&ctl.rows_seen[i], 4);
+      ctl.pflags[i] = 0;
     }
     mbar_init(&ctl.q_ready, 8);
     mbar_init(&ctl.resc_done, 4);
@@ -279,11 +283,10 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
     mbar_init(&ctl.o_free, 8);
     mbar_init(&ctl.epi_go, 4);
     mbar_init(&ctl.epi_done, 8);
-    for (int i = 0; i < kPSlots; ++i) mbar_init(&ctl.rows_seen[i], 4);
     mbar_init(&ctl.grp, 8);
     mbar_init(&ctl.mma_final, 1);
     if (rank == 1)     // the first pages' probabilities will arrive
-      for (int i = 0; i < kPSlots; ++i) mbar_arrive_expect_tx(&ctl.p_recv[i], kPMsgBytes);
+      for (int i = 0; i < kPUnits; ++i) mbar_arrive_expect_tx(&ctl.p_recv[i], kPMsgBytes);
     fence_mbar_init_cluster();
   }
   if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_pool);
@@ -425,7 +428,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
           }
         } else {
           const uint32_t idPV = idesc_bf16_f32(128, 256, 0, 1);
-          uint32_t lo_par = 0;   // per slot: parity of the next low-parts phase
+          uint32_t un = 0;       // unit counter
           for (int ii = 0; ii < n_items && !*abort_flag; ++ii) {
             const Item it = ctl.items[ii];
             const int L = a.seqlens[it.b];
@@ -433,12 +436,12 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
             // the previous item's epilogue must have read O before it is overwritten
             bool ok = it_cnt == 0 || mbar_wait(&ctl.o_free, (it_cnt - 1) & 1, abort_flag, kWaitNs);
             for (int i = 0; ok && i < it.j1 - it.j0; ++i) {
-              const uint32_t g = g_page + i, slot = g % kPSlots;
+              const uint32_t g = g_page + i, slot = un % kPUnits;
               const int j = it.j0 + i;
-              ok = mbar_wait_cluster(&ctl.p_recv[slot], (g / kPSlots) & 1, abort_flag, kWaitNs);
+              ok = mbar_wait_cluster(&ctl.p_recv[slot], (un / kPUnits) & 1, abort_flag, kWaitNs);
               if (!ok) break;
-              fence_proxy_async_smem();   // the probabilities came in as generic stores
-              const uint8_t* ps = pslots + slot * kPSlotBytes;
+              fence_proxy_async_smem();
+              const uint8_t* ps = pslots + slot * kPUnitBytes;
               const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(ps + kPBytes);
               if ((flags & 1u) && i > 0) {          // rows rescaled by the value warps
                 ok = mbar_wait(&ctl.resc_done, n_resc & 1, abort_flag, kWaitNs);
@@ -449,12 +452,9 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
                 ++n_vz;
               }
               const bool lo = (flags & kFlagLo) != 0;
+              const uint8_t* pl = pslots + ((un + 1) % kPUnits) * kPUnitBytes;   // low parts' unit
               if (ok && lo) {
-                // the low parts may already be here (the count then goes below
-                // zero until this expectation is added)
-                mbar_arrive_expect_tx(&ctl.lo_recv[slot], kPBytes);
-                ok = mbar_wait_cluster(&ctl.lo_recv[slot], (lo_par >> slot) & 1, abort_flag, kWaitNs);
-                lo_par ^= 1u << slot;
+                ok = mbar_wait_cluster(&ctl.p_recv[(un + 1) % kPUnits], ((un + 1) / kPUnits) & 1, abort_flag, kWaitNs);
                 fence_proxy_async_smem();
               }
               for (int nh = 0; ok && nh < 2; ++nh) {
@@ -472,7 +472,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
                 if (lo) {
 #pragma unroll
                   for (int kk = 0; kk < 4; ++kk) {   // the same V rows, A = low parts
-                    const uint64_t ad = sdesc_sw128(smem_u32(ps + kLoOff + kk * 32), 16, 1024);
+                    const uint64_t ad = sdesc_sw128(smem_u32(pl + kk * 32), 16, 1024);
                     const uint64_t bd = sdesc_sw128(smem_u32(vp + kk * 2048), kBox, 1024);
                     mma_ss(tmem + nh * 256, ad, bd, idPV, 1);
                   }
@@ -481,6 +481,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
               }
               if (!ok) break;
               mma_commit(&ctl.pv_done[slot]);
+              un += lo ? 2 : 1;
             }
             if (!ok) { fail(&ctl, a.err); break; }
             g_page += it.j1 - it.j0;
@@ -499,7 +500,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
       const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
       const uint32_t peer_p = mapa(smem_u32(pslots), 1);               // value CTA's slots
       const uint32_t peer_precv = mapa(smem_u32(&ctl.p_recv[0]), 1);   // + 8 * slot
-      const uint32_t peer_lorecv = mapa(smem_u32(&ctl.lo_recv[0]), 1); // + 8 * slot
+      uint32_t un_s = 0;   // leader: unit counter
       const bool leader = threadIdx.x == 64;
       const int t = r / a.H;
       uint8_t* qr = smem + kOffQr;
@@ -569,7 +570,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
 #pragma unroll
           for (int q = 1; q < 64; ++q) mx = fmaxf(mx, x[q]);
           ctl.rowx[half][r] = mx;
-          const uint32_t fh = (gA + half) % (2 * kPSlots);   // this half's page flags
+          const uint32_t fh = (gA + half) % 6;   // this half's page flags
           {
             // Precision of the bf16 probabilities: a page whose largest
             // probability is not small against the row sum so far also sends
@@ -577,20 +578,13 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
             // the rows' maxima are merged: against this half's own running sum
             // and the previous reference (both can only make the test pass more
             // often than with the merged values).
+            // The item's last page always sends them: its two units then give
+            // the value CTA's epilogue its staging space.
             const bool heavy = has && ex2(mx * sl2 - m_run) >= l_half;
-            if (__any_sync(0xffffffffu, heavy) && lane == 0) atomicOr(&ctl.pflags[fh], kFlagLo);
+            const bool item_last = has && last_step && half == (two ? 1 : 0);
+            if ((__any_sync(0xffffffffu, heavy) || item_last) && lane == 0) atomicOr(&ctl.pflags[fh], kFlagLo);
           }
-          if (leader) {
-            // the value CTA must have finished with the pages that last used these slots
-            bool fr = true;
-            for (uint32_t e = 0; e < (two ? 2u : 1u) && fr; ++e) {
-              const uint32_t ge = gA + e;
-              if (ge >= (uint32_t)kPSlots)
-                fr = mbar_wait_cluster(&ctl.pfree[ge % kPSlots], ((ge / kPSlots) - 1) & 1, abort_flag, kWaitNs);
-            }
-            if (!fr) fail(&ctl, a.err);
-            bulk_wait_read0();   // the previous step's copies have read the staging
-          }
+          if (leader) bulk_wait_read0();   // the previous step's copies have read the staging
           if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { ok = false; break; }   // [A]
           const float m_page = fmaxf(mx, ctl.rowx[half ^ 1][r]) * sl2;
           const float m_new = fmaxf(m_run, m_page);
@@ -601,7 +595,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
             m_run = m_new;
             l_half *= alpha;
           }
-          uint8_t* stg = smem + kOffStg + half * kPSlotBytes;   // this half's page message
+          uint8_t* stg = smem + kOffStg + half * kStgPageBytes;   // this half's page message
           if (has) {
             // probabilities, rounded to bf16 (and, for a heavy page, the
             // residual rounded again); l sums exactly what the value MMA sees.
@@ -628,12 +622,12 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
               }
               const int off = r * 128 + ((c ^ (r & 7)) << 4);
               *reinterpret_cast<uint4*>(stg + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              if (lo) *reinterpret_cast<uint4*>(stg + kLoOff + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+              if (lo) *reinterpret_cast<uint4*>(stg + kPUnitBytes + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
             }
             l_half += psum;
           }
           if (__any_sync(0xffffffffu, need) && k > 0 && lane == 0 && half == 0)
-            atomicOr(&ctl.pflags[gA % (2 * kPSlots)], kFlagRescale);
+            atomicOr(&ctl.pflags[gA % 6], kFlagRescale);
           float l_tot = 0.f;
           if (last_step) {
             ctl.rowl[half][r] = l_half;
@@ -656,25 +650,31 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
             fence_proxy_async_smem();      // the bulk copy reads the staging
           }
           if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { ok = false; break; }   // [B]
-          // headers (flags gathered from all warps of each page), then per page
-          // one bulk copy of probabilities + header + factors into the value
-          // CTA's slot (its bytes complete the slot's barrier) and, for a heavy
-          // page, one of the low parts (completing the slot's second barrier)
+          // headers (flags gathered from all warps of each page), then per unit
+          // one bulk copy into the value CTA's ring once the value CTA has freed
+          // that unit; its bytes complete the unit's barrier there.  Only this
+          // thread waits here: the staging is local, so the softmax of the
+          // next step runs while the value CTA catches up.
           if (leader) {
-            for (uint32_t e = 0; e < (two ? 2u : 1u); ++e) {
-              const uint32_t sl = (gA + e) % kPSlots;
-              uint8_t* st = smem + kOffStg + e * kPSlotBytes;
-              const uint32_t fi = (gA + e) % (2 * kPSlots);
+            bool fr = true;
+            for (uint32_t e = 0; e < (two ? 2u : 1u) && fr; ++e) {
+              uint8_t* st = smem + kOffStg + e * kStgPageBytes;
+              const uint32_t fi = (gA + e) % 6;
               const uint32_t fl = ctl.pflags[fi];
               ctl.pflags[fi] = 0u;              // ready for page gA + e + 6
               *reinterpret_cast<uint4*>(st + kPBytes) = make_uint4(fl, 0u, 0u, 0u);
               fence_proxy_async_smem();
-              bulk_copy_to_peer(peer_p + sl * kPSlotBytes, st, kPMsgBytes, peer_precv + 8 * sl);
-              if (fl & kFlagLo)
-                bulk_copy_to_peer(peer_p + sl * kPSlotBytes + kLoOff, st + kLoOff, kPBytes,
-                                  peer_lorecv + 8 * sl);
+              for (uint32_t part = 0; part < ((fl & kFlagLo) ? 2u : 1u) && fr; ++part) {
+                const uint32_t un = un_s++, us = un % kPUnits;
+                if (un >= (uint32_t)kPUnits)
+                  fr = mbar_wait_cluster(&ctl.pfree[us], ((un / kPUnits) - 1) & 1, abort_flag, kWaitNs);
+                if (fr)
+                  bulk_copy_to_peer(peer_p + us * kPUnitBytes, st + part * kPUnitBytes, kPMsgBytes,
+                                    peer_precv + 8 * us);
+              }
             }
             bulk_commit();
+            if (!fr) fail(&ctl, a.err);
           }
           g_page += two ? 2 : 1;
           ++g_step;
@@ -692,22 +692,27 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
       const int r = 32 * q4 + lane;
       const int tq = threadIdx.x - 64;             // 0..127 (row warps)
       const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-      const uint32_t peer_pfree = mapa(smem_u32(&ctl.pfree[0]), 0);   // + 8 * slot
+      const uint32_t peer_pfree = mapa(smem_u32(&ctl.pfree[0]), 0);   // + 8 * unit slot
+      // row warps: unit counter, and per unit slot the parity of the next
+      // phase of its page barriers (pv_done, rows_seen advance only when the
+      // slot holds a page's first unit)
+      uint32_t un_v = 0, pvpar = 0, prev_slot = 0, prev_par = 0;
       for (int ii = 0; ii < n_items; ++ii) {
         if (__any_sync(0xffffffffu, *abort_flag)) break;
         const Item it = ctl.items[ii];
         const int L = a.seqlens[it.b];
         const int Pb = pages_of(L, a.T_q, cap);
         const int n = it.j1 - it.j0;
-        const uint32_t g_last = g_page + n - 1, slot_last = g_last % kPSlots;
         bool ok = true;
         if (row_warp) {
           for (int i = 0; i < n; ++i) {
-            const uint32_t g = g_page + i, slot = g % kPSlots;
+            const uint32_t g = g_page + i, slot = un_v % kPUnits;
             const int j = it.j0 + i;
-            uint8_t* ps = pslots + slot * kPSlotBytes;
-            if (!warp_wait_cluster(&ctl.p_recv[slot], (g / kPSlots) & 1, abort_flag)) { ok = false; break; }
+            uint8_t* ps = pslots + slot * kPUnitBytes;
+            if (!warp_wait_cluster(&ctl.p_recv[slot], (un_v / kPUnits) & 1, abort_flag)) { ok = false; break; }
             const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(ps + kPBytes);
+            const bool lo = (flags & kFlagLo) != 0;
+            const uint32_t par = (pvpar >> slot) & 1;
             const float* info = reinterpret_cast<const float*>(ps + kPBytes + 16);
             if (j == Pb - 1 && (L & (kPage - 1)) != 0) {
               // last page: zero the V rows past the sequence end (they may hold NaN)
@@ -729,7 +734,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
             }
             if ((flags & 1u) && i > 0) {
               // rescale O rows before this page's value MMA: O holds pages < j
-              if (!warp_wait(&ctl.pv_done[(g - 1) % kPSlots], ((g - 1) / kPSlots) & 1, abort_flag)) { ok = false; break; }
+              if (!warp_wait(&ctl.pv_done[prev_slot], prev_par, abort_flag)) { ok = false; break; }
               tc_fence_after();
               const float alpha = info[2 * r];
 #pragma unroll 1
@@ -751,30 +756,37 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
               __syncwarp();
               if (lane == 0) mbar_arrive(&ctl.resc_done);
             }
-            // header and factors read by this warp (one barrier per slot: a warp
-            // may run up to three pages ahead of the releasing warp, never four,
-            // since page g + 4 arrives only after slot g is released)
+            // header and factors read by this warp (one barrier per unit slot: a
+            // warp cannot reach the slot's next page before this unit is released)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl.rows_seen[slot]);
             // this page's value MMA done
-            if (!warp_wait(&ctl.pv_done[slot], (g / kPSlots) & 1, abort_flag)) { ok = false; break; }
+            if (!warp_wait(&ctl.pv_done[slot], par, abort_flag)) { ok = false; break; }
             if (i < n - 1) {
-              // the slot may be refilled once every row warp is past its header
+              // the page's units may be refilled once every row warp is past its header
               if (threadIdx.x == 64) {
-                if (mbar_wait(&ctl.rows_seen[slot], (g / kPSlots) & 1, abort_flag, kWaitNs)) {
-                  mbar_arrive_expect_tx(&ctl.p_recv[slot], kPMsgBytes);
-                  mbar_arrive_remote(peer_pfree + 8 * slot);
+                if (mbar_wait(&ctl.rows_seen[slot], par, abort_flag, kWaitNs)) {
+                  for (uint32_t e = 0; e < (lo ? 2u : 1u); ++e) {
+                    const uint32_t us = (un_v + e) % kPUnits;
+                    mbar_arrive_expect_tx(&ctl.p_recv[us], kPMsgBytes);
+                    mbar_arrive_remote(peer_pfree + 8 * us);
+                  }
                 } else {
                   fail(&ctl, a.err);
                 }
               }
               __syncwarp();
             } else {
-              // O is final; the last page's slot becomes the epilogue staging
-              // buffer and is handed back only after the epilogue
+              // O is final; the last page's two units (it always carries low
+              // parts) become the epilogue staging and are handed back after it
+              if (threadIdx.x == 64) ctl.epi_unit = lo ? un_v : 0xffffffffu;
               __syncwarp();
               if (lane == 0) mbar_arrive(&ctl.epi_go);
             }
+            prev_slot = slot;
+            prev_par = par;
+            pvpar ^= 1u << slot;
+            un_v += lo ? 2 : 1;
           }
         }
         if (ok && !warp_wait(&ctl.epi_go, it_cnt & 1, abort_flag)) ok = false;
@@ -782,7 +794,10 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
         // ---- epilogue: normalise and write the item's 128 x 512 output, each
         // warp staging 32 rows x 16 columns at a time for full-sector writes
         tc_fence_after();
-        uint8_t* ps_last = pslots + slot_last * kPSlotBytes;
+        const uint32_t eu = ctl.epi_unit;
+        if (eu == 0xffffffffu) { fail(&ctl, a.err); break; }   // cannot happen: the last page sends low parts
+        uint8_t* ps_last = pslots + (eu % kPUnits) * kPUnitBytes;
+        uint8_t* ps_lo = pslots + ((eu + 1) % kPUnits) * kPUnitBytes;
         const float l_row = reinterpret_cast<const float*>(ps_last + kPBytes + 16)[2 * r + 1];
         const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
         const bool whole = it.flags & 1;
@@ -790,11 +805,39 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
         float* out_base = (whole ? a.o + (size_t)it.b * rows * a.d_c
                                  : a.ws_o + (size_t)(it.b + w) * rows * a.d_c) + 256 * ch;
         if (grp_rows > 0) out_base += (size_t)(32 * q4) * a.d_c;
-        float4* stg = reinterpret_cast<float4*>(ps_last + (warp - 2) * 2048);   // 32 rows x 4 float4
         // every thread must have read l before the staging writes below
         __syncwarp();
+        if (grp_rows == 32) {
+          // whole 32-row group: 32 x 32 fp32 boxes staged (SW128) in the
+          // slot's probability areas (not its factors) and written by TMA
+          const CUtensorMap* tmo = whole ? &tm_o : &tm_ws;
+          const int row0 = (whole ? it.b : it.b + w) * rows + 32 * q4;
+          const int wi = warp - 2;
+          uint8_t* box = wi < 4 ? ps_last + wi * 4096 : ps_lo + (wi - 4) * 4096;
 #pragma unroll 1
-        for (int c = 0; c < (grp_rows > 0 ? 4 : 0); ++c) {
+          for (int c = 0; c < 8; ++c) {
+            float o[32];
+            tmem_ld32(tmem + lane_off + 256 * ch + 32 * c, o);
+            tmem_ld_wait();
+            if (lane == 0) bulk_wait_read0();     // the previous box has been read
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<float4*>(box + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                  make_float4(o[4 * k] * inv, o[4 * k + 1] * inv, o[4 * k + 2] * inv, o[4 * k + 3] * inv);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(tmo, box, 256 * ch + 32 * c, row0);
+              bulk_commit();
+            }
+          }
+          if (lane == 0) bulk_wait_read0();         // staging free before the slot is handed back
+          __syncwarp();
+        }
+        float4* stg = reinterpret_cast<float4*>(ps_last + (warp - 2) * 2048);   // 32 rows x 4 float4
+#pragma unroll 1
+        for (int c = 0; c < (grp_rows > 0 && grp_rows < 32 ? 4 : 0); ++c) {
           float o[64];
           tmem_ld64(tmem + lane_off + 256 * ch + 64 * c, o);
           tmem_ld_wait();
@@ -825,8 +868,11 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
         if (threadIdx.x == 64) {
           // hand the staging slot back once every epilogue warp is done with it
           if (mbar_wait(&ctl.epi_done, it_cnt & 1, abort_flag, kWaitNs)) {
-            mbar_arrive_expect_tx(&ctl.p_recv[slot_last], kPMsgBytes);
-            mbar_arrive_remote(peer_pfree + 8 * slot_last);
+            for (uint32_t e = 0; e < 2; ++e) {
+              const uint32_t us = (eu + e) % kPUnits;
+              mbar_arrive_expect_tx(&ctl.p_recv[us], kPMsgBytes);
+              mbar_arrive_remote(peer_pfree + 8 * us);
+            }
           } else {
             fail(&ctl, a.err);
           }
@@ -845,6 +891,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // ---- drain: all MMAs complete, all TMA loads and bulk copies done, then free TMEM
   if (rank == 0 && threadIdx.x == 64) bulk_wait0();
+  if (rank == 1 && warp >= 2 && lane == 0) bulk_wait0();   // output stores complete
   if (warp == 1 && lane == 0) {
     mma_commit(&ctl.mma_final);
     if (!mbar_wait(&ctl.mma_final, 0, &ctl.never, kWaitNs)) atomicOr(a.err, kErrTimeout);
@@ -885,13 +932,14 @@ cudaError_t get_encode() {
 }
 
 cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
-                     uint32_t box_cols, uint32_t box_rows) {
+                     uint32_t box_cols, uint32_t box_rows, bool f32 = false) {
+  const uint64_t es_bytes = f32 ? 4 : 2;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
+  cuuint64_t strides[1] = {cols * es_bytes};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  CUresult r = g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -935,8 +983,14 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
   if ((long long)a.num_blocks * kPage >= (1LL << 31)) return cudaErrorInvalidValue;
-  CUtensorMap tm_pool;
+  CUtensorMap tm_pool, tm_o, tm_ws;
   e = make_map(&tm_pool, a.cache, (uint64_t)a.D, (uint64_t)a.num_blocks * kPage, 64, 64);
+  if (e != cudaSuccess) return e;
+  // outputs and split parts: [rows, 512] fp32, written in 32 x 32 boxes
+  const uint64_t rows = (uint64_t)a.T_q * a.H;
+  e = make_map(&tm_o, a.o, (uint64_t)a.d_c, (uint64_t)a.B * rows, 32, 32, true);
+  if (e != cudaSuccess) return e;
+  e = make_map(&tm_ws, a.ws_o, (uint64_t)a.d_c, (uint64_t)(a.B + a.W) * rows, 32, 32, true);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -950,7 +1004,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   attr.val.clusterDim.x = 2; attr.val.clusterDim.y = 1; attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, a, tm_pool);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, a, tm_pool, tm_o, tm_ws);
 }
 
 }  // namespace mla

@@ -212,6 +212,13 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* desc) {
 }
 // 2-D tiled load of box (x = c0 innermost, y = c1) into shared memory,
 // completing `bytes` on `bar`.
+// 2-D tiled store of a shared-memory box to global memory, in this thread's
+// current bulk async-group (bulk_commit / bulk_wait_read0 / bulk_wait0)
+__device__ __forceinline__ void tma_store_2d(const void* desc, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(desc),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* desc, uint64_t* bar, int c0,
                                             int c1, uint64_t cache_hint) {
   asm volatile(
