@@ -46,7 +46,8 @@ SIGNATURES = {
     "mla_last_cuda_error": (ctypes.c_char_p, []),
     "mla_check_status": (_I, [_P]),
     "mla_version": (_I, []),
-    "mla_decode_split_plan": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+    "mla_decode_split_plan": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "mla_decode_item_cost": (_I, [_I, _I, _I, _I, _I]),
     "mla_decode_num_workers": (_I, [_I, _I, _I, _I, _I, _I]),
     "mla_decode_path": (_I, [_I, _I, _I, _I, _I]),
 }
@@ -251,7 +252,7 @@ def mla_absorb_output(o_lat, w_uv, w_o, *, out=None, stream=None):
     return out
 
 
-def mla_decode_split_plan(seqlens, T_q, max_blocks_per_seq, num_workers):
+def mla_decode_split_plan(seqlens, T_q, max_blocks_per_seq, num_workers, item_cost=0):
     """Host helper: (first_worker, last_worker, total_pages) per sequence."""
     import numpy as np
     sl = np.ascontiguousarray(seqlens, dtype=np.int32)
@@ -260,10 +261,16 @@ def mla_decode_split_plan(seqlens, T_q, max_blocks_per_seq, num_workers):
     last = np.empty(B, dtype=np.int32)
     total = ctypes.c_int64(0)
     st = lib().mla_decode_split_plan(sl.ctypes.data, B, T_q, max_blocks_per_seq, num_workers,
-                                     first.ctypes.data, last.ctypes.data,
+                                     item_cost, first.ctypes.data, last.ctypes.data,
                                      ctypes.addressof(total))
     _check(st, "mla_decode_split_plan")
     return first, last, int(total.value)
+
+
+def mla_decode_item_cost(T_q, H, d_c, d_r, dtype=torch.bfloat16) -> int:
+    """The split partition's per-item cost (pages) mla_decode_paged uses for a shape."""
+    code = MLA_BF16 if dtype == torch.bfloat16 else MLA_F32
+    return int(lib().mla_decode_item_cost(T_q, H, d_c, d_r, code))
 
 
 def mla_decode_num_workers(B, T_q, H, d_c, d_r, dtype=torch.bfloat16) -> int:

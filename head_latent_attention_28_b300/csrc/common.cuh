@@ -18,27 +18,46 @@ enum DType { F32 = 0, BF16 = 1 };
 // ---------------------------------------------------------------------------
 // Split-KV partition.
 //
-// Sequence b owns the global page range [S_b, S_b + P_b), P_b = ceil(L_b/64),
-// S_b = sum_{b'<b} P_b'.  With T = sum_b P_b pages and W' = min(W, T) active
-// workers (W launched), worker w < W' processes pages
-// [floor(T*w/W'), floor(T*(w+1)/W')): every active worker gets the same
-// number of pages give or take one, whatever the length mix, and none is
-// empty (so the workers between a sequence's first and last one all hold a
-// part of it).  A sequence
-// whose pages fall to a single worker is finished by that worker; otherwise
-// every worker that touched it leaves a partial (o, lse) in slot b + w of the
-// workspace (b + w is unique among intersecting (b, w) pairs because both
-// page ranges are ordered), and the combine kernel merges them.
+// Work is laid out on a cost axis: every valid sequence b (P_b = ceil(L_b/64)
+// > 0 pages) covers C + P_b units, C units for the fixed cost of one work item
+// (loading the query rows, the output epilogue) followed by one unit per page.
+// With U units in all and W' = min(W, floor(U / (C + 1))) active workers (W
+// launched), worker w < W' takes the units [floor(U*w/W'), floor(U*(w+1)/W'))
+// and, of sequence b starting at unit A_b (its first page at A_b + C), the
+// pages j with A_b + C + j in that range.  A worker whose range crosses into
+// a new sequence so gets about C pages fewer, and the cost pages + C * items
+// of the active workers differs by at most 2C + 1 units (a range holds the
+// floor or ceiling of U / W' units; a worker starting inside a sequence's
+// pages pays C for that item outside its units, and one whose range ends
+// inside a sequence's C units holds units it does not pay for).  Each range
+// spans at least C + 1
+// units, so it holds at least one page and none is empty (the workers between
+// a sequence's first and last one all hold a part of it).  With C = 0 this is
+// the plain even split of the pages.  A sequence whose pages fall to a single
+// worker is finished by that worker; otherwise every worker that touched it
+// leaves a partial (o, lse) in slot b + w of the workspace (b + w is unique
+// among intersecting (b, w) pairs because both ranges are ordered), and the
+// combine kernel merges them.
 // ---------------------------------------------------------------------------
-__host__ __device__ inline int part_active(long long T, int W) {
-  return (int)(T < (long long)W ? T : (long long)W);
+__host__ __device__ inline int part_active(long long U, int W, int C) {
+  const long long m = U / (long long)(C + 1);
+  return (int)(m < (long long)W ? m : (long long)W);
 }
-__host__ __device__ inline long long part_begin(long long T, int W, int w) {
-  return (T * (long long)w) / W;
+// first unit of worker w
+__host__ __device__ inline long long part_begin(long long U, int W, int w) {
+  return (U * (long long)w) / W;
 }
-// the worker whose range holds page p (0 <= p < T)
-__host__ __device__ inline int part_worker_of(long long T, int W, long long p) {
-  return (int)(((p + 1) * (long long)W - 1) / T);
+// the worker whose range holds unit x (0 <= x < U)
+__host__ __device__ inline int part_worker_of(long long U, int W, long long x) {
+  return (int)(((x + 1) * (long long)W - 1) / U);
+}
+// pages [*j0, *j1) of a sequence with P pages, the first at unit A, that lie
+// in the units [x0, x1)
+__host__ __device__ inline void part_pages(long long x0, long long x1, long long A, int P,
+                                           int* j0, int* j1) {
+  const long long a = x0 - A, b = x1 - A;
+  *j0 = (int)(a < 0 ? 0 : a > P ? P : a);
+  *j1 = (int)(b < 0 ? 0 : b > P ? P : b);
 }
 
 // Workspace layout for rows = T_q*H query rows per sequence.
@@ -76,6 +95,7 @@ struct DecodeArgs {
   float* ws_lse;
   float* ws_o;
   int W;                      // number of split workers
+  int item_cost;              // C of the split partition (units per work item)
   unsigned* err;              // device error word
 };
 

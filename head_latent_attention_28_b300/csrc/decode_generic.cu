@@ -83,40 +83,42 @@ __global__ void __launch_bounds__(GT) decode_generic_kernel(DecodeArgs a) {
   const int cap = a.max_blocks * kPage;
   const float sl2 = a.scale * kLog2e;
 
-  // ---- pass 1: total pages (and the error flag for invalid lengths)
+  // ---- pass 1: total cost units (and the error flag for invalid lengths)
+  const int C = a.item_cost;
   long long mine = 0;
   bool bad = false;
   for (int b = tid; b < a.B; b += GT) {
     int L = a.seqlens[b];
     int P = pages_of(L, a.T_q, cap);
     bad |= (P == 0);
-    mine += P;
+    mine += P > 0 ? C + P : 0;
   }
   if (bad && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(a.err, kErrBadIndex);
 #pragma unroll
   for (int o = 16; o; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
   if (lane == 0) red_tmp[warp] = mine;
   __syncthreads();
-  long long Tpages = 0;
-  for (int i = 0; i < GT / 32; ++i) Tpages += red_tmp[i];
-  if (Tpages == 0) return;
-  const int Wa = part_active(Tpages, a.W);
+  long long U = 0;
+  for (int i = 0; i < GT / 32; ++i) U += red_tmp[i];
+  if (U == 0) return;
+  const int Wa = part_active(U, a.W, C);
   if (w >= Wa) return;
-  const long long p0 = part_begin(Tpages, Wa, w), p1 = part_begin(Tpages, Wa, w + 1);
+  const long long x0 = part_begin(U, Wa, w), x1 = part_begin(U, Wa, w + 1);
 
-  // ---- pass 2: walk sequences in chunks, process the ones meeting [p0, p1)
+  // ---- pass 2: walk sequences in chunks, process the ones with pages in [x0, x1)
   long long base = 0;
-  for (int c0 = 0; c0 < a.B && base < p1; c0 += GT) {
+  for (int c0 = 0; c0 < a.B && base < x1; c0 += GT) {
     const int bq = c0 + tid;
     const int P = bq < a.B ? pages_of(a.seqlens[bq], a.T_q, cap) : 0;
     int chunk_total;
-    const int excl = block_exclusive_scan(P, scan_tmp, &chunk_total);
+    const int excl = block_exclusive_scan(P > 0 ? C + P : 0, scan_tmp, &chunk_total);
     seg_start[tid] = excl;
     if (tid == 0) { seg_first = GT; seg_last = -1; }
     __syncthreads();
     {
-      long long S = base + excl;
-      if (P > 0 && S < p1 && S + P > p0) { atomicMin(&seg_first, tid); atomicMax(&seg_last, tid); }
+      int j0, j1;
+      part_pages(x0, x1, base + excl + C, P, &j0, &j1);
+      if (P > 0 && j1 > j0) { atomicMin(&seg_first, tid); atomicMax(&seg_last, tid); }
     }
     __syncthreads();
     const int f = seg_first, l = seg_last;
@@ -125,14 +127,13 @@ __global__ void __launch_bounds__(GT) decode_generic_kernel(DecodeArgs a) {
       const int L = a.seqlens[b];
       const int Pb = pages_of(L, a.T_q, cap);
       if (Pb == 0) continue;
-      const long long Sb = base + seg_start[i];
-      const long long g0 = Sb > p0 ? Sb : p0;
-      const long long g1 = (Sb + Pb) < p1 ? (Sb + Pb) : p1;
-      const int j0 = (int)(g0 - Sb), j1 = (int)(g1 - Sb);
+      const long long Ab = base + seg_start[i] + C;   // unit of the first page
+      int j0, j1;
+      part_pages(x0, x1, Ab, Pb, &j0, &j1);
+      if (j1 <= j0) continue;
       const bool whole = (j0 == 0 && j1 == Pb);
       if (j0 == 0 && blockIdx.y == 0 && tid == 0)
-        a.meta[b] = make_int2(part_worker_of(Tpages, Wa, Sb),
-                              part_worker_of(Tpages, Wa, Sb + Pb - 1));
+        a.meta[b] = make_int2(part_worker_of(U, Wa, Ab), part_worker_of(U, Wa, Ab + Pb - 1));
       const int tok0 = j0 * kPage;
       const int tok1 = min(j1 * kPage, L);
 

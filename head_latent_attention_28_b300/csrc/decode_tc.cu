@@ -161,40 +161,45 @@ __device__ int cta_excl_scan(int v, int* scan, int* total) {
 }
 
 // Plan the work items of worker w with item index in [offset, offset + kMaxItems).
-// Same page partition as the CUDA-core kernel (see part_begin / part_worker_of).
+// Same partition as the CUDA-core kernel (see part_begin / part_pages), with
+// the item cost the launcher chose for this kernel.
 __device__ void plan_batch(const DecodeArgs& a, int w, int offset, SmemCtl* ctl) {
   const int tid = threadIdx.x;
   const int cap = a.max_blocks * kPage;
+  const int C = a.item_cost;
   int mine = 0;
-  for (int b = tid; b < a.B; b += kThreads) mine += pages_of(a.seqlens[b], a.T_q, cap);
+  for (int b = tid; b < a.B; b += kThreads) {
+    const int P = pages_of(a.seqlens[b], a.T_q, cap);
+    mine += P > 0 ? C + P : 0;
+  }
   int total;
   cta_excl_scan(mine, ctl->scan, &total);
-  const long long T = total;
-  const int Wa = part_active(T, a.W);
+  const long long U = total;
+  const int Wa = part_active(U, a.W, C);
   int n_total = 0, n_batch = 0;
-  if (T > 0 && w < Wa) {
-    const long long p0 = part_begin(T, Wa, w), p1 = part_begin(T, Wa, w + 1);
+  if (U > 0 && w < Wa) {
+    const long long x0 = part_begin(U, Wa, w), x1 = part_begin(U, Wa, w + 1);
     long long base = 0;
     int count = 0;
-    for (int c0 = 0; c0 < a.B && base < p1; c0 += kThreads) {
+    for (int c0 = 0; c0 < a.B && base < x1; c0 += kThreads) {
       const int b = c0 + tid;
       const int P = b < a.B ? pages_of(a.seqlens[b], a.T_q, cap) : 0;
       int chunk_total;
-      const int excl = cta_excl_scan(P, ctl->scan, &chunk_total);
-      const long long S = base + excl;
-      const int hit = (P > 0 && S < p1 && S + P > p0) ? 1 : 0;
+      const int excl = cta_excl_scan(P > 0 ? C + P : 0, ctl->scan, &chunk_total);
+      const long long A = base + excl + C;   // unit of the sequence's first page
+      int j0, j1;
+      part_pages(x0, x1, A, P, &j0, &j1);
+      const int hit = (P > 0 && j1 > j0) ? 1 : 0;
       int hits;
       const int idx = count + cta_excl_scan(hit, ctl->scan, &hits);
       if (hit && idx >= offset && idx < offset + kMaxItems) {
-        const long long g0 = S > p0 ? S : p0;
-        const long long g1 = (S + P) < p1 ? (S + P) : p1;
         Item it;
         it.b = b;
-        it.j0 = (int)(g0 - S);
-        it.j1 = (int)(g1 - S);
-        it.w_first = part_worker_of(T, Wa, S);
-        it.w_last = part_worker_of(T, Wa, S + P - 1);
-        it.flags = (it.j0 == 0 && it.j1 == P) ? 1 : 0;
+        it.j0 = j0;
+        it.j1 = j1;
+        it.w_first = part_worker_of(U, Wa, A);
+        it.w_last = part_worker_of(U, Wa, A + P - 1);
+        it.flags = (j0 == 0 && j1 == P) ? 1 : 0;
         ctl->items[idx - offset] = it;
       }
       count += hits;
@@ -952,6 +957,15 @@ int g_max_clusters[64] = {};
 bool tc_supported(int dtype, int H, int T_q, int d_c, int d_r) {
   // up to 128 query rows (heads x query tokens); fewer are padded to 128
   return dtype == BF16 && d_c == 512 && d_r == 64 && H * T_q >= 1 && H * T_q <= kRows;
+}
+
+int tc_item_cost(int rows) {
+  // Fixed cost of one work item, in pages: the worker loads the item's query
+  // rows through the same SM port that streams the pages, and the value CTA
+  // drains 128 x 512 fp32 of output before the next item may start.  Measured
+  // on B300 by sweeping the cost: about five pages' time at 128 query rows,
+  // three at 32.
+  return 2 + (3 * rows + 64) / 128;
 }
 
 int tc_workers(int num_sms) {

@@ -16,6 +16,7 @@ cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s);
 // decode_tc.cu (tensor-core path: bf16, D = 576, d_c = 512, H*T_q in [64, 128])
 bool tc_supported(int dtype, int H, int T_q, int d_c, int d_r);
 int tc_workers(int num_sms);
+int tc_item_cost(int rows);   // the split partition's item cost C for this kernel
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
 
 // append_absorb.cu

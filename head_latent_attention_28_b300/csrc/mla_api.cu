@@ -88,6 +88,12 @@ int decode_workers(int dtype, int B, int T_q, int H, int d_c, int d_r, int sms) 
                                                      : mla::generic_workers(sms);
 }
 
+// the split partition's item cost for the kernel a shape selects (the
+// CUDA-core kernel splits pages evenly)
+int decode_item_cost(int dtype, int T_q, int H, int d_c, int d_r) {
+  return mla::tc_supported(dtype, H, T_q, d_c, d_r) ? mla::tc_item_cost(T_q * H) : 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -183,32 +189,41 @@ size_t mla_decode_workspace_size(int B, int T_q, int H, int d_c, int d_r, int dt
 }
 
 int mla_decode_split_plan(const int32_t* seqlens_host, int B, int T_q, int max_blocks_per_seq,
-                          int num_workers, int32_t* first_worker, int32_t* last_worker,
-                          int64_t* total_pages) {
+                          int num_workers, int item_cost, int32_t* first_worker,
+                          int32_t* last_worker, int64_t* total_pages) {
   if (!seqlens_host || !first_worker || !last_worker || B < 1 || T_q < 1 ||
-      max_blocks_per_seq < 1 || num_workers < 1)
+      max_blocks_per_seq < 1 || num_workers < 1 || item_cost < 0 || item_cost > 1024)
     return MLA_ERR_INVALID_ARG;
   const long long cap = (long long)max_blocks_per_seq * MLA_PAGE_SIZE;
-  long long T = 0;
-  for (int b = 0; b < B; ++b) {
-    const long long L = seqlens_host[b];
-    if (L >= T_q && L <= cap) T += (L + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
-  }
-  long long S = 0;
-  const int Wa = mla::part_active(T, num_workers);
+  long long T = 0, U = 0;
   for (int b = 0; b < B; ++b) {
     const long long L = seqlens_host[b];
     if (L >= T_q && L <= cap) {
       const long long P = (L + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
-      first_worker[b] = mla::part_worker_of(T, Wa, S);
-      last_worker[b] = mla::part_worker_of(T, Wa, S + P - 1);
-      S += P;
+      T += P;
+      U += item_cost + P;
+    }
+  }
+  long long A = 0;   // first unit of the next valid sequence
+  const int Wa = mla::part_active(U, num_workers, item_cost);
+  for (int b = 0; b < B; ++b) {
+    const long long L = seqlens_host[b];
+    if (L >= T_q && L <= cap) {
+      const long long P = (L + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
+      first_worker[b] = mla::part_worker_of(U, Wa, A + item_cost);
+      last_worker[b] = mla::part_worker_of(U, Wa, A + item_cost + P - 1);
+      A += item_cost + P;
     } else {
       first_worker[b] = last_worker[b] = -1;
     }
   }
   if (total_pages) *total_pages = T;
   return MLA_OK;
+}
+
+int mla_decode_item_cost(int T_q, int H, int d_c, int d_r, int dtype) {
+  if (!decode_dims_ok(1, T_q, H, d_c, d_r) || !dtype_ok(dtype)) return -1;
+  return decode_item_cost(dtype, T_q, H, d_c, d_r);
 }
 
 int mla_decode_path(int T_q, int H, int d_c, int d_r, int dtype) {
@@ -247,6 +262,7 @@ int decode_impl(int stage, const void* q_lat, const void* kv_cache, int dtype,
   if (e != cudaSuccess) return note_cuda(e);
   const bool tc = mla::tc_supported(dtype, H, T_q, d_c, d_r);
   a.W = decode_workers(dtype, B, T_q, H, d_c, d_r, sms);
+  a.item_cost = decode_item_cost(dtype, T_q, H, d_c, d_r);
   const mla::WsLayout L = mla::ws_layout(B, T_q * H, d_c, a.W);
   if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);

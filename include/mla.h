@@ -231,22 +231,37 @@ int mla_absorb_output(const float* o_lat, const void* w_uv, const void* w_o, int
 
 /*
  * mla_decode_split_plan -- HOST helper: which split workers mla_decode_paged
- * assigns to each sequence, for a given worker count (no device needed).
+ * assigns to each sequence, for a given worker count and item cost (no
+ * device needed).
  *
- * The pages of all valid sequences are laid end to end (sequence b owns
- * ceil(L_b / 64) pages, T pages in all) and cut into min(num_workers, T)
- * non-empty ranges whose sizes differ by at most one page.  For each b, first_worker[b] / last_worker[b] get the
- * first and last worker whose range meets sequence b (-1 for a sequence
- * whose length is outside [T_q, 64 * max_blocks_per_seq]).  A sequence with
- * first == last is finished by one worker; otherwise its partial results are
- * merged by the log-sum-exp combine.  Returns the total page count through
- * *total_pages (may be NULL).  All pointers are host pointers.
+ * Work is laid on a cost axis: each valid sequence b covers item_cost units
+ * (the fixed cost of one work item: loading its query rows and writing its
+ * output) followed by ceil(L_b / 64) units, one per page (T pages, U units in
+ * all).  The axis is cut into W' = min(num_workers, floor(U / (item_cost + 1)))
+ * ranges whose sizes differ by at most one unit, so every active worker
+ * carries about the same cost; each range holds at least one page.  For each
+ * b, first_worker[b] / last_worker[b] get the first and last worker holding
+ * one of its pages (-1 for a sequence whose length is outside
+ * [T_q, 64 * max_blocks_per_seq]).  A sequence with first == last is finished
+ * by one worker; otherwise its partial results are merged by the
+ * log-sum-exp combine.  item_cost = 0 is the plain even split of the pages;
+ * mla_decode_paged uses mla_decode_item_cost() of the shape.  Returns the
+ * total page count through *total_pages (may be NULL).  All pointers are host
+ * pointers.
  * Host errors: NULL arrays, B < 1, T_q < 1, max_blocks_per_seq < 1,
- * num_workers < 1.
+ * num_workers < 1, item_cost outside [0, 1024].
  */
 int mla_decode_split_plan(const int32_t* seqlens_host, int B, int T_q, int max_blocks_per_seq,
-                          int num_workers, int32_t* first_worker, int32_t* last_worker,
-                          int64_t* total_pages);
+                          int num_workers, int item_cost, int32_t* first_worker,
+                          int32_t* last_worker, int64_t* total_pages);
+
+/*
+ * mla_decode_item_cost -- the item cost (in pages) mla_decode_paged gives the
+ * split partition for a shape: measured for the tensor-core kernel (about 5
+ * at 128 query rows, 3 at 32), 0 for the CUDA-core kernel.  Returns -1 for
+ * invalid dims.  Host only; needs no device.
+ */
+int mla_decode_item_cost(int T_q, int H, int d_c, int d_r, int dtype);
 
 /*
  * mla_decode_num_workers -- the worker count mla_decode_paged uses for this

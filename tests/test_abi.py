@@ -7,6 +7,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 import head_latent_attention_28_b300 as mla
 
@@ -69,42 +70,58 @@ def test_other_calls_reject_bad_arguments_on_host():
     assert lib.mla_absorb_output(P, P, P, 1, 1, 256, 256, 64, 64, P, None) == 1  # H*d_h too big
 
 
-def brute_force_plan(seqlens, T_q, max_blocks, W):
-    """Explicit page list: with W' = min(W, T) active workers, page p goes to
-    the worker w with floor(T w / W') <= p < floor(T (w+1) / W')."""
+def brute_force_plan(seqlens, T_q, max_blocks, W, C=0):
+    """Explicit unit list: each valid sequence contributes C item-cost units,
+    then one unit per page; with W' = min(W, U // (C + 1)) active workers,
+    unit u goes to the worker w with floor(U w / W') <= u < floor(U (w+1) / W').
+    Returns first/last owner of each sequence's pages, T, and per active
+    worker (pages, items)."""
     cap = max_blocks * 64
-    owners = []
-    seq_of_page = []
+    units = []                              # (sequence, is_page)
     for b, L in enumerate(seqlens):
         if T_q <= L <= cap:
-            seq_of_page += [b] * ((L + 63) // 64)
-    T = len(seq_of_page)
-    Wa = min(W, T)
+            units += [(b, False)] * C + [(b, True)] * ((L + 63) // 64)
+    U = len(units)
+    T = sum(1 for _, pg in units if pg)
+    Wa = min(W, U // (C + 1))
+    owners = []
     for w in range(Wa):
-        cnt = (T * (w + 1)) // Wa - (T * w) // Wa
-        assert cnt >= 1                     # no active worker is empty
-        owners += [w] * cnt
+        owners += [w] * ((U * (w + 1)) // Wa - (U * w) // Wa)
     first = [-1] * len(seqlens)
     last = [-1] * len(seqlens)
-    for p, b in enumerate(seq_of_page):
+    work = [[0, set()] for _ in range(Wa)]
+    for (b, pg), w in zip(units, owners):
+        if not pg:
+            continue
         if first[b] < 0:
-            first[b] = owners[p]
-        last[b] = owners[p]
-    return first, last, T
+            first[b] = w
+        last[b] = w
+        work[w][0] += 1
+        work[w][1].add(b)
+    return first, last, T, [(n, len(items)) for n, items in work]
 
 
+@pytest.mark.parametrize("C", [0, 3, 5])
 @pytest.mark.parametrize("W", [1, 3, 74, 148, 1000])
-def test_split_plan_matches_brute_force(W):
-    rng = np.random.default_rng(W)
+def test_split_plan_matches_brute_force(W, C):
+    rng = np.random.default_rng(W + 7 * C)
     for trial in range(5):
         B = int(rng.integers(1, 60))
         seqlens = rng.integers(0, 3000, size=B).astype(np.int32)
         seqlens[rng.random(B) < 0.1] = 5000       # over capacity -> invalid
-        f, l, T = mla.mla_decode_split_plan(seqlens, 2, 64, W)
-        bf, bl, bT = brute_force_plan(seqlens.tolist(), 2, 64, W)
+        f, l, T = mla.mla_decode_split_plan(seqlens, 2, 64, W, C)
+        bf, bl, bT, work = brute_force_plan(seqlens.tolist(), 2, 64, W, C)
         assert T == bT
         np.testing.assert_array_equal(f, bf)
         np.testing.assert_array_equal(l, bl)
+        # no active worker is empty, and the cost pages + C * items of the
+        # workers differs by at most 2 C + 1 units (a range holds floor or
+        # ceil of U / W' units; a worker starting inside a sequence's pages
+        # pays C for that item outside its units, and one whose range ends
+        # inside a sequence's C units holds units it does not pay for)
+        assert all(n >= 1 for n, _ in work)
+        costs = [n + C * k for n, k in work]
+        assert max(costs) - min(costs) <= 2 * C + 1
         # partial slots b + w are distinct over all (sequence, worker) pairs,
         # and every worker between a sequence's first and last holds part of it
         slots = [b + w for b in range(B) if f[b] >= 0 and f[b] != l[b]
@@ -116,5 +133,21 @@ def test_split_plan_matches_brute_force(W):
             assert f[b1] in (l[b0], l[b0] + 1)   # contiguous, no skipped worker
 
     # few pages, many workers: the case where idle workers would leave holes
-    f, l, T = mla.mla_decode_split_plan(np.array([300, 129], np.int32), 1, 8, W)
-    assert T == 8 and f[0] == 0 and l[1] == min(W, 8) - 1
+    f, l, T = mla.mla_decode_split_plan(np.array([300, 129], np.int32), 1, 8, W, C)
+    assert T == 8 and f[0] == 0 and l[1] == min(W, (8 + 2 * C) // (C + 1)) - 1
+
+
+def test_item_cost_per_kernel():
+    # tensor-core shapes: grows with the query rows (5 pages at 128 rows, 3 at 32)
+    assert mla.mla_decode_item_cost(1, 128, 512, 64) == 5
+    assert mla.mla_decode_item_cost(2, 16, 512, 64) == 3
+    assert mla.mla_decode_item_cost(1, 1, 512, 64) == 2
+    # the CUDA-core kernel splits pages evenly
+    assert mla.mla_decode_item_cost(1, 128, 512, 64, dtype=torch.float32) == 0
+    assert mla.mla_decode_item_cost(1, 8, 64, 16) == 0
+    assert mla.mla_decode_item_cost(1, 256, 512, 64) == 0
+    # invalid dims
+    assert mla.mla_decode_item_cost(0, 128, 512, 64) == -1
+    # the host plan rejects a negative cost
+    with pytest.raises(mla.MLAError):
+        mla.mla_decode_split_plan(np.array([100], np.int32), 1, 8, 4, -1)
