@@ -13,7 +13,7 @@ from ._lib import (  # noqa: F401
     MLA_ERR_TIMEOUT, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE, MLA_F32, MLA_OK, PAGE_SIZE,
     SIGNATURES, MLAError, alloc_workspace, lib, load_library, mla_absorb_output,
     mla_absorb_query, mla_cache_append, mla_check_status, mla_decode_paged,
-    mla_decode_paged_noalloc, mla_decode_workspace_size, mla_status_string, mla_decode_split_plan, mla_decode_item_cost,
+    mla_decode_paged_noalloc, mla_decode_workspace_size, mla_status_string, mla_decode_split_plan, mla_decode_item_cost, mla_decode_row_groups,
     mla_decode_num_workers)
 
 lib()  # load now: no silent fallback path exists

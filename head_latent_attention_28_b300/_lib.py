@@ -48,6 +48,7 @@ SIGNATURES = {
     "mla_version": (_I, []),
     "mla_decode_split_plan": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "mla_decode_item_cost": (_I, [_I, _I, _I, _I, _I]),
+    "mla_decode_row_groups": (_I, [_I, _I, _I, _I, _I]),
     "mla_decode_num_workers": (_I, [_I, _I, _I, _I, _I, _I]),
     "mla_decode_path": (_I, [_I, _I, _I, _I, _I]),
 }
@@ -271,6 +272,12 @@ def mla_decode_item_cost(T_q, H, d_c, d_r, dtype=torch.bfloat16) -> int:
     """The split partition's per-item cost (pages) mla_decode_paged uses for a shape."""
     code = MLA_BF16 if dtype == torch.bfloat16 else MLA_F32
     return int(lib().mla_decode_item_cost(T_q, H, d_c, d_r, code))
+
+
+def mla_decode_row_groups(T_q, H, d_c, d_r, dtype=torch.bfloat16) -> int:
+    """How many row groups (work items over the same pages) a sequence's query rows form."""
+    code = MLA_BF16 if dtype == torch.bfloat16 else MLA_F32
+    return int(lib().mla_decode_row_groups(T_q, H, d_c, d_r, code))
 
 
 def mla_decode_num_workers(B, T_q, H, d_c, d_r, dtype=torch.bfloat16) -> int:

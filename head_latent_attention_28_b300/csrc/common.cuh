@@ -96,6 +96,14 @@ struct DecodeArgs {
   float* ws_o;
   int W;                      // number of split workers
   int item_cost;              // C of the split partition (units per work item)
+  // Row groups: the tensor-core kernel handles at most 128 query rows of a
+  // sequence at a time; a sequence with more rows is planned as G "virtual
+  // sequences" (b, g), g < G, over the same pages, each with rows
+  // [g * SR, min((g + 1) * SR, T_q * H)).  Workspace slots, partials and the
+  // merge are per virtual sequence (b * G + g), SR rows each.  G = 1 and
+  // SR = T_q * H otherwise.
+  int G;
+  int SR;
   unsigned* err;              // device error word
 };
 

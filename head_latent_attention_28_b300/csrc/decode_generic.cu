@@ -279,10 +279,16 @@ __global__ void __launch_bounds__(CT) combine_kernel(DecodeArgs a) {
   // grid has completed and its writes are visible (no-op otherwise)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ float wts[];            // [CR][nw] normalised weights
-  const int b = blockIdx.x;
+  // one virtual sequence (sequence b, row group g) per blockIdx.x: its rows
+  // [g * SR, g * SR + rows_g) of the sequence, slots vb + w of the workspace
+  const int vb = blockIdx.x;
+  const int b = vb / a.G, g = vb - b * a.G;
   const int rows = a.T_q * a.H;
+  const int rows_g = min(a.SR, rows - g * a.SR);
   const int r0 = blockIdx.y * CR;
-  const int nr = min(CR, rows - r0);
+  const int nr = min(CR, rows_g - r0);
+  if (nr <= 0) return;
+  const size_t orow0 = (size_t)b * rows + (size_t)g * a.SR;   // first output row of the group
   const int L = a.seqlens[b];
   const bool valid = L >= a.T_q && L <= a.max_blocks * kPage;
   const int dc4 = a.d_c / VEC;
@@ -292,12 +298,12 @@ __global__ void __launch_bounds__(CT) combine_kernel(DecodeArgs a) {
     zero_vec(z);
     for (int idx = threadIdx.x; idx < nr * dc4; idx += CT) {
       const int rr = idx / dc4, c4 = idx - rr * dc4;
-      reinterpret_cast<V*>(a.o + ((size_t)b * rows + r0 + rr) * a.d_c)[c4] = z;
+      reinterpret_cast<V*>(a.o + (orow0 + r0 + rr) * a.d_c)[c4] = z;
     }
-    if (threadIdx.x < nr && a.lse) a.lse[(size_t)b * rows + r0 + threadIdx.x] = 0.f;
+    if (threadIdx.x < nr && a.lse) a.lse[orow0 + r0 + threadIdx.x] = 0.f;
     return;
   }
-  const int2 m = a.meta[b];
+  const int2 m = a.meta[vb];
   if (m.x == m.y) return;  // finished by its only worker
   const int nw = m.y - m.x + 1;
   // weights: one warp per row
@@ -305,12 +311,12 @@ __global__ void __launch_bounds__(CT) combine_kernel(DecodeArgs a) {
   for (int rr = warp; rr < nr; rr += CT / 32) {
     const int r = r0 + rr;
     float lmax = -INFINITY;
-    for (int k = lane; k < nw; k += 32) lmax = fmaxf(lmax, a.ws_lse[(size_t)(b + m.x + k) * rows + r]);
+    for (int k = lane; k < nw; k += 32) lmax = fmaxf(lmax, a.ws_lse[(size_t)(vb + m.x + k) * a.SR + r]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
     float sumw = 0.f;
     for (int k = lane; k < nw; k += 32) {
-      const float lw = a.ws_lse[(size_t)(b + m.x + k) * rows + r];
+      const float lw = a.ws_lse[(size_t)(vb + m.x + k) * a.SR + r];
       const float wt = (lw == -INFINITY) ? 0.f : expf(lw - lmax);
       wts[rr * nw + k] = wt;
       sumw += wt;
@@ -320,7 +326,7 @@ __global__ void __launch_bounds__(CT) combine_kernel(DecodeArgs a) {
     const float inv = sumw > 0.f ? 1.f / sumw : 0.f;
     __syncwarp();
     for (int k = lane; k < nw; k += 32) wts[rr * nw + k] *= inv;
-    if (lane == 0 && a.lse) a.lse[(size_t)b * rows + r] = sumw > 0.f ? lmax + logf(sumw) : -INFINITY;
+    if (lane == 0 && a.lse) a.lse[orow0 + r] = sumw > 0.f ? lmax + logf(sumw) : -INFINITY;
   }
   __syncthreads();
   // each thread keeps kOut outputs in registers and issues the loads of up
@@ -344,7 +350,7 @@ __global__ void __launch_bounds__(CT) combine_kernel(DecodeArgs a) {
 #pragma unroll
       for (int kk = 0; kk < kParts; ++kk) {
         const int k = min(k0 + kk, nw - 1);
-        const V* part = reinterpret_cast<const V*>(a.ws_o + (size_t)(b + m.x + k) * rows * a.d_c);
+        const V* part = reinterpret_cast<const V*>(a.ws_o + (size_t)(vb + m.x + k) * a.SR * a.d_c);
 #pragma unroll
         for (int t = 0; t < kOut; ++t) v[kk][t] = part[off[t]];
       }
@@ -355,7 +361,7 @@ __global__ void __launch_bounds__(CT) combine_kernel(DecodeArgs a) {
           for (int t = 0; t < kOut; ++t) fma_vec(wts[wrow[t] + k0 + kk], v[kk][t], acc[t]);
         }
     }
-    V* out = reinterpret_cast<V*>(a.o + (size_t)b * rows * a.d_c);
+    V* out = reinterpret_cast<V*>(a.o + orow0 * a.d_c);
 #pragma unroll
     for (int t = 0; t < kOut; ++t)
       if (base + t * CT < total) out[off[t]] = acc[t];
@@ -390,8 +396,7 @@ cudaError_t launch_decode_generic(const DecodeArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s) {
-  const int rows = a.T_q * a.H;
-  dim3 grid(a.B, (rows + CR - 1) / CR);
+  dim3 grid(a.B * a.G, (a.SR + CR - 1) / CR);
   // a sequence's parts come from at most W workers
   const size_t smem = sizeof(float) * (size_t)CR * (size_t)(a.W > 0 ? a.W : 1);
   const bool vec4 = a.d_c % 4 == 0 && (reinterpret_cast<uintptr_t>(a.o) & 15u) == 0 &&

@@ -1,7 +1,8 @@
-// Tensor-core MLA decode for sm_103a: up to 128 query rows (heads x query
-// tokens) per sequence, cached rows of 512 latent + 64 rotary bfloat16
-// numbers.  The MMAs always run M = 128 rows; fewer rows are zero padding,
-// masked out and never written.
+// Tensor-core MLA decode for sm_103a: query rows (heads x query tokens) of a
+// sequence in groups of up to 128, cached rows of 512 latent + 64 rotary
+// bfloat16 numbers.  The MMAs always run M = 128 rows; fewer rows are zero
+// padding, masked out and never written.  A sequence with more than 128 rows
+// is split into row groups, each a work item of its own over the same pages.
 //
 // What it computes is the latent-space attention of the absorbed MLA path
 // ("Attention, Part 2: MQA, GQA and MLA", the absorbed inference path: score =
@@ -48,7 +49,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kThreads = 320;            // 10 warps
-constexpr int kRows = 128;               // query rows per sequence handled here
+constexpr int kRows = 128;               // query rows per work item (one row group)
 constexpr int kBox = 8192;               // 64 tokens x 64 dims x bf16
 constexpr int kCell = 2 * kBox;          // score CTA: box c of both pages of a pair
 constexpr int kCells = 6;                // score CTA: ring depth (cells); measured on B300:
@@ -93,8 +94,9 @@ static_assert(4 * 4096 <= kPBytes, "four epilogue boxes fit in a unit's probabil
 
 struct Item {
   int b, j0, j1;            // sequence, page range [j0, j1)
-  int w_first, w_last;      // workers holding the sequence's first and last page
-  int flags;                // bit 0: this worker holds the whole sequence
+  int g, vb;                // row group, virtual sequence b * G + g
+  int w_first, w_last;      // workers holding the virtual sequence's first and last page
+  int flags;                // bit 0: this worker holds the whole (virtual) sequence
 };
 
 struct SmemCtl {
@@ -168,9 +170,10 @@ __device__ void plan_batch(const DecodeArgs& a, int w, int offset, SmemCtl* ctl)
   const int tid = threadIdx.x;
   const int cap = a.max_blocks * kPage;
   const int C = a.item_cost;
+  const int nv = a.B * a.G;   // virtual sequences (sequence, row group), b-major
   int mine = 0;
-  for (int b = tid; b < a.B; b += kThreads) {
-    const int P = pages_of(a.seqlens[b], a.T_q, cap);
+  for (int v = tid; v < nv; v += kThreads) {
+    const int P = pages_of(a.seqlens[v / a.G], a.T_q, cap);
     mine += P > 0 ? C + P : 0;
   }
   int total;
@@ -182,9 +185,10 @@ __device__ void plan_batch(const DecodeArgs& a, int w, int offset, SmemCtl* ctl)
     const long long x0 = part_begin(U, Wa, w), x1 = part_begin(U, Wa, w + 1);
     long long base = 0;
     int count = 0;
-    for (int c0 = 0; c0 < a.B && base < x1; c0 += kThreads) {
-      const int b = c0 + tid;
-      const int P = b < a.B ? pages_of(a.seqlens[b], a.T_q, cap) : 0;
+    for (int c0 = 0; c0 < nv && base < x1; c0 += kThreads) {
+      const int v = c0 + tid;
+      const int b = v < nv ? v / a.G : 0;
+      const int P = v < nv ? pages_of(a.seqlens[b], a.T_q, cap) : 0;
       int chunk_total;
       const int excl = cta_excl_scan(P > 0 ? C + P : 0, ctl->scan, &chunk_total);
       const long long A = base + excl + C;   // unit of the sequence's first page
@@ -196,6 +200,8 @@ __device__ void plan_batch(const DecodeArgs& a, int w, int offset, SmemCtl* ctl)
       if (hit && idx >= offset && idx < offset + kMaxItems) {
         Item it;
         it.b = b;
+        it.g = v - b * a.G;
+        it.vb = v;
         it.j0 = j0;
         it.j1 = j1;
         it.w_first = part_worker_of(U, Wa, A);
@@ -305,7 +311,8 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
   const uint32_t tmem = ctl.tmem_base;
 
   const float sl2 = a.scale * kLog2e;
-  const int rows = a.T_q * a.H;   // query rows of a sequence (<= kRows; the MMAs
+  const int rows = a.T_q * a.H;   // query rows of a sequence (a work item takes
+                                  // the <= 128 rows of one row group; the MMAs
                                   // always run 128 rows, the rest are zero padding)
   const int cap = a.max_blocks * kPage;
 
@@ -508,21 +515,23 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
       const uint32_t peer_precv = mapa(smem_u32(&ctl.p_recv[0]), 1);   // + 8 * slot
       uint32_t un_s = 0;   // leader: unit counter
       const bool leader = threadIdx.x == 64;
-      const int t = r / a.H;
       uint8_t* qr = smem + kOffQr;
       for (int ii = 0; ii < n_items; ++ii) {
         if (__any_sync(0xffffffffu, *abort_flag)) break;
         const Item it = ctl.items[ii];
         const int L = a.seqlens[it.b];
-        // padding rows (r >= rows) see no token at all
-        const int lim = r >= rows ? -1 : a.causal ? (L - a.T_q + t) : (L - 1);
+        const int rb = kRows * it.g;                   // first row of the group
+        const int rows_g = min(kRows, rows - rb);       // its real rows
+        const int t = (rb + r) / a.H;                  // query token of this row
+        // padding rows (r >= rows_g) see no token at all
+        const int lim = r >= rows_g ? -1 : a.causal ? (L - a.T_q + t) : (L - 1);
         const int n = it.j1 - it.j0;
         // the query row: latent dims -> TMEM (half 0: [0, 256), half 1: [256, 512)),
         // rotary dims -> shared memory (K-major SW128; half h: 16-byte chunks 4h..4h+3)
         {
-          const bool real = r < rows;
+          const bool real = r < rows_g;
           const uint4* src = reinterpret_cast<const uint4*>(
-              static_cast<const __nv_bfloat16*>(a.q) + ((size_t)it.b * rows + (real ? r : 0)) * a.D);
+              static_cast<const __nv_bfloat16*>(a.q) + ((size_t)it.b * rows + rb + (real ? r : 0)) * a.D);
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t v[32];
@@ -567,7 +576,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
           if (lane == 0) mbar_arrive(&ctl.s_free[sb]);     // score buffer reusable
           // mask (tokens past the visible range, a missing page, a bad block id)
           const int tok0 = jh * kPage;
-          if (!page_ok || tok0 + 63 > L - a.T_q || r >= rows) {
+          if (!page_ok || tok0 + 63 > L - a.T_q || r >= rows_g) {
             const int lim_page = page_ok ? lim : -1;
 #pragma unroll
             for (int q = 0; q < 64; ++q) x[q] = (tok0 + q <= lim_page) ? x[q] : -INFINITY;
@@ -639,12 +648,12 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
             ctl.rowl[half][r] = l_half;
             if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { ok = false; break; }
             l_tot = ctl.rowl[0][r] + ctl.rowl[1][r];
-            if (half == 0 && r < rows) {
+            if (half == 0 && r < rows_g) {
               const float lse = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
-              const int wslot = it.b + w;
-              if (it.flags & 1) { if (a.lse) a.lse[(size_t)it.b * rows + r] = lse; }
-              else a.ws_lse[(size_t)wslot * rows + r] = lse;
-              if (r == 0 && it.j0 == 0) a.meta[it.b] = make_int2(it.w_first, it.w_last);
+              const int wslot = it.vb + w;
+              if (it.flags & 1) { if (a.lse) a.lse[(size_t)it.b * rows + rb + r] = lse; }
+              else a.ws_lse[(size_t)wslot * a.SR + r] = lse;
+              if (r == 0 && it.j0 == 0) a.meta[it.vb] = make_int2(it.w_first, it.w_last);
             }
           }
           // per-row (alpha, l): the rescale factor rides on the pair's first
@@ -807,9 +816,10 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
         const float l_row = reinterpret_cast<const float*>(ps_last + kPBytes + 16)[2 * r + 1];
         const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
         const bool whole = it.flags & 1;
-        const int grp_rows = min(32, rows - 32 * q4);   // real rows of this warp's group
-        float* out_base = (whole ? a.o + (size_t)it.b * rows * a.d_c
-                                 : a.ws_o + (size_t)(it.b + w) * rows * a.d_c) + 256 * ch;
+        const int rb = kRows * it.g;                            // first row of the row group
+        const int grp_rows = min(32, min(kRows, rows - rb) - 32 * q4);   // real rows of this warp's group
+        float* out_base = (whole ? a.o + ((size_t)it.b * rows + rb) * a.d_c
+                                 : a.ws_o + (size_t)(it.vb + w) * a.SR * a.d_c) + 256 * ch;
         if (grp_rows > 0) out_base += (size_t)(32 * q4) * a.d_c;
         // every thread must have read l before the staging writes below
         __syncwarp();
@@ -817,7 +827,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
           // whole 32-row group: 32 x 32 fp32 boxes staged (SW128) in the
           // slot's probability areas (not its factors) and written by TMA
           const CUtensorMap* tmo = whole ? &tm_o : &tm_ws;
-          const int row0 = (whole ? it.b : it.b + w) * rows + 32 * q4;
+          const int row0 = (whole ? it.b * rows + rb : (it.vb + w) * a.SR) + 32 * q4;
           const int wi = warp - 2;
           uint8_t* box = wi < 4 ? ps_last + wi * 4096 : ps_lo + (wi - 4) * 4096;
 #pragma unroll 1
@@ -956,8 +966,8 @@ int g_max_clusters[64] = {};
 }  // namespace
 
 bool tc_supported(int dtype, int H, int T_q, int d_c, int d_r) {
-  // up to 128 query rows (heads x query tokens); fewer are padded to 128
-  return dtype == BF16 && d_c == 512 && d_r == 64 && H * T_q >= 1 && H * T_q <= kRows;
+  // query rows (heads x query tokens) in groups of up to 128; a short group is padded
+  return dtype == BF16 && d_c == 512 && d_r == 64 && H * T_q >= 1;
 }
 
 int tc_item_cost(int rows) {
@@ -1005,7 +1015,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   const uint64_t rows = (uint64_t)a.T_q * a.H;
   e = make_map(&tm_o, a.o, (uint64_t)a.d_c, (uint64_t)a.B * rows, 32, 32, true);
   if (e != cudaSuccess) return e;
-  e = make_map(&tm_ws, a.ws_o, (uint64_t)a.d_c, (uint64_t)(a.B + a.W) * rows, 32, 32, true);
+  e = make_map(&tm_ws, a.ws_o, (uint64_t)a.d_c, ((uint64_t)a.B * a.G + a.W) * a.SR, 32, 32, true);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;

@@ -91,7 +91,22 @@ int decode_workers(int dtype, int B, int T_q, int H, int d_c, int d_r, int sms) 
 // the split partition's item cost for the kernel a shape selects (the
 // CUDA-core kernel splits pages evenly)
 int decode_item_cost(int dtype, int T_q, int H, int d_c, int d_r) {
-  return mla::tc_supported(dtype, H, T_q, d_c, d_r) ? mla::tc_item_cost(T_q * H) : 0;
+  return mla::tc_supported(dtype, H, T_q, d_c, d_r) ? mla::tc_item_cost(T_q * H < 128 ? T_q * H : 128)
+                                                     : 0;
+}
+
+// row groups of the kernel a shape selects: the tensor-core kernel takes at
+// most 128 query rows per work item (G groups of SR rows), the CUDA-core
+// kernel all rows of a sequence
+void decode_row_groups(int dtype, int T_q, int H, int d_c, int d_r, int* G, int* SR) {
+  const int rows = T_q * H;
+  if (mla::tc_supported(dtype, H, T_q, d_c, d_r) && rows > 128) {
+    *G = (rows + 127) / 128;
+    *SR = 128;
+  } else {
+    *G = 1;
+    *SR = rows;
+  }
 }
 
 }  // namespace
@@ -185,7 +200,10 @@ size_t mla_decode_workspace_size(int B, int T_q, int H, int d_c, int d_r, int dt
   int sms = 0;
   if (device_info(nullptr, &sms) != cudaSuccess) return 0;
   const int W = decode_workers(dtype, B, T_q, H, d_c, d_r, sms);
-  return mla::ws_layout(B, T_q * H, d_c, W).total;
+  int G = 1, SR = 1;
+  decode_row_groups(dtype, T_q, H, d_c, d_r, &G, &SR);
+  if ((long long)B * G > (1 << 30)) return 0;
+  return mla::ws_layout(B * G, SR, d_c, W).total;
 }
 
 int mla_decode_split_plan(const int32_t* seqlens_host, int B, int T_q, int max_blocks_per_seq,
@@ -226,6 +244,13 @@ int mla_decode_item_cost(int T_q, int H, int d_c, int d_r, int dtype) {
   return decode_item_cost(dtype, T_q, H, d_c, d_r);
 }
 
+int mla_decode_row_groups(int T_q, int H, int d_c, int d_r, int dtype) {
+  if (!decode_dims_ok(1, T_q, H, d_c, d_r) || !dtype_ok(dtype)) return -1;
+  int G = 1, SR = 1;
+  decode_row_groups(dtype, T_q, H, d_c, d_r, &G, &SR);
+  return G;
+}
+
 int mla_decode_path(int T_q, int H, int d_c, int d_r, int dtype) {
   if (!decode_dims_ok(1, T_q, H, d_c, d_r) || !dtype_ok(dtype)) return -1;
   return mla::tc_supported(dtype, H, T_q, d_c, d_r) ? 1 : 0;
@@ -263,7 +288,9 @@ int decode_impl(int stage, const void* q_lat, const void* kv_cache, int dtype,
   const bool tc = mla::tc_supported(dtype, H, T_q, d_c, d_r);
   a.W = decode_workers(dtype, B, T_q, H, d_c, d_r, sms);
   a.item_cost = decode_item_cost(dtype, T_q, H, d_c, d_r);
-  const mla::WsLayout L = mla::ws_layout(B, T_q * H, d_c, a.W);
+  decode_row_groups(dtype, T_q, H, d_c, d_r, &a.G, &a.SR);
+  if ((long long)B * a.G > (1 << 30)) return MLA_ERR_INVALID_ARG;
+  const mla::WsLayout L = mla::ws_layout(B * a.G, a.SR, d_c, a.W);
   if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   a.q = q_lat; a.cache = kv_cache; a.block_table = block_table; a.seqlens = seqlens;

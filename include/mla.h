@@ -145,8 +145,9 @@ size_t mla_decode_workspace_size(int B, int T_q, int H, int d_c, int d_r, int dt
  *   workspace, workspace_bytes           >= mla_decode_workspace_size(...)
  * Long or ragged batches are split into page ranges processed in parallel
  * (partial softmax results in the workspace) and merged by a log-sum-exp
- * combine kernel.  The bf16 shape d_c = 512, d_r = 64, H*T_q <= 128 runs the
- * tensor-core (tcgen05/TMEM) kernel; every other shape a CUDA-core kernel.
+ * combine kernel.  The bf16 shape d_c = 512, d_r = 64 runs the tensor-core
+ * (tcgen05/TMEM) kernel, any H*T_q (rows in groups of up to 128, see
+ * mla_decode_row_groups); every other shape a CUDA-core kernel.
  * Host errors: NULL pointers, B/T_q/H < 1, d_c < 1 or > 512, d_r < 0,
  * D > 1024, page_size != 64, max_blocks_per_seq < 1, num_blocks < 1.
  * Device errors (MLA_ERR_BAD_INDEX): L_b < T_q or L_b > 64*max_blocks_per_seq
@@ -262,6 +263,18 @@ int mla_decode_split_plan(const int32_t* seqlens_host, int B, int T_q, int max_b
  * invalid dims.  Host only; needs no device.
  */
 int mla_decode_item_cost(int T_q, int H, int d_c, int d_r, int dtype);
+
+/*
+ * mla_decode_row_groups -- how many row groups the decode forms of a
+ * sequence's T_q * H query rows: the tensor-core kernel handles at most 128
+ * rows per work item, so a sequence with more rows becomes G = ceil(rows/128)
+ * work items over the same pages (rows [128 g, 128 g + 128)); 1 for the
+ * CUDA-core kernel.  The split partition then runs over the B * G virtual
+ * sequences in order (sequence-major): mla_decode_split_plan gives their
+ * workers when each length is repeated G times.  Returns -1 for invalid dims.
+ * Host only; needs no device.
+ */
+int mla_decode_row_groups(int T_q, int H, int d_c, int d_r, int dtype);
 
 /*
  * mla_decode_num_workers -- the worker count mla_decode_paged uses for this

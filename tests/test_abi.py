@@ -145,9 +145,24 @@ def test_item_cost_per_kernel():
     # the CUDA-core kernel splits pages evenly
     assert mla.mla_decode_item_cost(1, 128, 512, 64, dtype=torch.float32) == 0
     assert mla.mla_decode_item_cost(1, 8, 64, 16) == 0
-    assert mla.mla_decode_item_cost(1, 256, 512, 64) == 0
+    # more than 128 rows: row groups of 128 on the tensor-core kernel
+    assert mla.mla_decode_item_cost(1, 256, 512, 64) == 5
+    assert mla.mla_decode_item_cost(3, 24, 512, 64) == 4      # 72 rows
     # invalid dims
     assert mla.mla_decode_item_cost(0, 128, 512, 64) == -1
     # the host plan rejects a negative cost
     with pytest.raises(mla.MLAError):
         mla.mla_decode_split_plan(np.array([100], np.int32), 1, 8, 4, -1)
+
+
+def test_row_groups_per_kernel():
+    assert mla.mla_decode_row_groups(1, 128, 512, 64) == 1
+    assert mla.mla_decode_row_groups(2, 128, 512, 64) == 2
+    assert mla.mla_decode_row_groups(3, 64, 512, 64) == 2      # 192 rows: 128 + 64
+    assert mla.mla_decode_row_groups(8, 128, 512, 64) == 8
+    assert mla.mla_decode_row_groups(2, 128, 512, 64, dtype=torch.float32) == 1
+    assert mla.mla_decode_row_groups(1, 8, 64, 16) == 1
+    assert mla.mla_decode_row_groups(0, 8, 512, 64) == -1
+    # the tensor-core path takes any row count for d_c = 512, d_r = 64, bf16
+    assert mla.lib().mla_decode_path(2, 128, 512, 64, mla.MLA_BF16) == 1
+    assert mla.lib().mla_decode_path(2, 128, 512, 64, mla.MLA_F32) == 0

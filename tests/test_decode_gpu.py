@@ -38,6 +38,16 @@ MEDIUM = [
                   seqlens=(2, 300, 4000)),
     mi.DecodeSpec("h32_tq4_causal", seed=16, B=3, H=32, T_q=4, causal=True,
                   seqlens=(4, 67, 1500)),
+    # more than 128 query rows: the tensor-core kernel takes them in row groups
+    # of 128 over the same pages (the last group may be short)
+    mi.DecodeSpec("h128_tq2_causal_row_groups", seed=26, B=3, H=128, T_q=2, causal=True,
+                  seqlens=(2, 1000, 2050)),
+    mi.DecodeSpec("h32_tq8_causal_row_groups", seed=27, B=2, H=32, T_q=8, causal=True,
+                  seqlens=(300, 1500)),
+    mi.DecodeSpec("h64_tq3_causal_short_group", seed=28, B=3, H=64, T_q=3, causal=True,
+                  seqlens=(3, 200, 1300)),
+    mi.DecodeSpec("h128_tq4_four_groups", seed=29, B=2, H=128, T_q=4, causal=True,
+                  seqlens=(65, 700)),
     mi.DecodeSpec("h8_small_rows", seed=17, B=2, H=8, d_c=64, d_r=16, seqlens=(129, 40),
                   softmax_scale=1 / math.sqrt(48)),
     mi.DecodeSpec("many_short_seqs", seed=18, B=600, H=16, seqlen_range=(1, 200)),
