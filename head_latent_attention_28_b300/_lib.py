@@ -49,6 +49,9 @@ SIGNATURES = {
     "mla_decode_split_plan": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "mla_decode_item_cost": (_I, [_I, _I, _I, _I, _I]),
     "mla_decode_row_groups": (_I, [_I, _I, _I, _I, _I]),
+    "mla_decode_step_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "mla_decode_step": (_I, [_P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I,
+                             _I, _I, _F, _I, _F, _P, _SZ, _P, _P, _P]),
     "mla_decode_num_workers": (_I, [_I, _I, _I, _I, _I, _I]),
     "mla_decode_path": (_I, [_I, _I, _I, _I, _I]),
 }
@@ -272,6 +275,50 @@ def mla_decode_item_cost(T_q, H, d_c, d_r, dtype=torch.bfloat16) -> int:
     """The split partition's per-item cost (pages) mla_decode_paged uses for a shape."""
     code = MLA_BF16 if dtype == torch.bfloat16 else MLA_F32
     return int(lib().mla_decode_item_cost(T_q, H, d_c, d_r, code))
+
+
+def alloc_step_workspace(B, T_q, H, d_c, d_r, dtype=torch.bfloat16, device="cuda"):
+    code = MLA_BF16 if dtype == torch.bfloat16 else MLA_F32
+    n = int(lib().mla_decode_step_workspace_size(B, T_q, H, d_c, d_r, code))
+    if n == 0:
+        raise ValueError("invalid decode dims")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def mla_decode_step(q_nope, q_rope, w_uk, c_new, k_rope_new, kv_cache, block_table, seqlens, *,
+                    softmax_scale, causal=False, rope_base=10000.0, workspace=None, o_lat=None,
+                    lse=None, want_lse=True, stream=None):
+    """One decode step: absorb q_nope/q_rope [B*T_q, H, .] into q_lat, append the new
+    tokens' rows [c_new ; RoPE(k_rope_new)] at positions seqlens[b] - T_q + t, attend.
+    Returns (o_lat [B, T_q, H, d_c] float32, lse [B, T_q, H] float32 or None)."""
+    N, H, d_h = q_nope.shape
+    d_r = q_rope.shape[2]
+    num_blocks, page, D = kv_cache.shape
+    d_c = D - d_r
+    B = block_table.shape[0]
+    if N % B or w_uk.shape != (H * d_h, d_c) or c_new.shape != (N, d_c) or \
+            k_rope_new.shape != (N, d_r) or seqlens.shape != (B,):
+        raise ValueError("shape mismatch")
+    T_q = N // B
+    if any(t.dtype != kv_cache.dtype for t in (q_nope, q_rope, w_uk, c_new, k_rope_new)):
+        raise TypeError("all step inputs share the cache dtype")
+    if workspace is None:
+        workspace = alloc_step_workspace(B, T_q, H, d_c, d_r, kv_cache.dtype, kv_cache.device)
+    if o_lat is None:
+        o_lat = torch.empty((B, T_q, H, d_c), dtype=torch.float32, device=kv_cache.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, T_q, H), dtype=torch.float32, device=kv_cache.device)
+    st = lib().mla_decode_step(
+        _dev(q_nope, "q_nope"), _dev(q_rope, "q_rope"), _dev(w_uk, "w_uk"), d_h,
+        _dev(c_new, "c_new"), _dev(k_rope_new, "k_rope_new"), _dev(kv_cache, "kv_cache"),
+        _dtype_code(kv_cache), _dev(block_table, "block_table", torch.int32),
+        _dev(seqlens, "seqlens", torch.int32), B, T_q, H, d_c, d_r, page, block_table.shape[1],
+        num_blocks, float(softmax_scale), int(bool(causal)), float(rope_base),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev(o_lat, "o_lat", torch.float32), _dev(lse, "lse", torch.float32) if lse is not None else None,
+        _stream(stream))
+    _check(st, "mla_decode_step")
+    return o_lat, lse
 
 
 def mla_decode_row_groups(T_q, H, d_c, d_r, dtype=torch.bfloat16) -> int:

@@ -1,10 +1,18 @@
 // Cache append, query absorption and output absorption kernels.
 //
-// None of these is on the per-step hot loop (each touches O(new tokens)
-// data), so they are written for exactness and simplicity: float
-// accumulation, RoPE angles and rotations in double precision.
+// Each touches O(new tokens) data per step.  The append and the output
+// absorption are written for exactness and simplicity (float accumulation,
+// RoPE angles and rotations in double precision).  The query absorption,
+// a per-head [tokens x d_h] . [d_h x 512] product that reads the whole W^UK
+// once per step, has a tensor-core kernel for bf16 (below) and a plain one
+// for everything else.
+#include <cuda.h>
+
+#include <cmath>
+
 #include "common.cuh"
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace mla {
 
@@ -32,11 +40,52 @@ __device__ __forceinline__ void rope_pair(double x1, double x2, int pos, int j, 
   *y2 = x1 * sn + x2 * cs;
 }
 
+// Rotary frequencies as turns per position, base^(-2j/d_r) / (2 pi), in
+// 64-bit fixed point (computed on the host in double precision): the angle of
+// position s is then s * turn[j] modulo one turn, exact in integer arithmetic
+// up to the rounding of turn[j], with no large angle to reduce.
+constexpr int kAbMaxPairs = 256;             // rotary pairs (d_r / 2) the table holds
+struct RopeFreqs {
+  uint64_t turn[kAbMaxPairs];
+};
+
+RopeFreqs rope_freqs(float base, int d_r) {
+  RopeFreqs fr{};
+  for (int j = 0; j < d_r / 2 && j < kAbMaxPairs; ++j) {
+    const double turns = std::pow((double)base, -2.0 * (double)j / (double)d_r) /
+                         6.283185307179586476925286766559;   // < 1
+    fr.turn[j] = (uint64_t)std::ldexp(turns, 64);
+  }
+  return fr;
+}
+
+// the angle of pair j at position pos, in half turns (angle / pi) in [-1, 1):
+// the 64-bit product pos * turn[j] wraps around whole turns
+__device__ __forceinline__ double rope_half_turns(const RopeFreqs& fr, int pos, int j) {
+  return (double)(int64_t)((uint64_t)(int64_t)pos * fr.turn[j]) * 0x1p-63;
+}
+
+// decode-step mode: token i is query token t = i % T_q of sequence b = i / T_q,
+// at position seqlens[b] - T_q + t
+__device__ __forceinline__ int step_position(const int32_t* seqlens, int T_q, int i, int* b) {
+  *b = i / T_q;
+  return seqlens[*b] - T_q + (i - *b * T_q);
+}
+
 // One CTA per new token: row (seq, pos) <- [c ; RoPE_pos(k_rope)].
 template <typename Tin, typename Tc>
-__global__ void __launch_bounds__(128) cache_append_kernel(AppendArgs a) {
+__global__ void __launch_bounds__(128) cache_append_kernel(AppendArgs a, const __grid_constant__ RopeFreqs fr) {
+  // inside mla_decode_step: the query absorption before this kernel must be
+  // complete before this one is (the decode waits for this kernel only)
+  if (a.step) asm volatile("griddepcontrol.wait;" ::: "memory");
   const int i = blockIdx.x;
-  const int b = a.seq_ids[i], pos = a.positions[i];
+  int b, pos;
+  if (a.seq_ids) {
+    b = a.seq_ids[i];
+    pos = a.positions[i];
+  } else {
+    pos = step_position(a.seqlens, a.T_q, i, &b);
+  }
   const int D = a.d_c + a.d_r;
   if (b < 0 || b >= a.B || pos < 0 || pos >= a.max_blocks * kPage) {
     if (threadIdx.x == 0) atomicOr(a.err, kErrBadIndex);
@@ -54,8 +103,18 @@ __global__ void __launch_bounds__(128) cache_append_kernel(AppendArgs a) {
     row[k] = cast_outf<Tc>(load_as_float(c, k));
   for (int j = threadIdx.x; j < a.d_r / 2; j += blockDim.x) {
     double y1, y2;
-    rope_pair(load_as_float(kr, 2 * j), load_as_float(kr, 2 * j + 1), pos, j, a.d_r,
-              (double)a.rope_base, &y1, &y2);
+    if (a.d_r / 2 <= kAbMaxPairs) {
+      // the angle exactly as a fraction of a turn; sine, cosine and the
+      // rotation in double precision
+      double sn, cs;
+      sincospi(rope_half_turns(fr, pos, j), &sn, &cs);
+      const double x1 = load_as_float(kr, 2 * j), x2 = load_as_float(kr, 2 * j + 1);
+      y1 = x1 * cs - x2 * sn;
+      y2 = x1 * sn + x2 * cs;
+    } else {
+      rope_pair(load_as_float(kr, 2 * j), load_as_float(kr, 2 * j + 1), pos, j, a.d_r,
+                (double)a.rope_base, &y1, &y2);
+    }
     row[a.d_c + 2 * j] = cast_out<Tc>(y1);
     row[a.d_c + 2 * j + 1] = cast_out<Tc>(y2);
   }
@@ -79,7 +138,8 @@ __global__ void __launch_bounds__(128) absorb_query_kernel(AbsorbQArgs a) {
     for (int d = 0; d < a.d_h; ++d) acc = fmaf(qn[d], load_as_float(w, (size_t)d * a.d_c + c), acc);
     out[c] = cast_outf<Tq>(acc);
   }
-  const int pos = a.positions[n];
+  int bq;
+  const int pos = a.positions ? a.positions[n] : step_position(a.seqlens, a.T_q, n, &bq);
   for (int j = threadIdx.x; j < a.d_r / 2; j += blockDim.x) {
     double y1, y2;
     rope_pair(load_as_float(q_rope, 2 * j), load_as_float(q_rope, 2 * j + 1), pos, j, a.d_r,
@@ -87,6 +147,182 @@ __global__ void __launch_bounds__(128) absorb_query_kernel(AbsorbQArgs a) {
     out[a.d_c + 2 * j] = cast_out<Tq>(y1);
     out[a.d_c + 2 * j + 1] = cast_out<Tq>(y2);
   }
+}
+
+// Tensor-core query absorption (bf16, d_c = 512, d_h = 64 or 128): one CTA
+// per (head h, tile of 128 tokens).  TMA brings W^UK_h (d_h x 512, kept
+// MN-major: eight 64-column chunks of d_h rows, SW128) and the tile's q_nope
+// rows (K-major SW128, one 64-dim box per 64 of d_h) into shared memory; one
+// thread issues tcgen05.mma with M = 128 tokens, N = 256, K = 16 into TMEM
+// (all 512 fp32 columns); the four warps read their 32 tokens back (token r
+// in TMEM lane r) and write q_lat with 16-byte stores, then rotate the rotary
+// query.  Tokens past N are zero rows (TMA fill) and are not written.  Waits
+// are bounded (2 s); on expiry the kernel sets MLA_ERR_TIMEOUT and writes
+// nothing.
+constexpr int kAbT = 128;                    // threads = tokens per CTA
+constexpr int kAbSmem = 2 * 16384 + 8 * 128 * 128 + 1024;
+constexpr uint64_t kAbWaitNs = 2000000000ull;
+
+__device__ __forceinline__ void store32(float* dst, const float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+__device__ __forceinline__ void store32(__nv_bfloat16* dst, const float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 p = __floats2bfloat162_rn(v[8 * i + 2 * e], v[8 * i + 2 * e + 1]);
+      w[e] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+template <typename Tq>
+__global__ void __launch_bounds__(kAbT, 1)
+absorb_query_tc_kernel(const AbsorbQArgs a, const __grid_constant__ CUtensorMap tm_qn,
+                       const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ RopeFreqs fr) {
+  using namespace sm100;
+  extern __shared__ uint8_t ab_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ab_smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ uint64_t full, done;
+  __shared__ uint32_t tbase;
+  __shared__ int failed, never;
+  // inside mla_decode_step the next kernel (the cache append) may launch now
+  if (a.step) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int warp = threadIdx.x >> 5;
+  const int h = blockIdx.x, n0 = blockIdx.y * kAbT;
+  const int kb = a.d_h / 64;                        // 64-dim boxes of q_nope along K
+  const uint32_t wchunk = (uint32_t)a.d_h * 128;    // bytes of one 64-column chunk of W^UK_h
+  uint8_t* sa = smem;                               // q_nope tile
+  uint8_t* sw = smem + 2 * 16384;                   // W^UK_h
+  if (threadIdx.x == 0) {
+    failed = 0;
+    never = 0;
+    mbar_init(&full, 1);
+    mbar_init(&done, 1);
+    fence_mbar_init_cluster();
+  }
+  if (warp == 0) tmem_alloc(&tbase, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tbase;
+  if (threadIdx.x == 0) {
+    const uint64_t pol = policy_evict_first();
+    mbar_arrive_expect_tx(&full, (uint32_t)kb * 16384 + 8 * wchunk);
+    for (int k = 0; k < kb; ++k) tma_load_3d(sa + k * 16384, &tm_qn, &full, 64 * k, h, n0, pol);
+    for (int j = 0; j < 8; ++j) tma_load_2d(sw + j * wchunk, &tm_w, &full, 64 * j, h * a.d_h, pol);
+    if (mbar_wait(&full, 0, &never, kAbWaitNs)) {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16_f32(128, 256, 0, 1);   // A K-major, B MN-major
+      for (int nh = 0; nh < 2; ++nh)
+        for (int kk = 0; kk < a.d_h / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(smem_u32(sa + (kk >> 2) * 16384 + (kk & 3) * 32), 16, 1024);
+          const uint64_t bd = sdesc_sw128(smem_u32(sw + nh * 4 * wchunk + kk * 2048), wchunk, 1024);
+          mma_ss(tmem + nh * 256, ad, bd, id, kk > 0 ? 1 : 0);
+        }
+      mma_commit(&done);
+    } else {
+      failed = 1;
+      atomicOr(a.err, kErrTimeout);
+      mbar_wait(&full, 0, &never, kAbWaitNs);   // the copies in flight land before the CTA exits
+    }
+  }
+  __syncwarp();
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(&done, 0, &failed, kAbWaitNs));
+  tc_fence_after();
+  const int n = n0 + threadIdx.x;                   // the token of this TMEM lane
+  const int D = a.d_c + a.d_r;
+  Tq* out = static_cast<Tq*>(a.q_lat) + ((size_t)(n < a.N ? n : 0) * a.H + h) * D;
+  if (ok) {
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+#pragma unroll 1
+    for (int c = 0; c < 16; ++c) {
+      float v[32];
+      tmem_ld32(tmem + lane_off + 32 * c, v);
+      tmem_ld_wait();
+      if (n < a.N) store32(out + 32 * c, v);
+    }
+    // rotary dims: the angle as a fraction of a turn in [-1/2, 1/2), from the
+    // 64-bit product position * turn[j] (its wrap-around drops the whole
+    // turns); sine, cosine and the rotation in float
+    if (n < a.N) {
+      const __nv_bfloat16* q_rope =
+          static_cast<const __nv_bfloat16*>(a.q_rope) + ((size_t)n * a.H + h) * a.d_r;
+      int bq;
+      const int p = a.positions ? a.positions[n] : step_position(a.seqlens, a.T_q, n, &bq);
+      const uint64_t pos = (uint64_t)(int64_t)p;   // two's complement: modular product
+      for (int j = 0; j < a.d_r / 2; ++j) {
+        const float half_turns = (float)(int64_t)(pos * fr.turn[j]) * 0x1p-63f;   // angle / pi
+        float sn, cs;
+        sincospif(half_turns, &sn, &cs);
+        const float x1 = load_as_float(q_rope, 2 * j), x2 = load_as_float(q_rope, 2 * j + 1);
+        out[a.d_c + 2 * j] = cast_outf<Tq>(x1 * cs - x2 * sn);
+        out[a.d_c + 2 * j + 1] = cast_outf<Tq>(x1 * sn + x2 * cs);
+      }
+    }
+  } else if (threadIdx.x == 0) {
+    atomicOr(a.err, kErrTimeout);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+bool absorb_tc_ok(const AbsorbQArgs& a) {
+  const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  return a.dtype == BF16 && a.d_c == 512 && (a.d_h == 64 || a.d_h == 128) && a.N >= 1 &&
+         a.d_r / 2 <= kAbMaxPairs && a.err != nullptr && al16(a.q_nope) && al16(a.w_uk) &&
+         al16(a.q_lat) && (long long)a.H * a.d_h < (1LL << 31) && (long long)a.N <= 65535LL * kAbT;
+}
+
+cudaError_t launch_absorb_query_tc(const AbsorbQArgs& a, cudaStream_t s) {
+  TensorMapEncodeFn enc = nullptr;
+  cudaError_t e = tensor_map_encoder(&enc);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tm_qn, tm_w;
+  {
+    // q_nope [N, H, d_h] as a 3-D tensor: box of 64 dims x 1 head x 128 tokens
+    cuuint64_t dims[3] = {(cuuint64_t)a.d_h, (cuuint64_t)a.H, (cuuint64_t)a.N};
+    cuuint64_t strides[2] = {(cuuint64_t)a.d_h * 2, (cuuint64_t)a.H * a.d_h * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)kAbT};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&tm_qn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q_nope), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // w_uk [H * d_h, 512]: box of 64 columns x d_h rows (one head)
+    cuuint64_t dims[2] = {(cuuint64_t)a.d_c, (cuuint64_t)a.H * a.d_h};
+    cuuint64_t strides[1] = {(cuuint64_t)a.d_c * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)a.d_h};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.w_uk), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const RopeFreqs fr = rope_freqs(a.rope_base, a.d_r);
+  dim3 grid(a.H, (a.N + kAbT - 1) / kAbT), block(kAbT);
+  if (a.q_dtype == F32) {
+    e = cudaFuncSetAttribute(absorb_query_tc_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAbSmem);
+    if (e != cudaSuccess) return e;
+    absorb_query_tc_kernel<float><<<grid, block, kAbSmem, s>>>(a, tm_qn, tm_w, fr);
+  } else {
+    e = cudaFuncSetAttribute(absorb_query_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAbSmem);
+    if (e != cudaSuccess) return e;
+    absorb_query_tc_kernel<__nv_bfloat16><<<grid, block, kAbSmem, s>>>(a, tm_qn, tm_w, fr);
+  }
+  return cudaGetLastError();
 }
 
 constexpr int AO_T = 256;    // threads
@@ -128,16 +364,26 @@ __global__ void __launch_bounds__(AO_T) absorb_output_kernel(AbsorbOArgs a) {
 
 cudaError_t launch_cache_append(const AppendArgs& a, cudaStream_t s) {
   if (a.n_new == 0) return cudaSuccess;
-  dim3 grid(a.n_new), block(128);
-  if (a.dtype_in == F32 && a.cache_dtype == F32) cache_append_kernel<float, float><<<grid, block, 0, s>>>(a);
-  else if (a.dtype_in == F32) cache_append_kernel<float, __nv_bfloat16><<<grid, block, 0, s>>>(a);
-  else if (a.cache_dtype == F32) cache_append_kernel<__nv_bfloat16, float><<<grid, block, 0, s>>>(a);
-  else cache_append_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, block, 0, s>>>(a);
-  return cudaGetLastError();
+  const RopeFreqs fr = rope_freqs(a.rope_base, a.d_r);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_new);
+  cfg.blockDim = dim3(128);
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = a.step ? 1 : 0;
+  if (a.dtype_in == F32 && a.cache_dtype == F32)
+    return cudaLaunchKernelEx(&cfg, cache_append_kernel<float, float>, a, fr);
+  if (a.dtype_in == F32) return cudaLaunchKernelEx(&cfg, cache_append_kernel<float, __nv_bfloat16>, a, fr);
+  if (a.cache_dtype == F32) return cudaLaunchKernelEx(&cfg, cache_append_kernel<__nv_bfloat16, float>, a, fr);
+  return cudaLaunchKernelEx(&cfg, cache_append_kernel<__nv_bfloat16, __nv_bfloat16>, a, fr);
 }
 
 cudaError_t launch_absorb_query(const AbsorbQArgs& a, cudaStream_t s) {
   if (a.N == 0) return cudaSuccess;
+  if (absorb_tc_ok(a)) return launch_absorb_query_tc(a, s);
   dim3 grid(a.N, a.H), block(128);
   size_t smem = sizeof(float) * a.d_h;
   if (a.dtype == F32 && a.q_dtype == F32) absorb_query_kernel<float, float><<<grid, block, smem, s>>>(a);

@@ -1004,6 +1004,12 @@ int tc_workers(int num_sms) {
   return g_max_clusters[dev];
 }
 
+cudaError_t tensor_map_encoder(TensorMapEncodeFn* fn) {
+  const cudaError_t e = get_encode();
+  if (e == cudaSuccess) *fn = g_encode;
+  return e;
+}
+
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;

@@ -1,12 +1,20 @@
 // Launchers shared between the translation units of the library (internal).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "common.cuh"
 
 namespace mla {
+
+// cuTensorMapEncodeTiled from the driver, looked up once (decode_tc.cu)
+using TensorMapEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                       const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                       const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                       CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+cudaError_t tensor_map_encoder(TensorMapEncodeFn* fn);
 
 // decode_generic.cu
 int generic_workers(int num_sms);
@@ -27,12 +35,23 @@ struct AppendArgs {
   void* cache; int cache_dtype; int num_blocks;
   int d_c, d_r; float rope_base;
   unsigned* err;
+  // decode-step mode (seq_ids == positions == nullptr): token i is query
+  // token t = i % T_q of sequence b = i / T_q, at position seqlens[b] - T_q + t
+  const int32_t* seqlens = nullptr;
+  int T_q = 1;
+  bool step = false;   // launched as a programmatic dependent inside mla_decode_step
 };
 cudaError_t launch_cache_append(const AppendArgs& a, cudaStream_t s);
 
 struct AbsorbQArgs {
   const void* q_nope; const void* q_rope; const int32_t* positions; const void* w_uk;
   int dtype; int N, H, d_h, d_c, d_r; float rope_base; void* q_lat; int q_dtype;
+  unsigned* err;   // device error word (timeouts of the tensor-core kernel)
+  // decode-step mode (positions == nullptr): token n is query token
+  // t = n % T_q of sequence b = n / T_q, at position seqlens[b] - T_q + t
+  const int32_t* seqlens = nullptr;
+  int T_q = 1;
+  bool step = false;   // first kernel of mla_decode_step: lets its dependents launch early
 };
 cudaError_t launch_absorb_query(const AbsorbQArgs& a, cudaStream_t s);
 

@@ -177,8 +177,11 @@ int mla_absorb_query(const void* q_nope, const void* q_rope, const int32_t* posi
   if (!q_nope || (d_r > 0 && !q_rope) || !positions || !w_uk || !q_lat)
     return MLA_ERR_INVALID_ARG;
   mla::AbsorbQArgs a{q_nope, q_rope, positions, w_uk, dtype, N, H, d_h, d_c, d_r,
-                     rope_base, q_lat, q_dtype};
+                     rope_base, q_lat, q_dtype, nullptr};
   if (H > 65535) return MLA_ERR_UNSUPPORTED;
+  int sms = 0;
+  cudaError_t ei = device_info(&a.err, &sms);
+  if (ei != cudaSuccess) return note_cuda(ei);
   cudaError_t e = mla::launch_absorb_query(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : note_cuda(e);
 }
@@ -373,4 +376,64 @@ int mla_decode_combine(const void* q_lat, const void* kv_cache, int dtype,
                      workspace, workspace_bytes, o_lat, lse, stream);
 }
 
+
+// ---------------------------------------------------------------------------
+// One decode step: absorb the new queries, append the new tokens' rows, attend.
+// ---------------------------------------------------------------------------
+static size_t step_q_bytes(int B, int T_q, int H, int d_c, int d_r, int dtype) {
+  const size_t es = dtype == MLA_BF16 ? 2 : 4;
+  return mla::align_up((size_t)B * (size_t)T_q * (size_t)H * (size_t)(d_c + d_r) * es, 256);
+}
+
+size_t mla_decode_step_workspace_size(int B, int T_q, int H, int d_c, int d_r, int dtype) {
+  const size_t dec = mla_decode_workspace_size(B, T_q, H, d_c, d_r, dtype);
+  if (dec == 0) return 0;
+  return step_q_bytes(B, T_q, H, d_c, d_r, dtype) + dec;
+}
+
+int mla_decode_step(const void* q_nope, const void* q_rope, const void* w_uk, int d_h,
+                    const void* c_new, const void* k_rope_new, void* kv_cache, int dtype,
+                    const int32_t* block_table, const int32_t* seqlens,
+                    int B, int T_q, int H, int d_c, int d_r, int page_size,
+                    int max_blocks_per_seq, int num_blocks, float softmax_scale, int causal,
+                    float rope_base, void* workspace, size_t workspace_bytes,
+                    float* o_lat, float* lse, void* stream) {
+  if (!q_nope || (d_r > 0 && (!q_rope || !k_rope_new)) || !w_uk || !c_new || !kv_cache ||
+      !block_table || !seqlens || !o_lat)
+    return MLA_ERR_INVALID_ARG;
+  if (!decode_dims_ok(B, T_q, H, d_c, d_r) || !dtype_ok(dtype) || d_h < 1 || d_h > 12288 ||
+      (d_r & 1) || !(rope_base > 0.f) || H > 65535 || (long long)B * T_q > (1LL << 30))
+    return MLA_ERR_INVALID_ARG;
+  const size_t qb = step_q_bytes(B, T_q, H, d_c, d_r, dtype);
+  const size_t need = mla_decode_step_workspace_size(B, T_q, H, d_c, d_r, dtype);
+  if (need == 0) return MLA_ERR_CUDA;
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MLA_ERR_WORKSPACE;
+  unsigned* err = nullptr;
+  cudaError_t e = device_info(&err, nullptr);
+  if (e != cudaSuccess) return note_cuda(e);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* q_lat = workspace;                       // [B, T_q, H, d_c + d_r] in the cache dtype
+  const int N = B * T_q;
+  // 1. q_lat = [W^UK^T q_nope ; RoPE(q_rope)] at the new tokens' positions
+  mla::AbsorbQArgs aq{q_nope, q_rope, nullptr, w_uk, dtype, N, H, d_h, d_c, d_r,
+                      rope_base, q_lat, dtype, err};
+  aq.seqlens = seqlens;
+  aq.T_q = T_q;
+  aq.step = true;
+  e = mla::launch_absorb_query(aq, s);
+  if (e != cudaSuccess) return note_cuda(e);
+  // 2. the new tokens' rows [c ; RoPE(k_rope)] into the cache
+  mla::AppendArgs ap{c_new, k_rope_new, dtype, nullptr, nullptr, N, block_table, B,
+                     max_blocks_per_seq, kv_cache, dtype, num_blocks, d_c, d_r, rope_base, err};
+  ap.seqlens = seqlens;
+  ap.T_q = T_q;
+  ap.step = true;
+  e = mla::launch_cache_append(ap, s);
+  if (e != cudaSuccess) return note_cuda(e);
+  // 3. attention over the cache, split pass and merge
+  return decode_impl(kStageBoth, q_lat, kv_cache, dtype, block_table, seqlens, B, T_q, H, d_c,
+                     d_r, page_size, max_blocks_per_seq, num_blocks, softmax_scale, causal,
+                     static_cast<char*>(workspace) + qb, workspace_bytes - qb, o_lat, lse, stream);
+}
 }  // extern "C"

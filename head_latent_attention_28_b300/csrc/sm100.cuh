@@ -227,6 +227,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* desc, uint64_
       "l"(desc), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(cache_hint)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* desc, uint64_t* bar, int c0,
+                                            int c1, int c2, uint64_t cache_hint) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(desc), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(cache_hint)
+      : "memory");
+}
 // L2 cache policies (createpolicy fractional)
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

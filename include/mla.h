@@ -216,6 +216,41 @@ int mla_decode_combine(const void* q_lat, const void* kv_cache, int dtype,
                        float* o_lat, float* lse, void* stream);
 
 /*
+ * mla_decode_step -- one decode step of the absorbed MLA layer in one call:
+ * the chain "The MLA equations" / "The trick that makes it fast" describe for
+ * new tokens (cache the latent and the rotated decoupled key, absorb W^UK
+ * into the query, attend in latent space).
+ *
+ * For sequence b with L_b = seqlens[b] cached rows INCLUDING its T_q new
+ * tokens, new token t sits at position s = L_b - T_q + t and has flat index
+ * i = b * T_q + t.  In stream order:
+ *   1. q_lat[b, t, h] = [ W^UK_h^T q_nope[i, h] ; RoPE_s(q_rope[i, h]) ]
+ *      (as mla_absorb_query, stored in the cache dtype in the workspace);
+ *   2. cache row (b, s) <- [ c_new[i] ; RoPE_s(k_rope_new[i]) ]
+ *      (as mla_cache_append);
+ *   3. o_lat, lse = mla_decode_paged over the cache with q_lat.
+ * The cache append is launched as a programmatic dependent of the query
+ * absorption (its launch overlaps the absorption's tail).
+ *
+ *   q_nope [B*T_q, H, d_h], q_rope [B*T_q, H, d_r], w_uk [H*d_h, d_c],
+ *   c_new [B*T_q, d_c], k_rope_new [B*T_q, d_r]: all in `dtype`, the cache's
+ *   dtype; the other arguments as for mla_decode_paged.
+ *   workspace: >= mla_decode_step_workspace_size(...) bytes, 256-byte aligned
+ *   (q_lat first, then the decode's split workspace).
+ * Host errors: those of the three calls; MLA_ERR_WORKSPACE for a small or
+ * misaligned workspace.  Device errors: as the three calls (a position
+ * outside the block table, a bad block id, an invalid length).
+ */
+size_t mla_decode_step_workspace_size(int B, int T_q, int H, int d_c, int d_r, int dtype);
+int mla_decode_step(const void* q_nope, const void* q_rope, const void* w_uk, int d_h,
+                    const void* c_new, const void* k_rope_new, void* kv_cache, int dtype,
+                    const int32_t* block_table, const int32_t* seqlens,
+                    int B, int T_q, int H, int d_c, int d_r, int page_size,
+                    int max_blocks_per_seq, int num_blocks, float softmax_scale, int causal,
+                    float rope_base, void* workspace, size_t workspace_bytes,
+                    float* o_lat, float* lse, void* stream);
+
+/*
  * mla_absorb_output -- apply W^UV per head, then W^O, to the attended latent.
  *
  *   o[n, h, v] = sum_c w_uv[h*d_h + v, c] * o_lat[n, h, c]

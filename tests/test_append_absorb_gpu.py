@@ -90,6 +90,31 @@ def test_absorb_query_matches_oracle(dtype):
     np.testing.assert_allclose(out.double().cpu().numpy(), want, rtol=0, atol=2e-5)
 
 
+@pytest.mark.parametrize("d_h", [64, 128])
+def test_absorb_query_tensor_core_tiles(d_h):
+    """bf16 inputs with d_c = 512 take the tensor-core kernel: 200 tokens are
+    two tiles of 128 (the second ragged); bf16 output within one rounding step
+    of the fp64 oracle, fp32 output within float accumulation error."""
+    rng = np.random.default_rng(44 + d_h)
+    N, H, d_c, d_r = 200, 16, 512, 64
+    qn, qr = (mi.bf16_bits_to_f32(mi.f32_to_bf16_bits(x)).reshape(x.shape) for x in
+              (rng.standard_normal((N, H, d_h)).astype(np.float32),
+               rng.standard_normal((N, H, d_r)).astype(np.float32)))
+    w = (rng.standard_normal((H * d_h, d_c)) / np.sqrt(d_h)).astype(np.float32)
+    w = mi.bf16_bits_to_f32(mi.f32_to_bf16_bits(w)).reshape(w.shape)
+    pos = rng.integers(0, 1 << 17, size=N).astype(np.int32)
+    args = [torch.from_numpy(x).cuda().to(torch.bfloat16) for x in (qn, qr)]
+    want = orc.absorb_query(qn, qr, pos, w, 10000.0)
+    out32 = mla.mla_absorb_query(args[0], args[1], torch.from_numpy(pos).cuda(),
+                                 torch.from_numpy(w).cuda().to(torch.bfloat16), q_dtype=torch.float32)
+    out16 = mla.mla_absorb_query(args[0], args[1], torch.from_numpy(pos).cuda(),
+                                 torch.from_numpy(w).cuda().to(torch.bfloat16), q_dtype=torch.bfloat16)
+    assert mla.mla_check_status() == mla.MLA_OK
+    np.testing.assert_allclose(out32.double().cpu().numpy(), want, rtol=0, atol=2e-5)
+    got = out16.double().cpu().numpy()
+    assert np.all(np.abs(got - want) <= bf16_ulp(want) + 1e-5)
+
+
 def test_absorb_query_bf16_output_rounds_once():
     rng = np.random.default_rng(42)
     N, H, d_h, d_c, d_r = 3, 16, 64, 512, 64
