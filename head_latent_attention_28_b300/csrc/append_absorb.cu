@@ -72,13 +72,13 @@ __device__ __forceinline__ int step_position(const int32_t* seqlens, int T_q, in
   return seqlens[*b] - T_q + (i - *b * T_q);
 }
 
-// One CTA per new token: row (seq, pos) <- [c ; RoPE_pos(k_rope)].
+// Row (seq, pos) of new token i <- [c ; RoPE_pos(k_rope)], written by nthr
+// threads (index tid) together.  The angle is exact as a fraction of a turn;
+// sine, cosine and the rotation run in float for a bf16 cache (whose rounding
+// is far coarser) and in double for an fp32 one.
 template <typename Tin, typename Tc>
-__global__ void __launch_bounds__(128) cache_append_kernel(AppendArgs a, const __grid_constant__ RopeFreqs fr) {
-  // inside mla_decode_step: the query absorption before this kernel must be
-  // complete before this one is (the decode waits for this kernel only)
-  if (a.step) asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int i = blockIdx.x;
+__device__ __forceinline__ void write_cache_row(const AppendArgs& a, const RopeFreqs& fr, int i,
+                                                int tid, int nthr) {
   int b, pos;
   if (a.seq_ids) {
     b = a.seq_ids[i];
@@ -88,36 +88,53 @@ __global__ void __launch_bounds__(128) cache_append_kernel(AppendArgs a, const _
   }
   const int D = a.d_c + a.d_r;
   if (b < 0 || b >= a.B || pos < 0 || pos >= a.max_blocks * kPage) {
-    if (threadIdx.x == 0) atomicOr(a.err, kErrBadIndex);
+    if (tid == 0) atomicOr(a.err, kErrBadIndex);
     return;
   }
   const int blk = a.block_table[(size_t)b * a.max_blocks + pos / kPage];
   if (blk < 0 || blk >= a.num_blocks) {
-    if (threadIdx.x == 0) atomicOr(a.err, kErrBadIndex);
+    if (tid == 0) atomicOr(a.err, kErrBadIndex);
     return;
   }
   const Tin* c = static_cast<const Tin*>(a.c) + (size_t)i * a.d_c;
   const Tin* kr = static_cast<const Tin*>(a.k_rope) + (size_t)i * a.d_r;
   Tc* row = static_cast<Tc*>(a.cache) + ((size_t)blk * kPage + pos % kPage) * D;
-  for (int k = threadIdx.x; k < a.d_c; k += blockDim.x)
-    row[k] = cast_outf<Tc>(load_as_float(c, k));
-  for (int j = threadIdx.x; j < a.d_r / 2; j += blockDim.x) {
-    double y1, y2;
-    if (a.d_r / 2 <= kAbMaxPairs) {
-      // the angle exactly as a fraction of a turn; sine, cosine and the
-      // rotation in double precision
+  if (nthr == 1 && sizeof(Tin) == 2 && sizeof(Tc) == 2 && a.d_c % 8 == 0 &&
+      ((reinterpret_cast<uintptr_t>(c) | reinterpret_cast<uintptr_t>(row)) & 15u) == 0) {
+    // one thread per row: the bf16 latent moves unchanged, 16 bytes at a time
+    for (int k = 0; k < a.d_c / 8; ++k)
+      reinterpret_cast<uint4*>(row)[k] = reinterpret_cast<const uint4*>(c)[k];
+  } else {
+    for (int k = tid; k < a.d_c; k += nthr) row[k] = cast_outf<Tc>(load_as_float(c, k));
+  }
+  for (int j = tid; j < a.d_r / 2; j += nthr) {
+    const float x1 = load_as_float(kr, 2 * j), x2 = load_as_float(kr, 2 * j + 1);
+    if (a.d_r / 2 > kAbMaxPairs) {
+      double y1, y2;
+      rope_pair(x1, x2, pos, j, a.d_r, (double)a.rope_base, &y1, &y2);
+      row[a.d_c + 2 * j] = cast_out<Tc>(y1);
+      row[a.d_c + 2 * j + 1] = cast_out<Tc>(y2);
+    } else if (sizeof(Tc) == 2) {
+      float sn, cs;
+      sincospif((float)rope_half_turns(fr, pos, j), &sn, &cs);
+      row[a.d_c + 2 * j] = cast_outf<Tc>(x1 * cs - x2 * sn);
+      row[a.d_c + 2 * j + 1] = cast_outf<Tc>(x1 * sn + x2 * cs);
+    } else {
       double sn, cs;
       sincospi(rope_half_turns(fr, pos, j), &sn, &cs);
-      const double x1 = load_as_float(kr, 2 * j), x2 = load_as_float(kr, 2 * j + 1);
-      y1 = x1 * cs - x2 * sn;
-      y2 = x1 * sn + x2 * cs;
-    } else {
-      rope_pair(load_as_float(kr, 2 * j), load_as_float(kr, 2 * j + 1), pos, j, a.d_r,
-                (double)a.rope_base, &y1, &y2);
+      row[a.d_c + 2 * j] = cast_out<Tc>((double)x1 * cs - (double)x2 * sn);
+      row[a.d_c + 2 * j + 1] = cast_out<Tc>((double)x1 * sn + (double)x2 * cs);
     }
-    row[a.d_c + 2 * j] = cast_out<Tc>(y1);
-    row[a.d_c + 2 * j + 1] = cast_out<Tc>(y2);
   }
+}
+
+// One CTA per new token.
+template <typename Tin, typename Tc>
+__global__ void __launch_bounds__(128) cache_append_kernel(AppendArgs a, const __grid_constant__ RopeFreqs fr) {
+  // inside mla_decode_step: the query absorption before this kernel must be
+  // complete before this one is (the decode waits for this kernel only)
+  if (a.step) asm volatile("griddepcontrol.wait;" ::: "memory");
+  write_cache_row<Tin, Tc>(a, fr, blockIdx.x, threadIdx.x, blockDim.x);
 }
 
 // One CTA per (token n, head h):
@@ -184,7 +201,8 @@ __device__ __forceinline__ void store32(__nv_bfloat16* dst, const float (&v)[32]
 template <typename Tq>
 __global__ void __launch_bounds__(kAbT, 1)
 absorb_query_tc_kernel(const AbsorbQArgs a, const __grid_constant__ CUtensorMap tm_qn,
-                       const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ RopeFreqs fr) {
+                       const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ RopeFreqs fr,
+                       const AppendArgs ap) {
   using namespace sm100;
   extern __shared__ uint8_t ab_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ab_smem_raw) + 1023) &
@@ -234,6 +252,13 @@ absorb_query_tc_kernel(const AbsorbQArgs a, const __grid_constant__ CUtensorMap 
     }
   }
   __syncwarp();
+  // inside mla_decode_step these CTAs also append the new tokens' cache rows
+  // while the tensor core works: token n0 + t goes to the CTA of head
+  // t mod H, whose threads write its row together (the same arithmetic as
+  // the append kernel)
+  if (ap.n_new > 0)
+    for (int t = h; t < kAbT && n0 + t < ap.n_new; t += a.H)
+      write_cache_row<__nv_bfloat16, __nv_bfloat16>(ap, fr, n0 + t, threadIdx.x, kAbT);
   const bool ok = __all_sync(0xffffffffu, mbar_wait(&done, 0, &failed, kAbWaitNs));
   tc_fence_after();
   const int n = n0 + threadIdx.x;                   // the token of this TMEM lane
@@ -284,7 +309,7 @@ bool absorb_tc_ok(const AbsorbQArgs& a) {
          al16(a.q_lat) && (long long)a.H * a.d_h < (1LL << 31) && (long long)a.N <= 65535LL * kAbT;
 }
 
-cudaError_t launch_absorb_query_tc(const AbsorbQArgs& a, cudaStream_t s) {
+cudaError_t launch_absorb_query_tc(const AbsorbQArgs& a, const AppendArgs& ap, cudaStream_t s) {
   TensorMapEncodeFn enc = nullptr;
   cudaError_t e = tensor_map_encoder(&enc);
   if (e != cudaSuccess) return e;
@@ -316,11 +341,11 @@ cudaError_t launch_absorb_query_tc(const AbsorbQArgs& a, cudaStream_t s) {
   if (a.q_dtype == F32) {
     e = cudaFuncSetAttribute(absorb_query_tc_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAbSmem);
     if (e != cudaSuccess) return e;
-    absorb_query_tc_kernel<float><<<grid, block, kAbSmem, s>>>(a, tm_qn, tm_w, fr);
+    absorb_query_tc_kernel<float><<<grid, block, kAbSmem, s>>>(a, tm_qn, tm_w, fr, ap);
   } else {
     e = cudaFuncSetAttribute(absorb_query_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAbSmem);
     if (e != cudaSuccess) return e;
-    absorb_query_tc_kernel<__nv_bfloat16><<<grid, block, kAbSmem, s>>>(a, tm_qn, tm_w, fr);
+    absorb_query_tc_kernel<__nv_bfloat16><<<grid, block, kAbSmem, s>>>(a, tm_qn, tm_w, fr, ap);
   }
   return cudaGetLastError();
 }
@@ -383,7 +408,11 @@ cudaError_t launch_cache_append(const AppendArgs& a, cudaStream_t s) {
 
 cudaError_t launch_absorb_query(const AbsorbQArgs& a, cudaStream_t s) {
   if (a.N == 0) return cudaSuccess;
-  if (absorb_tc_ok(a)) return launch_absorb_query_tc(a, s);
+  if (absorb_tc_ok(a)) {
+    AppendArgs none{};
+    none.n_new = 0;
+    return launch_absorb_query_tc(a, none, s);
+  }
   dim3 grid(a.N, a.H), block(128);
   size_t smem = sizeof(float) * a.d_h;
   if (a.dtype == F32 && a.q_dtype == F32) absorb_query_kernel<float, float><<<grid, block, smem, s>>>(a);
@@ -391,6 +420,18 @@ cudaError_t launch_absorb_query(const AbsorbQArgs& a, cudaStream_t s) {
   else if (a.q_dtype == F32) absorb_query_kernel<__nv_bfloat16, float><<<grid, block, smem, s>>>(a);
   else absorb_query_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, block, smem, s>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_absorb_and_append(const AbsorbQArgs& a, const AppendArgs& ap, cudaStream_t s) {
+  // one kernel when the absorption runs on the tensor cores and the cache is
+  // bf16 like the query; otherwise the two kernels, the append as a
+  // programmatic dependent of the absorption
+  if (absorb_tc_ok(a) && a.q_dtype == BF16 && ap.dtype_in == BF16 && ap.cache_dtype == BF16 &&
+      ap.n_new == a.N && ap.d_c == a.d_c && ap.d_r == a.d_r && ap.rope_base == a.rope_base)
+    return launch_absorb_query_tc(a, ap, s);
+  cudaError_t e = launch_absorb_query(a, s);
+  if (e != cudaSuccess) return e;
+  return launch_cache_append(ap, s);
 }
 
 cudaError_t launch_absorb_output(const AbsorbOArgs& a, cudaStream_t s) {

@@ -54,6 +54,8 @@ struct AbsorbQArgs {
   bool step = false;   // first kernel of mla_decode_step: lets its dependents launch early
 };
 cudaError_t launch_absorb_query(const AbsorbQArgs& a, cudaStream_t s);
+// the first two stages of mla_decode_step (query absorption, cache append)
+cudaError_t launch_absorb_and_append(const AbsorbQArgs& a, const AppendArgs& ap, cudaStream_t s);
 
 struct AbsorbOArgs {
   const float* o_lat; const void* w_uv; const void* w_o; int dtype;

@@ -421,15 +421,14 @@ int mla_decode_step(const void* q_nope, const void* q_rope, const void* w_uk, in
   aq.seqlens = seqlens;
   aq.T_q = T_q;
   aq.step = true;
-  e = mla::launch_absorb_query(aq, s);
-  if (e != cudaSuccess) return note_cuda(e);
-  // 2. the new tokens' rows [c ; RoPE(k_rope)] into the cache
+  // 2. the new tokens' rows [c ; RoPE(k_rope)] into the cache (in the same
+  //    kernel as 1 when the absorption runs on the tensor cores)
   mla::AppendArgs ap{c_new, k_rope_new, dtype, nullptr, nullptr, N, block_table, B,
                      max_blocks_per_seq, kv_cache, dtype, num_blocks, d_c, d_r, rope_base, err};
   ap.seqlens = seqlens;
   ap.T_q = T_q;
   ap.step = true;
-  e = mla::launch_cache_append(ap, s);
+  e = mla::launch_absorb_and_append(aq, ap, s);
   if (e != cudaSuccess) return note_cuda(e);
   // 3. attention over the cache, split pass and merge
   return decode_impl(kStageBoth, q_lat, kv_cache, dtype, block_table, seqlens, B, T_q, H, d_c,
