@@ -48,6 +48,11 @@ MEDIUM = [
                   seqlens=(3, 200, 1300)),
     mi.DecodeSpec("h128_tq4_four_groups", seed=29, B=2, H=128, T_q=4, causal=True,
                   seqlens=(65, 700)),
+    # a causal chunk of 32 new tokens (chunked prefill through the absorbed
+    # path): 32 row groups of 128 rows over the same pages, each query token
+    # sees the cache up to itself
+    mi.DecodeSpec("h128_chunk32_causal", seed=30, B=2, H=128, T_q=32, causal=True,
+                  seqlens=(32, 500)),
     mi.DecodeSpec("h8_small_rows", seed=17, B=2, H=8, d_c=64, d_r=16, seqlens=(129, 40),
                   softmax_scale=1 / math.sqrt(48)),
     mi.DecodeSpec("many_short_seqs", seed=18, B=600, H=16, seqlen_range=(1, 200)),
