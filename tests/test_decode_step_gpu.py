@@ -20,6 +20,9 @@ CASES = [
     (mi.DecodeSpec("step_h128", seed=50, B=3, H=128, seqlens=(70, 300, 129)), 128),
     (mi.DecodeSpec("step_h16_tq2", seed=51, B=3, H=16, T_q=2, causal=True,
                    seqlens=(2, 200, 65), softmax_scale=1 / math.sqrt(192)), 64),
+    # multi-token step with 256 query rows per sequence: two row groups
+    (mi.DecodeSpec("step_h128_tq2_row_groups", seed=53, B=2, H=128, T_q=2, causal=True,
+                   seqlens=(2, 333)), 128),
     # CUDA-core decode and plain absorption
     (mi.DecodeSpec("step_small_dims", seed=52, B=2, H=8, d_c=64, d_r=16, seqlens=(129, 40),
                    softmax_scale=1 / math.sqrt(48)), 32),
