@@ -851,7 +851,10 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
           if (lane == 0) bulk_wait_read0();         // staging free before the slot is handed back
           __syncwarp();
         }
-        float4* stg = reinterpret_cast<float4*>(ps_last + (warp - 2) * 2048);   // 32 rows x 4 float4
+        // a warp's own 4 KB of the two units (the same region its TMA boxes
+        // would use, so a partial group never overlaps another warp's box)
+        float4* stg = reinterpret_cast<float4*>((warp - 2) < 4 ? ps_last + (warp - 2) * 4096
+                                                                : ps_lo + (warp - 6) * 4096);   // 32 rows x 4 float4
 #pragma unroll 1
         for (int c = 0; c < (grp_rows > 0 && grp_rows < 32 ? 4 : 0); ++c) {
           float o[64];

@@ -48,6 +48,13 @@ MEDIUM = [
                   seqlens=(3, 200, 1300)),
     mi.DecodeSpec("h128_tq4_four_groups", seed=29, B=2, H=128, T_q=4, causal=True,
                   seqlens=(65, 700)),
+    # row counts that are not a multiple of 32: the last 32-row group of the
+    # epilogue is partial (72 = 2 x 32 + 8 rows; 40 = 32 + 8)
+    mi.DecodeSpec("h24_tq3_rows72", seed=31, B=5, H=24, T_q=3,
+                  seqlens=(3, 700, 1500, 64, 2100)),
+    mi.DecodeSpec("h40_causal_tq1_rows40", seed=32, B=3, H=40, seqlens=(129, 1, 900)),
+    mi.DecodeSpec("h20_tq2_causal_rows40", seed=33, B=3, H=20, T_q=2, causal=True,
+                  seqlens=(2, 500, 1200)),
     # a causal chunk of 32 new tokens (chunked prefill through the absorbed
     # path): 32 row groups of 128 rows over the same pages, each query token
     # sees the cache up to itself
