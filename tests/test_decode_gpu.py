@@ -260,3 +260,30 @@ def test_full_size_workload_sampled(spec):
     for b in batch:
         assert_decode_close(o[b], want_o[b], what=f"{spec.name} seq {b}")
         np.testing.assert_allclose(lse[b], want_l[b], rtol=0, atol=2e-2)
+
+
+def _random_specs(n, seed):
+    """Seeded random shapes: any head count and query-token count (row groups
+    and partial 32-row epilogue groups), causal or not, ragged lengths."""
+    rng = np.random.default_rng(seed)
+    specs = []
+    for k in range(n):
+        H, T_q = int(rng.integers(1, 129)), int(rng.integers(1, 9))
+        B = int(rng.integers(1, 5))
+        causal = bool(rng.random() < 0.5)
+        lens = tuple(int(x) for x in rng.integers(T_q, 1500, size=B))
+        specs.append(mi.DecodeSpec(f"random{k}_h{H}_tq{T_q}", seed=seed * 100 + k, B=B, H=H,
+                                   T_q=T_q, causal=causal, seqlens=lens))
+    return specs
+
+
+RANDOM = _random_specs(10, 61)
+
+
+@pytest.mark.parametrize("spec", RANDOM, ids=[s.name for s in RANDOM])
+def test_random_shapes_match_oracle(spec):
+    inp = mi.make_decode_inputs(spec)
+    o, lse = run_decode(inp)
+    want_o, want_lse = oracle_all(inp)
+    assert_decode_close(o, want_o, what=spec.name)
+    np.testing.assert_allclose(lse, want_lse, rtol=0, atol=2e-2)
