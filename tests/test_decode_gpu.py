@@ -63,6 +63,8 @@ MEDIUM = [
     mi.DecodeSpec("h8_small_rows", seed=17, B=2, H=8, d_c=64, d_r=16, seqlens=(129, 40),
                   softmax_scale=1 / math.sqrt(48)),
     mi.DecodeSpec("many_short_seqs", seed=18, B=600, H=16, seqlen_range=(1, 200)),
+    # more than 64 work items per worker: the planner hands them out in batches
+    mi.DecodeSpec("items_beyond_one_batch", seed=34, B=5000, H=8, seqlen_range=(1, 64)),
 ]
 
 
