@@ -27,11 +27,17 @@
 //    the receiver's barrier).
 //  * CTA 1, the value CTA, keeps the full 128 x 512 fp32 output in tensor
 //    memory (all 512 columns), streams the 512 latent dims of the same pages
-//    in half-page units through a 4-deep ring (the second read of a page is
+//    in half-page units through a 3-deep ring (the second read of a page is
 //    an L2 hit) and accumulates O += P . V with tcgen05.mma (A = P from shared
-//    memory, B = V MN-major, N = 256 per half).  Four warps apply row
-//    rescales and zero the rows of a last page past the sequence end (0 x NaN
-//    would poison O); eight warps write the normalised output.
+//    memory, B = V MN-major, N = 256 per half).  The probabilities arrive in
+//    a ring of six 18 KB units (one per page, two when the page also sends
+//    the low bf16 parts of its probabilities).  Four warps apply row rescales
+//    and zero the rows of a last page past the sequence end (0 x NaN would
+//    poison O); eight warps write the normalised output with TMA tensor
+//    stores (or the split's partial output, merged later).
+//  * Each worker takes a contiguous range of the cost-weighted split
+//    partition (common.cuh): work items are (sequence, row group, page
+//    range), planned on the device in batches of up to 64.
 // The data flow is one-way (score CTA -> value CTA), so the distributed-
 // shared-memory latency is pipelined, never on a round trip.
 // Every mbarrier wait is bounded (2 s): on expiry the kernel records
