@@ -305,6 +305,18 @@ __global__ void __launch_bounds__(CT) combine_kernel(DecodeArgs a) {
   }
   const int2 m = a.meta[vb];
   if (m.x == m.y) return;  // finished by its only worker
+  if (m.x < 0 || m.y < m.x || m.y >= a.W) {
+    // no consistent merge record (the partial pass gave up before writing
+    // it): report and write zeros rather than follow it
+    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(a.err, kErrTimeout);
+    V z;
+    zero_vec(z);
+    for (int idx = threadIdx.x; idx < nr * dc4; idx += CT) {
+      const int rr = idx / dc4, c4 = idx - rr * dc4;
+      reinterpret_cast<V*>(a.o + (orow0 + r0 + rr) * a.d_c)[c4] = z;
+    }
+    return;
+  }
   const int nw = m.y - m.x + 1;
   // weights: one warp per row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

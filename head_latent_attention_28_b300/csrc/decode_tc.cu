@@ -328,6 +328,14 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
   uint32_t g_page = 0;                 // pages (score softmax, value MMA and warps)
   uint32_t it_cnt = 0;                 // items (MMA issuers, value warps)
   uint32_t grp_phase = 0, n_resc = 0, n_vz = 0;
+  // probability-unit counters: they run on across planning batches, like the
+  // mbarrier phases they index
+  uint32_t un = 0;                     // value MMA: units consumed
+  uint32_t un_s = 0;                   // score leader: units sent
+  // value row warps: units seen, and per unit slot the parity of the next
+  // phase of its page barriers (pv_done, rows_seen advance only when the slot
+  // holds a page's first unit)
+  uint32_t un_v = 0, pvpar = 0, prev_slot = 0, prev_par = 0;
 
   for (int offset = 0;; offset += kMaxItems) {
     plan_batch(a, w, offset, &ctl);
@@ -447,7 +455,6 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
           }
         } else {
           const uint32_t idPV = idesc_bf16_f32(128, 256, 0, 1);
-          uint32_t un = 0;       // unit counter
           for (int ii = 0; ii < n_items && !*abort_flag; ++ii) {
             const Item it = ctl.items[ii];
             const int L = a.seqlens[it.b];
@@ -519,7 +526,6 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
       const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
       const uint32_t peer_p = mapa(smem_u32(pslots), 1);               // value CTA's slots
       const uint32_t peer_precv = mapa(smem_u32(&ctl.p_recv[0]), 1);   // + 8 * slot
-      uint32_t un_s = 0;   // leader: unit counter
       const bool leader = threadIdx.x == 64;
       uint8_t* qr = smem + kOffQr;
       for (int ii = 0; ii < n_items; ++ii) {
@@ -686,9 +692,9 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
               *reinterpret_cast<uint4*>(st + kPBytes) = make_uint4(fl, 0u, 0u, 0u);
               fence_proxy_async_smem();
               for (uint32_t part = 0; part < ((fl & kFlagLo) ? 2u : 1u) && fr; ++part) {
-                const uint32_t un = un_s++, us = un % kPUnits;
-                if (un >= (uint32_t)kPUnits)
-                  fr = mbar_wait_cluster(&ctl.pfree[us], ((un / kPUnits) - 1) & 1, abort_flag, kWaitNs);
+                const uint32_t ui = un_s++, us = ui % kPUnits;
+                if (ui >= (uint32_t)kPUnits)
+                  fr = mbar_wait_cluster(&ctl.pfree[us], ((ui / kPUnits) - 1) & 1, abort_flag, kWaitNs);
                 if (fr)
                   bulk_copy_to_peer(peer_p + us * kPUnitBytes, st + part * kPUnitBytes, kPMsgBytes,
                                     peer_precv + 8 * us);
@@ -714,10 +720,6 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
       const int tq = threadIdx.x - 64;             // 0..127 (row warps)
       const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
       const uint32_t peer_pfree = mapa(smem_u32(&ctl.pfree[0]), 0);   // + 8 * unit slot
-      // row warps: unit counter, and per unit slot the parity of the next
-      // phase of its page barriers (pv_done, rows_seen advance only when the
-      // slot holds a page's first unit)
-      uint32_t un_v = 0, pvpar = 0, prev_slot = 0, prev_par = 0;
       for (int ii = 0; ii < n_items; ++ii) {
         if (__any_sync(0xffffffffu, *abort_flag)) break;
         const Item it = ctl.items[ii];
