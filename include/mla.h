@@ -168,6 +168,12 @@ int mla_decode_paged(const void* q_lat, const void* kv_cache, int dtype,
  * mla_decode_paged_noalloc -- mla_decode_paged without a caller workspace.
  * (An engineering variant: the pages have no counterpart of it.)
  *
+ * For callers that have no way to get device memory at the point of the
+ * call: a plain C or C++ host that holds only the pointers it was handed and
+ * has no allocator of its own, or a serving process that gave all free device
+ * memory to its cache pool at start-up, so that a workspace would have to
+ * come from cudaMalloc, which can fail there and stalls the whole device.
+ *
  * Same arguments and results as mla_decode_paged, minus workspace and
  * workspace_bytes.  The split workspace lives in a file-scope device array
  * of this library, 32 MiB per device: shapes whose
@@ -179,8 +185,8 @@ int mla_decode_paged(const void* q_lat, const void* kv_cache, int dtype,
  * The scratch is shared by all calls on a device: two calls that may overlap
  * in time (different streams, or different host threads) race on it; issue
  * them on one stream.  The first call on a device looks the scratch address
- * up (cudaGetSymbolAddress; it may load the module), so make it before any
- * stream capture; later calls can be captured into a graph.
+ * up (cudaGetSymbolAddress; it may load the module), so make that first call
+ * before any stream capture begins.
  */
 int mla_decode_paged_noalloc(const void* q_lat, const void* kv_cache, int dtype,
                              const int32_t* block_table, const int32_t* seqlens,

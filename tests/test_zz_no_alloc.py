@@ -1,7 +1,9 @@
 """The no-allocation decode entry point (mla_decode_paged_noalloc).
 
 It runs the same kernels as mla_decode_paged but keeps the split workspace in
-the library's own device scratch.  On the same inputs both must give the same
+the library's own device scratch, for callers that cannot get device memory at
+the call (a host with only the pointers it was handed, or a server that gave
+all free memory to its cache pool).  On the same inputs both must give the same
 bits, on two calls in a row (the scratch is reused, nothing in it has to start
 at zero), and shapes whose workspace exceeds the scratch are refused.  This
 file is collected last so that it also runs after every other GPU test.
