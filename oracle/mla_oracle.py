@@ -28,7 +28,7 @@ __all__ = [
     "decode_paged_logical", "absorb_output", "full_model_unabsorbed",
     "full_model_absorbed", "full_model_rope_on_reconstructed_keys",
     "mha_cache_numbers", "gqa_cache_numbers", "mla_cache_numbers",
-    "mla_equivalent_gqa_groups", "bf16_to_f64",
+    "mla_equivalent_gqa_groups", "bf16_to_f64", "rebuild_kv", "prefill_attention",
 ]
 
 
@@ -153,6 +153,55 @@ def absorb_output(o_lat, W_uv, W_o):
     W = np.asarray(W_uv, dtype=np.float64).reshape(H, -1, d_c)   # [H, d_h, d_c]
     o = np.stack([o_lat[:, hh, :] @ W[hh].T for hh in range(H)], axis=1)    # [n, H, d_h]
     return o.reshape(n, -1) @ np.asarray(W_o, dtype=np.float64).T
+
+
+# --------------------------------------------------------------------------
+# prefill over rebuilt per-head keys and values ("The MLA equations": the key
+# of head h is [W^UK_h c_s ; R_s k^R_s], its value W^UV_h c_s)
+# --------------------------------------------------------------------------
+
+def rebuild_kv(C, H, W_uk, W_uv, d_c):
+    """Per-head content keys and values of cached rows C [L, D].
+
+    W^UK and W^UV are [H*d_h, d_c]; head h owns rows h*d_h .. (h+1)*d_h - 1.
+    Returns k_nope [L, H, d_h] = W^UK_h c_s, v [L, H, d_h] = W^UV_h c_s and
+    k_rope [L, d_r] = R_s k^R_s (the row's rotary part, stored rotated)."""
+    C = np.asarray(C, dtype=np.float64)
+    L = C.shape[0]
+    c = C[:, :d_c]
+    k_nope = (c @ np.asarray(W_uk, np.float64).T).reshape(L, H, -1)
+    v = (c @ np.asarray(W_uv, np.float64).T).reshape(L, H, -1)
+    return k_nope, v, C[:, d_c:].copy()
+
+
+def prefill_attention(q_nope, q_rope_raw, positions, k_nope, v, k_rope, scale, base):
+    """Causal softmax attention of one sequence's new tokens over per-head keys.
+
+    q_nope [T, H, d_h] (content query q^C_h), q_rope_raw [T, H, d_r] (not yet
+    rotated; rotated here by the query's position), positions [T];
+    k_nope, v [L, H, d_h], k_rope [L, d_r].  Query i sees keys
+    0 .. positions[i].  score = scale * ([q^C_h ; R_t q^R_h] . [k_nope ;
+    k_rope]); o_h = sum_s p_s v_{s,h}.  Returns o [T, H, d_h] and the
+    natural-log log-sum-exp of the scaled scores, lse [T, H]."""
+    q_nope = np.asarray(q_nope, dtype=np.float64)
+    T, H, d_h = q_nope.shape
+    q_rope = rope(np.asarray(q_rope_raw, np.float64).transpose(1, 0, 2),
+                  positions, base).transpose(1, 0, 2)
+    k_nope = np.asarray(k_nope, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    k_rope = np.asarray(k_rope, dtype=np.float64)
+    o = np.zeros((T, H, d_h))
+    lse = np.zeros((T, H))
+    for i in range(T):
+        n = int(positions[i]) + 1
+        z = scale * (np.einsum("hd,shd->hs", q_nope[i], k_nope[:n]) +
+                     q_rope[i] @ k_rope[:n].T)            # [H, n]
+        m = z.max(axis=1, keepdims=True)
+        e = np.exp(z - m)
+        s = e.sum(axis=1, keepdims=True)
+        o[i] = np.einsum("hs,shd->hd", e / s, v[:n])
+        lse[i] = m[:, 0] + np.log(s[:, 0])
+    return o, lse
 
 
 # --------------------------------------------------------------------------
