@@ -2,7 +2,9 @@
 
 A C-ABI CUDA library (libmla.so, declared in include/mla.h) with four calls
 -- mla_cache_append, mla_absorb_query, mla_decode_paged, mla_absorb_output --
-plus mla_decode_step (append, absorb and attend in one call), and this thin
+plus mla_decode_step (append, absorb and attend in one call), the prefill
+pair mla_prefill_kv / mla_prefill_attention (attention over per-head keys and
+values rebuilt from the latent cache), and this thin
 Python binding with the same names.  PyTorch supplies device
 memory and streams only; every step of the path runs in the library's
 kernels.  Importing the package loads the library and fails loudly if it has
@@ -16,6 +18,6 @@ from ._lib import (  # noqa: F401
     mla_absorb_output, mla_absorb_query, mla_cache_append, mla_check_status,
     mla_decode_item_cost, mla_decode_num_workers, mla_decode_paged, mla_decode_paged_noalloc,
     mla_decode_row_groups, mla_decode_split_plan, mla_decode_step, mla_decode_workspace_size,
-    mla_status_string)
+    mla_prefill_attention, mla_prefill_kv, mla_prefill_kv_rows, mla_status_string)
 
 lib()  # load now: no silent fallback path exists

@@ -54,6 +54,10 @@ SIGNATURES = {
                              _I, _I, _F, _I, _F, _P, _SZ, _P, _P, _P]),
     "mla_decode_num_workers": (_I, [_I, _I, _I, _I, _I, _I]),
     "mla_decode_path": (_I, [_I, _I, _I, _I, _I]),
+    "mla_prefill_kv_rows": (_I, [_I]),
+    "mla_prefill_kv": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P]),
+    "mla_prefill_attention": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F,
+                                   _P, _P, _P]),
 }
 
 
@@ -332,6 +336,70 @@ def mla_decode_row_groups(T_q, H, d_c, d_r, dtype=torch.bfloat16) -> int:
 def mla_decode_num_workers(B, T_q, H, d_c, d_r, dtype=torch.bfloat16) -> int:
     code = MLA_BF16 if dtype == torch.bfloat16 else MLA_F32
     return int(lib().mla_decode_num_workers(B, T_q, H, d_c, d_r, code))
+
+
+# --------------------------------------------------------------------------
+# prefill over rebuilt per-head keys and values
+# --------------------------------------------------------------------------
+
+def mla_prefill_kv_rows(max_blocks_per_seq) -> int:
+    """Rows per sequence R of the rebuilt K/V buffers (64 * max_blocks rounded up to 128)."""
+    return int(lib().mla_prefill_kv_rows(int(max_blocks_per_seq)))
+
+
+def mla_prefill_kv(kv_cache, block_table, seqlens, w_uk, w_uv, *, H, out=None, stream=None):
+    """Rebuild k_nope = W^UK_h c_s, v = W^UV_h c_s ([B, R, H, d_h] bf16) and copy
+    k_rope = R_s k^R_s ([B, R, d_r]) for every cached row.  Returns
+    (k_nope, v, k_rope)."""
+    num_blocks, page, D = kv_cache.shape
+    B, max_blocks = block_table.shape
+    HD, d_c = w_uk.shape
+    if HD % H or w_uv.shape != w_uk.shape or seqlens.shape != (B,):
+        raise ValueError("shape mismatch")
+    d_h, d_r = HD // H, D - d_c
+    R = mla_prefill_kv_rows(max_blocks)
+    if out is None:
+        dev = kv_cache.device
+        out = (torch.empty((B, R, H, d_h), device=dev, dtype=kv_cache.dtype),
+               torch.empty((B, R, H, d_h), device=dev, dtype=kv_cache.dtype),
+               torch.empty((B, R, d_r), device=dev, dtype=kv_cache.dtype))
+    k_nope, v, k_rope = out
+    st = lib().mla_prefill_kv(
+        _dev(kv_cache, "kv_cache"), _dtype_code(kv_cache), _dev(block_table, "block_table", torch.int32),
+        _dev(seqlens, "seqlens", torch.int32), B, d_c, d_r, page, max_blocks, num_blocks,
+        _dev(w_uk, "w_uk", kv_cache.dtype), _dev(w_uv, "w_uv", kv_cache.dtype), H, d_h,
+        _dev(k_nope, "k_nope", kv_cache.dtype), _dev(v, "v", kv_cache.dtype),
+        _dev(k_rope, "k_rope", kv_cache.dtype), _stream(stream))
+    _check(st, "mla_prefill_kv")
+    return k_nope, v, k_rope
+
+
+def mla_prefill_attention(q_nope, q_rope, k_nope, v, k_rope, seqlens, *, max_blocks_per_seq,
+                          softmax_scale, rope_base=10000.0, o=None, lse=None, want_lse=True,
+                          stream=None):
+    """Causal attention of q [B, T_q, H, d_h (+ d_r unrotated)] over the rebuilt
+    keys and values.  Returns (o [B, T_q, H, d_h] fp32, lse [B, T_q, H] or None)."""
+    B, T_q, H, d_h = q_nope.shape
+    d_r = q_rope.shape[3]
+    if q_rope.shape[:3] != (B, T_q, H) or seqlens.shape != (B,):
+        raise ValueError("shape mismatch")
+    R = mla_prefill_kv_rows(max_blocks_per_seq)
+    if k_nope.shape != (B, R, H, d_h) or v.shape != (B, R, H, d_h) or k_rope.shape != (B, R, d_r):
+        raise ValueError("K/V buffers must be [B, R, H, d_h] and [B, R, d_r]")
+    dev = q_nope.device
+    if o is None:
+        o = torch.empty((B, T_q, H, d_h), device=dev, dtype=torch.float32)
+    if lse is None and want_lse:
+        lse = torch.empty((B, T_q, H), device=dev, dtype=torch.float32)
+    dt = q_nope.dtype
+    st = lib().mla_prefill_attention(
+        _dev(q_nope, "q_nope"), _dev(q_rope, "q_rope", dt), _dtype_code(q_nope),
+        _dev(k_nope, "k_nope", dt), _dev(v, "v", dt), _dev(k_rope, "k_rope", dt),
+        _dev(seqlens, "seqlens", torch.int32), B, T_q, H, d_h, d_r, int(max_blocks_per_seq),
+        float(rope_base), float(softmax_scale), _dev(o, "o", torch.float32),
+        _dev(lse, "lse", torch.float32) if lse is not None else None, _stream(stream))
+    _check(st, "mla_prefill_attention")
+    return o, lse
 
 
 def mla_check_status(stream=None) -> int:

@@ -40,31 +40,6 @@ __device__ __forceinline__ void rope_pair(double x1, double x2, int pos, int j, 
   *y2 = x1 * sn + x2 * cs;
 }
 
-// Rotary frequencies as turns per position, base^(-2j/d_r) / (2 pi), in
-// 64-bit fixed point (computed on the host in double precision): the angle of
-// position s is then s * turn[j] modulo one turn, exact in integer arithmetic
-// up to the rounding of turn[j], with no large angle to reduce.
-constexpr int kAbMaxPairs = 256;             // rotary pairs (d_r / 2) the table holds
-struct RopeFreqs {
-  uint64_t turn[kAbMaxPairs];
-};
-
-RopeFreqs rope_freqs(float base, int d_r) {
-  RopeFreqs fr{};
-  for (int j = 0; j < d_r / 2 && j < kAbMaxPairs; ++j) {
-    const double turns = std::pow((double)base, -2.0 * (double)j / (double)d_r) /
-                         6.283185307179586476925286766559;   // < 1
-    fr.turn[j] = (uint64_t)std::ldexp(turns, 64);
-  }
-  return fr;
-}
-
-// the angle of pair j at position pos, in half turns (angle / pi) in [-1, 1):
-// the 64-bit product pos * turn[j] wraps around whole turns
-__device__ __forceinline__ double rope_half_turns(const RopeFreqs& fr, int pos, int j) {
-  return (double)(int64_t)((uint64_t)(int64_t)pos * fr.turn[j]) * 0x1p-63;
-}
-
 // decode-step mode: token i is query token t = i % T_q of sequence b = i / T_q,
 // at position seqlens[b] - T_q + t
 __device__ __forceinline__ int step_position(const int32_t* seqlens, int T_q, int i, int* b) {
@@ -386,6 +361,16 @@ __global__ void __launch_bounds__(AO_T) absorb_output_kernel(AbsorbOArgs a) {
 }
 
 }  // namespace
+
+RopeFreqs rope_freqs(float base, int d_r) {
+  RopeFreqs fr{};
+  for (int j = 0; j < d_r / 2 && j < kAbMaxPairs; ++j) {
+    const double turns = std::pow((double)base, -2.0 * (double)j / (double)d_r) /
+                         6.283185307179586476925286766559;   // < 1
+    fr.turn[j] = (uint64_t)std::ldexp(turns, 64);
+  }
+  return fr;
+}
 
 cudaError_t launch_cache_append(const AppendArgs& a, cudaStream_t s) {
   if (a.n_new == 0) return cudaSuccess;

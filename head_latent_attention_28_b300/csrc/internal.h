@@ -27,6 +27,24 @@ int tc_workers(int num_sms);
 int tc_item_cost(int rows);   // the split partition's item cost C for this kernel
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
 
+// Rotary frequencies as turns per position, base^(-2j/d_r) / (2 pi), in
+// 64-bit fixed point (computed on the host in double precision by
+// rope_freqs, append_absorb.cu): the angle of position s is then s * turn[j]
+// modulo one turn, exact in integer arithmetic up to the rounding of
+// turn[j], with no large angle to reduce.
+constexpr int kAbMaxPairs = 256;             // rotary pairs (d_r / 2) the table holds
+struct RopeFreqs {
+  uint64_t turn[kAbMaxPairs];
+};
+RopeFreqs rope_freqs(float base, int d_r);
+#ifdef __CUDACC__
+// the angle of pair j at position pos, in half turns (angle / pi) in [-1, 1):
+// the 64-bit product pos * turn[j] wraps around whole turns
+__device__ __forceinline__ double rope_half_turns(const RopeFreqs& fr, int pos, int j) {
+  return (double)(int64_t)((uint64_t)(int64_t)pos * fr.turn[j]) * 0x1p-63;
+}
+#endif
+
 // append_absorb.cu
 struct AppendArgs {
   const void* c; const void* k_rope; int dtype_in;
@@ -62,5 +80,34 @@ struct AbsorbOArgs {
   int N, H, d_h, d_c, d; float* out;
 };
 cudaError_t launch_absorb_output(const AbsorbOArgs& a, cudaStream_t s);
+
+// prefill_tc.cu (materialised per-head keys and values; bf16, d_c = 512,
+// d_h = 128, d_r = 64)
+bool prefill_supported(int dtype, int d_c, int d_r, int d_h);
+int prefill_kv_rows(int max_blocks);   // rows per sequence of the rebuilt K/V buffers
+struct PrefillKvArgs {
+  const void* cache; const int32_t* block_table; const int32_t* seqlens;
+  int B, max_blocks, num_blocks, d_c, d_r;
+  const void* w_uk; const void* w_uv;   // [H * d_h, d_c]
+  int H, d_h;
+  int R;                                // rows per sequence of the outputs
+  void* k_nope; void* v;                // [B, R, H, d_h]
+  void* k_rope;                         // [B, R, d_r]
+  unsigned* err;
+};
+cudaError_t launch_prefill_kv(const PrefillKvArgs& a, cudaStream_t s);
+struct PrefillAttnArgs {
+  const void* q_nope; const void* q_rope;   // [B, T_q, H, d_h], [B, T_q, H, d_r] (unrotated)
+  const void* k_nope; const void* v; const void* k_rope;   // as PrefillKvArgs
+  const int32_t* seqlens;
+  int B, T_q, H, d_h, d_r;
+  int R;                                    // rows per sequence of the K/V buffers
+  int max_len;                              // longest valid sequence (max_blocks * 64)
+  float scale, rope_base;
+  float* o;                                 // [B, T_q, H, d_h]
+  float* lse;                               // [B, T_q, H] or nullptr
+  unsigned* err;
+};
+cudaError_t launch_prefill_attn(const PrefillAttnArgs& a, cudaStream_t s);
 
 }  // namespace mla

@@ -435,4 +435,62 @@ int mla_decode_step(const void* q_nope, const void* q_rope, const void* w_uk, in
                      d_r, page_size, max_blocks_per_seq, num_blocks, softmax_scale, causal,
                      static_cast<char*>(workspace) + qb, workspace_bytes - qb, o_lat, lse, stream);
 }
+
+int mla_prefill_kv_rows(int max_blocks_per_seq) {
+  if (max_blocks_per_seq < 1 || max_blocks_per_seq > (1 << 24)) return 0;
+  return mla::prefill_kv_rows(max_blocks_per_seq);
+}
+
+int mla_prefill_kv(const void* kv_cache, int dtype, const int32_t* block_table,
+                   const int32_t* seqlens, int B, int d_c, int d_r, int page_size,
+                   int max_blocks_per_seq, int num_blocks, const void* w_uk, const void* w_uv,
+                   int H, int d_h, void* k_nope, void* v, void* k_rope, void* stream) {
+  if (B < 0 || H < 1 || d_h < 1 || d_c < 1 || d_r < 0 || !dtype_ok(dtype) ||
+      page_size != MLA_PAGE_SIZE || max_blocks_per_seq < 1 || max_blocks_per_seq > (1 << 24) ||
+      num_blocks < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (!mla::prefill_supported(dtype, d_c, d_r, d_h)) return MLA_ERR_UNSUPPORTED;
+  if (B == 0) return MLA_OK;
+  const auto al16 = [](const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!al16(kv_cache) || !block_table || !seqlens || !al16(w_uk) || !al16(w_uv) ||
+      !al16(k_nope) || !al16(v) || !al16(k_rope))
+    return MLA_ERR_INVALID_ARG;
+  const int R = mla::prefill_kv_rows(max_blocks_per_seq);
+  if (B > 65535 || H > 65535 * 8 || (long long)B * R * H * d_h >= (1LL << 40) ||
+      (long long)num_blocks * MLA_PAGE_SIZE >= (1LL << 31) || (long long)B * R >= (1LL << 31))
+    return MLA_ERR_UNSUPPORTED;
+  mla::PrefillKvArgs a{kv_cache, block_table, seqlens, B, max_blocks_per_seq, num_blocks, d_c, d_r,
+                       w_uk, w_uv, H, d_h, R, k_nope, v, k_rope, nullptr};
+  cudaError_t e = device_info(&a.err, nullptr);
+  if (e != cudaSuccess) return note_cuda(e);
+  e = mla::launch_prefill_kv(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : note_cuda(e);
+}
+
+int mla_prefill_attention(const void* q_nope, const void* q_rope, int dtype, const void* k_nope,
+                          const void* v, const void* k_rope, const int32_t* seqlens, int B,
+                          int T_q, int H, int d_h, int d_r, int max_blocks_per_seq,
+                          float rope_base, float softmax_scale, float* o, float* lse,
+                          void* stream) {
+  if (B < 0 || T_q < 1 || H < 1 || d_h < 1 || d_r < 0 || !dtype_ok(dtype) ||
+      max_blocks_per_seq < 1 || max_blocks_per_seq > (1 << 24) || !(rope_base > 0.f) ||
+      !(softmax_scale > 0.f) || !(softmax_scale < 3.0e38f))
+    return MLA_ERR_INVALID_ARG;
+  if (!mla::prefill_supported(dtype, 512, d_r, d_h)) return MLA_ERR_UNSUPPORTED;
+  if (B == 0) return MLA_OK;
+  const auto al16 = [](const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!al16(q_nope) || !q_rope || !al16(k_nope) || !al16(v) || !al16(k_rope) || !seqlens ||
+      !al16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return MLA_ERR_INVALID_ARG;
+  const int R = mla::prefill_kv_rows(max_blocks_per_seq);
+  if (B > 65535 || H > 65535 || (long long)B * T_q >= (1LL << 31) || (long long)B * R >= (1LL << 31) ||
+      (long long)(T_q + 127) / 128 > 0x7fffffffLL)
+    return MLA_ERR_UNSUPPORTED;
+  mla::PrefillAttnArgs a{q_nope, q_rope, k_nope, v, k_rope, seqlens, B, T_q, H, d_h, d_r, R,
+                         max_blocks_per_seq * MLA_PAGE_SIZE, softmax_scale, rope_base, o, lse, nullptr};
+  cudaError_t e = device_info(&a.err, nullptr);
+  if (e != cudaSuccess) return note_cuda(e);
+  e = mla::launch_prefill_attn(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : note_cuda(e);
+}
 }  // extern "C"

@@ -1,0 +1,677 @@
+// Prefill with materialised per-head keys and values (bf16, d_c = 512,
+// d_h = 128, d^R_h = 64).
+//
+// For a chunk of T new tokens the absorbed path costs 2 (d_c + d^R_h) +
+// 2 d_c flops per (query, key, head) pair; rebuilding every head's content
+// key k_{s,h} = W^UK_h c_s and value v_{s,h} = W^UV_h c_s once per cached row
+// ("Attention, Part 2: MQA, GQA and MLA", the MLA equations: the key of head
+// h is [W^UK_h c_s ; R_s k^R_s], its value W^UV_h c_s) brings that down to
+// 2 (d_h + d^R_h) + 2 d_h, plus 4 d_c d_h per (row, head) for the rebuild.
+// With T in the hundreds and more, attention over the rebuilt keys is the
+// cheaper way ("Multi-head latent attention (MLA)", section 2: the up-
+// projections may be applied to the cached latent or absorbed; the result is
+// the same).
+//
+// Two kernels:
+//  * prefill_kv_kernel: one CTA per (sequence, 128-row tile, group of 8
+//    heads).  TMA brings the tile's two cache pages (latent columns only,
+//    128 x 512, kept for all heads of the group) and streams [W^UK_h ; W^UV_h]
+//    (256 x 512) in 64-column chunks; tcgen05.mma with M = 128 rows, N = 256,
+//    K = 512 accumulates both products of a head in TMEM (two buffers, so the
+//    epilogue of one head overlaps the MMAs of the next).  Four warps convert
+//    to bf16 and write k_nope[b, s, h, :] and v[b, s, h, :]; rows past the
+//    sequence end inside its last tile are written as zeros.  The first head
+//    group also copies the rotated rotary key R_s k^R_s of each row.
+//  * prefill_attn_kernel: one CTA per (128-token query tile, head, sequence),
+//    heavy (late) tiles first.  Scores over d_h + d^R_h = 192 dims
+//    (M = 128 queries, N = 128 keys) into one of two TMEM buffers, a base-2
+//    online softmax with a lazy running max (the output is rescaled only when
+//    a row maximum grows by more than 2^8; exact after the final division),
+//    probabilities to TMEM as bf16 and O += P . V with P read from TMEM
+//    (tcgen05.mma A operand in tensor memory).  Key and value tiles stream
+//    through two-stage rings, so the scores of tile j + 1 run while the
+//    softmax of tile j does.  The query's rotary half is rotated on the fly
+//    (the same fixed-point angle table as the query absorption).
+// Every mbarrier wait is bounded (2 s): on expiry the kernel records
+// MLA_ERR_TIMEOUT, lets its copies and MMAs finish, frees TMEM and returns.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm100.cuh"
+
+namespace mla {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kPfThreads = 192;          // 6 warps: producer, MMA issuer, 4 row warps
+constexpr int kBox16 = 16384;            // 128 rows x 64 dims bf16 (one SW128 box)
+constexpr uint64_t kPfWaitNs = 2000000000ull;
+constexpr float kPfLog2e = 1.4426950408889634f;
+constexpr float kPfLn2 = 0.6931471805599453f;
+constexpr float kPfRescale = 8.0f;       // lazy rescale threshold (log2 units)
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// every thread of the warp agrees that the wait succeeded; else the CTA aborts
+__device__ __forceinline__ bool warp_ok(bool ok, volatile int* abort_flag, unsigned* err) {
+  const bool all = __all_sync(0xffffffffu, ok);
+  if (!all && (threadIdx.x & 31) == 0) {
+    *abort_flag = 1;
+    atomicOr(err, kErrTimeout);
+  }
+  return all;
+}
+
+// ---------------------------------------------------------------------------
+// K/V rebuild
+// ---------------------------------------------------------------------------
+constexpr int kKvHeads = 8;              // heads per CTA (the latent tile is reused)
+constexpr int kKvStages = 2;             // weight chunk ring
+constexpr int kKvA = 8 * kBox16;         // 128 rows x 512 latents
+constexpr int kKvW = 2 * kBox16;         // 64-column chunk of W^UK_h (128 rows) and W^UV_h (128 rows)
+constexpr int kKvSmem = kKvA + kKvStages * kKvW + 1024;
+
+__global__ void __launch_bounds__(kPfThreads, 1)
+prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_pool,
+                  const __grid_constant__ CUtensorMap tm_wuk, const __grid_constant__ CUtensorMap tm_wuv) {
+  extern __shared__ uint8_t kv_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(kv_smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ uint64_t a_full, w_full[kKvStages], w_empty[kKvStages], d_full[2], d_empty[2], mma_final;
+  __shared__ uint32_t tbase;
+  __shared__ int abort_raw, never_raw;
+  volatile int* abort_flag = &abort_raw;
+  volatile int* never = &never_raw;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x, b = blockIdx.y, h0 = blockIdx.z * kKvHeads;
+  const int nh = min(kKvHeads, a.H - h0);
+  const int L = a.seqlens[b];
+  if (L < 0 || L > a.max_blocks * kPage) {
+    if (threadIdx.x == 0 && tile == 0 && blockIdx.z == 0) atomicOr(a.err, kErrBadIndex);
+    return;
+  }
+  const int r0 = tile * 128;
+  if (r0 >= L) return;   // the whole CTA: no row of this sequence here
+  const int pages = (L + kPage - 1) / kPage;
+
+  if (threadIdx.x == 0) {
+    abort_raw = 0;
+    never_raw = 0;
+    mbar_init(&a_full, 1);
+    for (int s = 0; s < kKvStages; ++s) {
+      mbar_init(&w_full[s], 1);
+      mbar_init(&w_empty[s], 1);
+    }
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(&d_full[d], 1);
+      mbar_init(&d_empty[d], 4);
+    }
+    mbar_init(&mma_final, 1);
+    fence_mbar_init_cluster();
+  }
+  if (warp == 1) tmem_alloc(&tbase, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tbase;
+  uint8_t* sA = smem;
+  uint8_t* sW = smem + kKvA;
+  uint32_t n_issued = 0;   // producer: weight chunks issued
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_a = policy_evict_first();   // each latent tile is read by 16 CTAs at most
+      const uint64_t pol_w = policy_evict_last();    // the weights are read by every tile
+      int y[2];
+      for (int p = 0; p < 2; ++p) {
+        const int j = 2 * tile + p;
+        int blk = -1;
+        if (j < pages) blk = a.block_table[(size_t)b * a.max_blocks + j];
+        const bool ok = blk >= 0 && blk < a.num_blocks;
+        if (j < pages && !ok) atomicOr(a.err, kErrBadIndex);
+        // a page past the sequence (or an invalid one) reads past the pool's end: zeros
+        y[p] = ok ? blk * kPage : a.num_blocks * kPage;
+      }
+      mbar_arrive_expect_tx(&a_full, kKvA);
+      for (int c = 0; c < 8; ++c)
+        for (int p = 0; p < 2; ++p)
+          tma_load_2d(sA + c * kBox16 + p * 8192, &tm_pool, &a_full, 64 * c, y[p], pol_a);
+      for (int hh = 0; hh < nh; ++hh) {
+        const int wrow = (h0 + hh) * a.d_h;
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t g = n_issued, s = g % kKvStages;
+          if (g >= (uint32_t)kKvStages &&
+              !mbar_wait(&w_empty[s], ((g / kKvStages) - 1) & 1, abort_flag, kPfWaitNs)) {
+            *abort_flag = 1;
+            atomicOr(a.err, kErrTimeout);
+            break;
+          }
+          uint8_t* dst = sW + s * kKvW;
+          mbar_arrive_expect_tx(&w_full[s], kKvW);
+          tma_load_2d(dst, &tm_wuk, &w_full[s], 64 * c, wrow, pol_w);
+          tma_load_2d(dst + kBox16, &tm_wuv, &w_full[s], 64 * c, wrow, pol_w);
+          ++n_issued;
+        }
+        if (*abort_flag) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id = idesc_bf16_f32(128, 256, 0, 0);   // A and B K-major
+      bool ok = mbar_wait(&a_full, 0, abort_flag, kPfWaitNs);
+      uint32_t g = 0;
+      for (int hh = 0; ok && hh < nh; ++hh) {
+        const uint32_t d = hh & 1;
+        if (hh >= 2) ok = mbar_wait(&d_empty[d], ((hh >> 1) - 1) & 1, abort_flag, kPfWaitNs);
+        for (int c = 0; ok && c < 8; ++c, ++g) {
+          const uint32_t s = g % kKvStages;
+          ok = mbar_wait(&w_full[s], (g / kKvStages) & 1, abort_flag, kPfWaitNs);
+          if (!ok) break;
+          tc_fence_after();
+          const uint8_t* wb = sW + s * kKvW;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint64_t ad = sdesc_sw128(smem_u32(sA + c * kBox16 + q * 32), 16, 1024);
+            const uint64_t bd = sdesc_sw128(smem_u32(wb + q * 32), 16, 1024);
+            mma_ss(tmem + d * 256, ad, bd, id, (c > 0 || q > 0) ? 1 : 0);
+          }
+          mma_commit(&w_empty[s]);
+        }
+        if (ok) mma_commit(&d_full[d]);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(a.err, kErrTimeout);
+      }
+    }
+  } else {
+    // row warps: TMEM lane quarter warp & 3 holds rows 32 (warp & 3) .. + 31
+    const int q4 = warp & 3;
+    const int r = 32 * q4 + lane;
+    const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+    const int row = r0 + r;
+    const bool real = row < L;
+    const size_t orow = (size_t)b * a.R + row;
+    if (blockIdx.z == 0) {
+      // R_s k^R_s, unchanged from the cache row (zeros past the sequence end)
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.k_rope) + orow * a.d_r);
+      int blk = -1;
+      if (real) blk = a.block_table[(size_t)b * a.max_blocks + row / kPage];
+      if (real && blk >= 0 && blk < a.num_blocks) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(a.cache) +
+            ((size_t)blk * kPage + row % kPage) * (a.d_c + a.d_r) + a.d_c);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dst[k] = __ldg(src + k);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dst[k] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    for (int hh = 0; hh < nh; ++hh) {
+      const uint32_t d = hh & 1;
+      if (!warp_ok(mbar_wait(&d_full[d], (hh >> 1) & 1, abort_flag, kPfWaitNs), abort_flag, a.err))
+        break;
+      tc_fence_after();
+      const size_t off = (orow * a.H + (h0 + hh)) * a.d_h;
+      __nv_bfloat16* kd = static_cast<__nv_bfloat16*>(a.k_nope) + off;
+      __nv_bfloat16* vd = static_cast<__nv_bfloat16*>(a.v) + off;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        float x[32];
+        tmem_ld32(tmem + lane_off + d * 256 + 32 * c, x);
+        tmem_ld_wait();
+        uint4* dst = reinterpret_cast<uint4*>((c < 4 ? kd : vd) + 32 * (c & 3));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (real)
+            w = make_uint4(pack_bf16x2(x[8 * i], x[8 * i + 1]), pack_bf16x2(x[8 * i + 2], x[8 * i + 3]),
+                           pack_bf16x2(x[8 * i + 4], x[8 * i + 5]), pack_bf16x2(x[8 * i + 6], x[8 * i + 7]));
+          dst[i] = w;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&d_empty[d]);
+    }
+  }
+
+  // ---- drain: MMAs complete, copies landed, then free TMEM
+  __syncwarp();
+  if (warp == 1 && lane == 0) {
+    mma_commit(&mma_final);
+    if (!mbar_wait(&mma_final, 0, never, kPfWaitNs)) atomicOr(a.err, kErrTimeout);
+  }
+  if (warp == 0 && lane == 0) {
+    if (!mbar_wait(&a_full, 0, never, kPfWaitNs)) atomicOr(a.err, kErrTimeout);
+    for (uint32_t k = 0; k < (uint32_t)kKvStages && k < n_issued; ++k) {
+      const uint32_t g = n_issued - 1 - k;
+      if (!mbar_wait(&w_full[g % kKvStages], (g / kKvStages) & 1, never, kPfWaitNs))
+        atomicOr(a.err, kErrTimeout);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// attention over the rebuilt keys and values
+// ---------------------------------------------------------------------------
+constexpr int kAtQ = 3 * kBox16;         // query tile: q_nope (2 boxes), rotated q_rope (1 box)
+constexpr int kAtK = 3 * kBox16;         // key tile: k_nope (2 boxes), k_rope (1 box)
+constexpr int kAtV = 2 * kBox16;         // value tile
+constexpr int kAtStages = 2;
+constexpr int kAtOffK = kAtQ;
+constexpr int kAtOffV = kAtOffK + kAtStages * kAtK;
+constexpr int kAtSmem = kAtOffV + kAtStages * kAtV + 1024;
+// TMEM columns: two score buffers, the output, two probability buffers (bf16 pairs)
+constexpr uint32_t kTS = 0, kTO = 256, kTP = 384;
+
+__global__ void __launch_bounds__(kPfThreads, 1)
+prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_kr,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ RopeFreqs fr) {
+  extern __shared__ uint8_t at_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ uint64_t q_full, q_ready, k_full[kAtStages], k_empty[kAtStages], v_full[kAtStages],
+      v_empty[kAtStages], s_full[2], s_free[2], p_full[2], pv_done[2], mma_final;
+  __shared__ uint32_t tbase;
+  __shared__ int abort_raw, never_raw;
+  volatile int* abort_flag = &abort_raw;
+  volatile int* never = &never_raw;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = gridDim.x - 1 - blockIdx.x;   // late query tiles see the most keys: start them first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int L = a.seqlens[b];
+  const bool bad = L < a.T_q || L > a.max_len;
+  const int q0 = qt * 128;                     // first query token of the tile
+  const int last_t = min(q0 + 127, a.T_q - 1);
+  // key tiles: keys 0 .. position of the tile's last query
+  const int n_kt = bad ? 0 : (L - a.T_q + last_t) / 128 + 1;
+  if (bad && threadIdx.x == 0 && qt == 0 && h == 0) atomicOr(a.err, kErrBadIndex);
+
+  if (threadIdx.x == 0) {
+    abort_raw = 0;
+    never_raw = 0;
+    mbar_init(&q_full, 1);
+    mbar_init(&q_ready, 4);
+    for (int s = 0; s < kAtStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], 4);
+      mbar_init(&p_full[s], 4);
+      mbar_init(&pv_done[s], 1);
+    }
+    mbar_init(&mma_final, 1);
+    fence_mbar_init_cluster();
+  }
+  if (warp == 1) tmem_alloc(&tbase, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tbase;
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + kAtOffK;
+  uint8_t* sV = smem + kAtOffV;
+  const int krow0 = b * a.R;                   // the sequence's first row in the K/V buffers
+  const int n_tok = b * a.T_q + q0;            // the tile's first query row in q_nope
+  uint32_t n_k = 0, n_v = 0;                   // producer: key and value tiles issued
+  bool q_issued = false;
+
+  if (warp == 0) {
+    if (lane == 0 && n_kt > 0) {
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();   // every query tile of the head re-reads them
+      mbar_arrive_expect_tx(&q_full, 2 * kBox16);
+      tma_load_3d(sQ, &tm_q, &q_full, 0, h, n_tok, pol_q);
+      tma_load_3d(sQ + kBox16, &tm_q, &q_full, 64, h, n_tok, pol_q);
+      q_issued = true;
+      bool ok = true;
+      for (int j = 0; ok && j < n_kt; ++j) {
+        const uint32_t s = j & 1;
+        const int y = krow0 + 128 * j;
+        ok = j < 2 || mbar_wait(&k_empty[s], ((j >> 1) - 1) & 1, abort_flag, kPfWaitNs);
+        if (!ok) break;
+        uint8_t* kd = sK + s * kAtK;
+        mbar_arrive_expect_tx(&k_full[s], kAtK);
+        tma_load_3d(kd, &tm_k, &k_full[s], 0, h, y, pol_kv);
+        tma_load_3d(kd + kBox16, &tm_k, &k_full[s], 64, h, y, pol_kv);
+        tma_load_2d(kd + 2 * kBox16, &tm_kr, &k_full[s], 0, y, pol_kv);
+        ++n_k;
+        ok = j < 2 || mbar_wait(&v_empty[s], ((j >> 1) - 1) & 1, abort_flag, kPfWaitNs);
+        if (!ok) break;
+        uint8_t* vd = sV + s * kAtV;
+        mbar_arrive_expect_tx(&v_full[s], kAtV);
+        tma_load_3d(vd, &tm_v, &v_full[s], 0, h, y, pol_kv);
+        tma_load_3d(vd + kBox16, &tm_v, &v_full[s], 64, h, y, pol_kv);
+        ++n_v;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(a.err, kErrTimeout);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && n_kt > 0) {
+      const uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);   // Q, K both K-major
+      const uint32_t idO = idesc_bf16_f32(128, 128, 0, 1);   // P from TMEM, V MN-major
+      bool ok = mbar_wait(&q_full, 0, abort_flag, kPfWaitNs) &&
+                mbar_wait(&q_ready, 0, abort_flag, kPfWaitNs);
+      for (int j = 0; ok && j <= n_kt; ++j) {
+        if (j < n_kt) {
+          const uint32_t s = j & 1;
+          ok = mbar_wait(&k_full[s], (j >> 1) & 1, abort_flag, kPfWaitNs);
+          if (ok && j >= 2) ok = mbar_wait(&s_free[s], ((j >> 1) - 1) & 1, abort_flag, kPfWaitNs);
+          if (!ok) break;
+          tc_fence_after();
+          const uint8_t* kd = sK + s * kAtK;
+#pragma unroll
+          for (int kk = 0; kk < 12; ++kk) {
+            const uint64_t ad = sdesc_sw128(smem_u32(sQ + (kk >> 2) * kBox16 + (kk & 3) * 32), 16, 1024);
+            const uint64_t bd = sdesc_sw128(smem_u32(kd + (kk >> 2) * kBox16 + (kk & 3) * 32), 16, 1024);
+            mma_ss(tmem + kTS + s * 128, ad, bd, idS, kk > 0 ? 1 : 0);
+          }
+          mma_commit(&k_empty[s]);
+          mma_commit(&s_full[s]);
+        }
+        if (j >= 1) {
+          const int i = j - 1;
+          const uint32_t s = i & 1;
+          ok = mbar_wait(&p_full[s], (i >> 1) & 1, abort_flag, kPfWaitNs) &&
+               mbar_wait(&v_full[s], (i >> 1) & 1, abort_flag, kPfWaitNs);
+          if (!ok) break;
+          tc_fence_after();
+          const uint8_t* vd = sV + s * kAtV;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {   // 16 keys per step
+            const uint64_t bd = sdesc_sw128(smem_u32(vd + kk * 2048), kBox16, 1024);
+            mma_ts(tmem + kTO, tmem + kTP + s * 64 + kk * 8, bd, idO, (i > 0 || kk > 0) ? 1 : 0);
+          }
+          mma_commit(&v_empty[s]);
+          mma_commit(&pv_done[s]);
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(a.err, kErrTimeout);
+      }
+    }
+  } else {
+    // row warps: thread = query row r of the tile (TMEM lane r)
+    const int q4 = warp & 3;
+    const int r = 32 * q4 + lane;
+    const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+    const int t = q0 + r;
+    const bool real = !bad && t < a.T_q;
+    const int lim = real ? L - a.T_q + t : -1;   // position of the query = its last visible key
+    const size_t qrow = (size_t)b * a.T_q + t;
+    if (n_kt > 0) {
+      // rotary half of the query, rotated by its position, into box 2 of the
+      // query tile (K-major, 128-byte swizzle: 16-byte chunk c of row r sits at
+      // chunk c ^ (r & 7))
+      const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q_rope) + (qrow * a.H + h) * a.d_r;
+      const uint64_t pos = (uint64_t)(int64_t)lim;
+      uint8_t* qrow_s = sQ + 2 * kBox16 + r * 128;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {   // 16-byte chunk c: rotary pairs 4c .. 4c + 3
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (real) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * c + e;
+            const float half_turns = (float)(int64_t)(pos * fr.turn[j]) * 0x1p-63f;
+            float sn, cs;
+            sincospif(half_turns, &sn, &cs);
+            const float x1 = __bfloat162float(qr[2 * j]), x2 = __bfloat162float(qr[2 * j + 1]);
+            w[e] = pack_bf16x2(x1 * cs - x2 * sn, x1 * sn + x2 * cs);
+          }
+        }
+        *reinterpret_cast<uint4*>(qrow_s + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_ready);
+    }
+
+    const float sl2 = a.scale * kPfLog2e;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kt; ++j) {
+      const uint32_t s = j & 1;
+      ok = warp_ok(mbar_wait(&s_full[s], (j >> 1) & 1, abort_flag, kPfWaitNs), abort_flag, a.err);
+      if (!ok) break;
+      tc_fence_after();
+      float x0[64], x1[64];
+      tmem_ld64(tmem + lane_off + kTS + s * 128, x0);
+      tmem_ld64(tmem + lane_off + kTS + s * 128 + 64, x1);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[s]);
+      const int key0 = 128 * j;
+      if (key0 + 127 > lim) {   // causal mask (and padding rows: every key)
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          if (key0 + c > lim) x0[c] = -INFINITY;
+          if (key0 + 64 + c > lim) x1[c] = -INFINITY;
+        }
+      }
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) mt = fmaxf(mt, fmaxf(x0[c], x1[c]));
+      const float m_cand = fmaxf(m_run, mt * sl2);
+      const bool grow = m_cand > m_run + kPfRescale;   // also the first finite maximum
+      float alpha = 1.f;
+      if (grow) {
+        alpha = (m_run == -INFINITY) ? 0.f : ex2f(m_run - m_cand);
+        m_run = m_cand;
+      }
+      // O holds the value sums of tiles < j: rescale the rows whose maximum grew
+      if (__any_sync(0xffffffffu, grow && l_run > 0.f)) {
+        ok = warp_ok(mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, kPfWaitNs),
+                     abort_flag, a.err);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float o[32];
+          tmem_ld32(tmem + lane_off + kTO + 32 * c, o);
+          tmem_ld_wait();
+          uint32_t u[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(o[e] * alpha);
+          tmem_st32(tmem + lane_off + kTO + 32 * c, u);
+        }
+        tmem_st_wait();
+      }
+      l_run *= alpha;
+      const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+      // the probability buffer s was last read by the value MMAs of tile j - 2
+      if (j >= 2) {
+        ok = warp_ok(mbar_wait(&pv_done[s], ((j >> 1) - 1) & 1, abort_flag, kPfWaitNs), abort_flag, a.err);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      float sum = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2f(fmaf(x0[2 * c], sl2, -mu)), p1 = ex2f(fmaf(x0[2 * c + 1], sl2, -mu));
+        sum += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      tmem_st32(tmem + lane_off + kTP + s * 64, pk);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2f(fmaf(x1[2 * c], sl2, -mu)), p1 = ex2f(fmaf(x1[2 * c + 1], sl2, -mu));
+        sum += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      tmem_st32(tmem + lane_off + kTP + s * 64 + 32, pk);
+      tmem_st_wait();
+      l_run += sum;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[s]);
+    }
+    // epilogue: o = O / l, lse = (m + log2 l) ln 2 (the TMEM loads are
+    // warp-wide; padding rows store nothing)
+    if (ok && n_kt > 0)
+      ok = warp_ok(mbar_wait(&pv_done[(n_kt - 1) & 1], ((n_kt - 1) >> 1) & 1, abort_flag, kPfWaitNs),
+                   abort_flag, a.err);
+    float* orow = a.o + (qrow * a.H + h) * a.d_h;
+    if (ok && n_kt > 0) {
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        tmem_ld32(tmem + lane_off + kTO + 32 * c, o);
+        tmem_ld_wait();
+        if (t < a.T_q) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            reinterpret_cast<float4*>(orow + 32 * c)[i] =
+                make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+        }
+      }
+      if (t < a.T_q && a.lse) a.lse[qrow * a.H + h] = (m_run + log2f(l_run)) * kPfLn2;
+    } else if (bad && t < a.T_q) {
+      // a sequence of invalid length: zeros (the error word says why)
+      for (int c = 0; c < 32; ++c) reinterpret_cast<float4*>(orow)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (a.lse) a.lse[qrow * a.H + h] = 0.f;
+    }
+  }
+
+  // ---- drain: MMAs complete, copies landed, then free TMEM
+  __syncwarp();
+  if (warp == 1 && lane == 0 && n_kt > 0) {
+    mma_commit(&mma_final);
+    if (!mbar_wait(&mma_final, 0, never, kPfWaitNs)) atomicOr(a.err, kErrTimeout);
+  }
+  if (warp == 0 && lane == 0) {
+    if (q_issued && !mbar_wait(&q_full, 0, never, kPfWaitNs)) atomicOr(a.err, kErrTimeout);
+    for (uint32_t k = 0; k < (uint32_t)kAtStages && k < n_k; ++k) {
+      const uint32_t j = n_k - 1 - k;
+      if (!mbar_wait(&k_full[j & 1], (j >> 1) & 1, never, kPfWaitNs)) atomicOr(a.err, kErrTimeout);
+    }
+    for (uint32_t k = 0; k < (uint32_t)kAtStages && k < n_v; ++k) {
+      const uint32_t j = n_v - 1 - k;
+      if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, never, kPfWaitNs)) atomicOr(a.err, kErrTimeout);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+bool prefill_supported(int dtype, int d_c, int d_r, int d_h) {
+  return dtype == BF16 && d_c == 512 && d_r == 64 && d_h == 128;
+}
+
+int prefill_kv_rows(int max_blocks) {
+  const long long rows = (long long)max_blocks * kPage;
+  return (int)((rows + 127) / 128 * 128);
+}
+
+cudaError_t launch_prefill_kv(const PrefillKvArgs& a, cudaStream_t s) {
+  if (a.B == 0) return cudaSuccess;
+  TensorMapEncodeFn enc = nullptr;
+  cudaError_t e = tensor_map_encoder(&enc);
+  if (e != cudaSuccess) return e;
+  const int D = a.d_c + a.d_r;
+  CUtensorMap tm_pool, tm_wuk, tm_wuv;
+  {
+    // the pool [num_blocks * 64 rows, D]: box of 64 columns x 64 rows (one page)
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)a.num_blocks * kPage};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tm_pool, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.cache), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const void* ws[2] = {a.w_uk, a.w_uv};
+  CUtensorMap* tms[2] = {&tm_wuk, &tm_wuv};
+  for (int i = 0; i < 2; ++i) {
+    // W [H * d_h, d_c]: box of 64 columns x 128 rows (one head)
+    cuuint64_t dims[2] = {(cuuint64_t)a.d_c, (cuuint64_t)a.H * a.d_h};
+    cuuint64_t strides[1] = {(cuuint64_t)a.d_c * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(tms[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ws[i]), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  e = cudaFuncSetAttribute(prefill_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.R / 128, a.B, (a.H + kKvHeads - 1) / kKvHeads);
+  prefill_kv_kernel<<<grid, kPfThreads, kKvSmem, s>>>(a, tm_pool, tm_wuk, tm_wuv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_attn(const PrefillAttnArgs& a, cudaStream_t s) {
+  if (a.B == 0) return cudaSuccess;
+  TensorMapEncodeFn enc = nullptr;
+  cudaError_t e = tensor_map_encoder(&enc);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tm_q, tm_k, tm_kr, tm_v;
+  const auto map3 = [&](CUtensorMap* tm, const void* base, long long rows) -> bool {
+    // [rows, H, 128] as a 3-D tensor: box of 64 dims x 1 head x 128 rows
+    cuuint64_t dims[3] = {(cuuint64_t)a.d_h, (cuuint64_t)a.H, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)a.d_h * 2, (cuuint64_t)a.H * a.d_h * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  const long long kv_rows = (long long)a.B * a.R;
+  if (!map3(&tm_q, a.q_nope, (long long)a.B * a.T_q) || !map3(&tm_k, a.k_nope, kv_rows) ||
+      !map3(&tm_v, a.v, kv_rows))
+    return cudaErrorInvalidValue;
+  {
+    // k_rope [rows, 64]: box of 64 dims x 128 rows
+    cuuint64_t dims[2] = {(cuuint64_t)a.d_r, (cuuint64_t)kv_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)a.d_r * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tm_kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.k_rope), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const RopeFreqs fr = rope_freqs(a.rope_base, a.d_r);
+  e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAtSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.T_q + 127) / 128, a.H, a.B);
+  prefill_attn_kernel<<<grid, kPfThreads, kAtSmem, s>>>(a, tm_q, tm_k, tm_kr, tm_v, fr);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

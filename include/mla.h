@@ -331,6 +331,75 @@ int mla_decode_num_workers(int B, int T_q, int H, int d_c, int d_r, int dtype);
  */
 int mla_decode_path(int T_q, int H, int d_c, int d_r, int dtype);
 
+/*
+ * ---- Prefill with rebuilt per-head keys and values ----
+ *
+ * For a chunk of T_q new tokens per sequence, attention can run on the
+ * per-head keys k_{s,h} = [W^UK_h c_s ; R_s k^R_s] and values
+ * v_{s,h} = W^UV_h c_s rebuilt from the latent cache ("Attention, Part 2:
+ * MQA, GQA and MLA", the MLA equations; "Multi-head latent attention (MLA)",
+ * section 2: absorbing W^UK and W^UV or applying them to the cached latent
+ * gives the same result).  Per (query, key, head) that costs
+ * 2 (d_h + d_r) + 2 d_h flops instead of the absorbed path's
+ * 2 (d_c + d_r) + 2 d_c, plus 4 d_c d_h per (cached row, head) for the
+ * rebuild: the cheaper way once a chunk has more than a few dozen tokens.
+ * The output is per head (o_h, d_h wide), ready for W^O; the absorbed path's
+ * o_lat is the same o_h before W^UV.
+ *
+ * Supported: bf16, d_c = 512, d_h = 128, d_r = 64, page_size = 64
+ * (MLA_ERR_UNSUPPORTED otherwise; there is no other kernel for these calls).
+ *
+ * Rebuilt buffers: R = mla_prefill_kv_rows(max_blocks_per_seq) rows per
+ * sequence (64 * max_blocks_per_seq rounded up to a multiple of 128);
+ * k_nope and v are bf16 [B, R, H, d_h], k_rope is bf16 [B, R, d_r]; row s of
+ * sequence b is cached token s.  All device pointers, owned by the caller,
+ * 16-byte aligned.
+ */
+int mla_prefill_kv_rows(int max_blocks_per_seq);   /* 0 for invalid input; host only */
+
+/*
+ * mla_prefill_kv -- rebuild k_nope[b, s, h] = W^UK_h c_s, v[b, s, h] =
+ * W^UV_h c_s and copy k_rope[b, s] = R_s k^R_s (the cached rotary key) for
+ * every cached row s < seqlens[b] of every sequence, reading the paged cache
+ * through block_table as mla_decode_paged does.  w_uk and w_uv are bf16
+ * [H * d_h, d_c] (row h * d_h + i is output feature i of head h).  Rows from
+ * seqlens[b] up to the next multiple of 128 are written as zeros (the
+ * attention call reads them, masked); later rows are not touched.
+ * Host errors: MLA_ERR_INVALID_ARG (bad sizes, NULL or unaligned pointers),
+ * MLA_ERR_UNSUPPORTED.  Device errors (MLA_ERR_BAD_INDEX, via
+ * mla_check_status): seqlens[b] < 0 or > 64 * max_blocks_per_seq (nothing
+ * written for b), a block id outside [0, num_blocks) (its page reads as
+ * zeros).  MLA_ERR_TIMEOUT: a bounded wait in the kernel gave up.
+ * Asynchronous on `stream`.
+ */
+int mla_prefill_kv(const void* kv_cache, int dtype, const int32_t* block_table,
+                   const int32_t* seqlens, int B, int d_c, int d_r, int page_size,
+                   int max_blocks_per_seq, int num_blocks, const void* w_uk, const void* w_uv,
+                   int H, int d_h, void* k_nope, void* v, void* k_rope, void* stream);
+
+/*
+ * mla_prefill_attention -- causal softmax attention of T_q new tokens per
+ * sequence over the rebuilt keys and values.  Query t of sequence b sits at
+ * position seqlens[b] - T_q + t (seqlens counts every cached row, the new
+ * tokens' included) and sees keys 0 .. that position.  q_nope is bf16
+ * [B, T_q, H, d_h] (the content query q^C_h); q_rope is bf16
+ * [B, T_q, H, d_r], NOT rotated: the call rotates it by the query's position
+ * (adjacent pairs, theta_i = rope_base^(-2i/d_r), as mla_absorb_query).
+ * k_nope, v, k_rope as written by mla_prefill_kv for the same
+ * max_blocks_per_seq (rows from seqlens[b] to the next multiple of 128 must
+ * be finite).  Outputs: o [B, T_q, H, d_h] fp32 = sum_s p_s v_{s,h};
+ * lse [B, T_q, H] fp32 natural-log log-sum-exp of the scaled scores, or NULL.
+ * Host errors: MLA_ERR_INVALID_ARG (bad sizes, softmax_scale <= 0, NULL or
+ * unaligned pointers), MLA_ERR_UNSUPPORTED.  Device errors (MLA_ERR_BAD_INDEX):
+ * seqlens[b] < T_q or > 64 * max_blocks_per_seq (zeros written for b).
+ * MLA_ERR_TIMEOUT: a bounded wait gave up.  Asynchronous on `stream`.
+ */
+int mla_prefill_attention(const void* q_nope, const void* q_rope, int dtype, const void* k_nope,
+                          const void* v, const void* k_rope, const int32_t* seqlens, int B,
+                          int T_q, int H, int d_h, int d_r, int max_blocks_per_seq,
+                          float rope_base, float softmax_scale, float* o, float* lse,
+                          void* stream);
+
 /* Text for a status code (static storage). */
 const char* mla_status_string(int status);
 

@@ -259,3 +259,86 @@ def shuffled_block_table(rng: np.random.Generator, n_tokens: int, num_blocks: in
         raise ValueError("pool too small")
     perm = rng.permutation(num_blocks).astype(np.int32)
     return perm[:nb].reshape(1, nb).copy()
+
+
+# --------------------------------------------------------------------------
+# prefill inputs (a chunk of T_q new tokens per sequence over the paged cache)
+# --------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class PrefillSpec:
+    """Prefill over per-head keys and values rebuilt from the latent cache."""
+    name: str
+    seed: int
+    B: int
+    H: int
+    T_q: int
+    seqlen: Optional[int] = None
+    seqlens: Optional[tuple] = None
+    d_h: int = 128
+    d_c: int = 512
+    d_r: int = 64
+    rope_base: float = 10000.0
+    softmax_scale: float = 1.0 / math.sqrt(192.0)
+
+
+# DeepSeek-V2-scale prefill of one 4096-token prompt
+V2_PREFILL = PrefillSpec("prefill_b1_t4096_h128", seed=5, B=1, H=128, T_q=4096, seqlen=4096)
+PREFILL_WORKLOADS = {V2_PREFILL.name: V2_PREFILL}
+
+
+def prefill_kv_rows(max_blocks: int) -> int:
+    """Rows per sequence of the rebuilt K/V buffers: 64 * max_blocks rounded up to 128."""
+    return (max_blocks * PAGE + 127) // 128 * 128
+
+
+@dataclasses.dataclass
+class PrefillInputs:
+    spec: PrefillSpec
+    cache: DecodeInputs          # seqlens, offsets, block_table, cache_bits, pool_bits
+    q_nope_bits: np.ndarray      # uint16 [B, T_q, H, d_h]
+    q_rope_bits: np.ndarray      # uint16 [B, T_q, H, d_r]  (not rotated)
+    w_uk_bits: np.ndarray        # uint16 [H * d_h, d_c]
+    w_uv_bits: np.ndarray        # uint16 [H * d_h, d_c]
+    # standalone key/value buffers for the attention call alone (with_kv=True):
+    # [B, R, H, d_h], [B, R, H, d_h], [B, R, d_r]; rows >= L_b are zero
+    k_nope_bits: Optional[np.ndarray] = None
+    v_bits: Optional[np.ndarray] = None
+    k_rope_bits: Optional[np.ndarray] = None
+
+
+def make_prefill_inputs(spec: PrefillSpec, with_kv: bool = False) -> PrefillInputs:
+    """The cache comes from make_decode_inputs with one head (draws 1, 2, 4 of
+    that recipe with the spec's seed; its one-head query is unused).  Then, from
+    default_rng(seed + 7919): q_nope, q_rope ~ N(0, 1); W^UK, W^UV ~
+    N(0, 1/d_c); and with with_kv the standalone buffers k_nope, v, k_rope ~
+    N(0, 1), in that order, all float32 rounded once to bfloat16."""
+    cache = make_decode_inputs(DecodeSpec(spec.name, spec.seed, spec.B, 1, T_q=spec.T_q,
+                                          d_c=spec.d_c, d_r=spec.d_r, seqlen=spec.seqlen,
+                                          seqlens=spec.seqlens))
+    rng = np.random.default_rng(spec.seed + 7919)
+    B, T, H = spec.B, spec.T_q, spec.H
+
+    def draw(shape, scale=1.0):
+        x = rng.standard_normal(shape, dtype=np.float32)
+        if scale != 1.0:
+            x = x * np.float32(scale)
+        return f32_to_bf16_bits(x).reshape(shape)
+
+    q_nope = draw((B, T, H, spec.d_h))
+    q_rope = draw((B, T, H, spec.d_r))
+    w_uk = draw((H * spec.d_h, spec.d_c), 1.0 / math.sqrt(spec.d_c))
+    w_uv = draw((H * spec.d_h, spec.d_c), 1.0 / math.sqrt(spec.d_c))
+    inp = PrefillInputs(spec, cache, q_nope, q_rope, w_uk, w_uv)
+    if with_kv:
+        R = prefill_kv_rows(cache.max_blocks)
+        k = draw((B, R, H, spec.d_h))
+        v = draw((B, R, H, spec.d_h))
+        kr = draw((B, R, spec.d_r))
+        for b in range(B):
+            L = int(cache.seqlens[b])
+            k[b, L:] = 0
+            v[b, L:] = 0
+            kr[b, L:] = 0
+        inp.k_nope_bits, inp.v_bits, inp.k_rope_bits = k, v, kr
+    return inp

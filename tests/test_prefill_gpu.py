@@ -1,0 +1,178 @@
+"""Prefill over rebuilt per-head keys and values (mla_prefill_kv,
+mla_prefill_attention) against the fp64 oracle.
+
+Tolerances:
+  * rebuilt keys and values are stored in bf16: the kernel accumulates the
+    512-term products in fp32 and rounds once, so a value may land one bf16
+    step from the oracle's fp64 value rounded (|err| <= 2^-8 |x| plus 2e-3
+    for the fp32 accumulation of terms of size ~1); the rotary key is a copy,
+    bit for bit; rows past the sequence end are exact zeros;
+  * attention outputs carry the bf16 rounding of the probabilities and of the
+    rotated query (each a relative 2^-9 per element): the decode tolerances,
+    max abs 2e-2 and relative L2 5e-3, and 2e-2 on the log-sum-exp.
+"""
+import numpy as np
+import pytest
+import torch
+
+import head_latent_attention_28_b300 as mla
+import mla_inputs as mi
+import oracle as orc
+from gpu_util import assert_decode_close, bits_to_device
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # three query tokens at the end of a 1000-row sequence, and a 3-row one
+    mi.PrefillSpec("pf_small_chunk_h4", seed=62, B=2, H=4, T_q=3, seqlens=(3, 1000)),
+    # pure prefill of 200 tokens (two query tiles, a ragged second one)
+    mi.PrefillSpec("pf_pure_t200_h8", seed=60, B=1, H=8, T_q=200, seqlens=(200,)),
+    # chunked prefill with earlier context; 12 heads (head groups of 8 and 4)
+    mi.PrefillSpec("pf_chunk_ragged_h12", seed=61, B=3, H=12, T_q=130, seqlens=(130, 400, 259)),
+    # DeepSeek-V2 head count, 256 new tokens after 128 cached ones
+    mi.PrefillSpec("pf_h128_t256", seed=63, B=1, H=128, T_q=256, seqlens=(384,)),
+]
+IDS = [c.name for c in CASES]
+
+
+def f64(bits):
+    return mi.bf16_bits_to_f32(bits).reshape(bits.shape).astype(np.float64)
+
+
+def upload(inp):
+    c = inp.cache
+    return dict(pool=bits_to_device(c.pool_bits), bt=torch.from_numpy(c.block_table).cuda(),
+                sl=torch.from_numpy(c.seqlens).cuda(), qn=bits_to_device(inp.q_nope_bits),
+                qr=bits_to_device(inp.q_rope_bits), wuk=bits_to_device(inp.w_uk_bits),
+                wuv=bits_to_device(inp.w_uv_bits))
+
+
+def positions(inp, b):
+    L = int(inp.cache.seqlens[b])
+    return np.arange(L - inp.spec.T_q, L)
+
+
+def oracle_chain(inp, b):
+    """fp64: rebuild the sequence's keys and values, then attend."""
+    s, c = inp.spec, inp.cache
+    k, v, kr = orc.rebuild_kv(f64(c.seq_rows(b)), s.H, f64(inp.w_uk_bits), f64(inp.w_uv_bits), s.d_c)
+    return orc.prefill_attention(f64(inp.q_nope_bits[b]), f64(inp.q_rope_bits[b]), positions(inp, b),
+                                 k, v, kr, s.softmax_scale, s.rope_base)
+
+
+@pytest.mark.parametrize("spec", CASES, ids=IDS)
+def test_prefill_kv_matches_oracle(spec):
+    inp = mi.make_prefill_inputs(spec)
+    dev = upload(inp)
+    k, v, kr = mla.mla_prefill_kv(dev["pool"], dev["bt"], dev["sl"], dev["wuk"], dev["wuv"], H=spec.H)
+    assert mla.mla_check_status() == mla.MLA_OK
+    R = mi.prefill_kv_rows(inp.cache.max_blocks)
+    assert k.shape == (spec.B, R, spec.H, spec.d_h) and R == mla.mla_prefill_kv_rows(inp.cache.max_blocks)
+    k, v = k.float().cpu().numpy(), v.float().cpu().numpy()
+    kr_bits = kr.view(torch.int16).cpu().numpy().view(np.uint16)
+    for b in range(spec.B):
+        L = int(inp.cache.seqlens[b])
+        rows = inp.cache.seq_rows(b)
+        want_k, want_v, _ = orc.rebuild_kv(f64(rows), spec.H, f64(inp.w_uk_bits), f64(inp.w_uv_bits), spec.d_c)
+        for got, want, what in ((k[b, :L], want_k, "k_nope"), (v[b, :L], want_v, "v")):
+            err = np.abs(got - want)
+            bound = 2.0 ** -8 * np.abs(want) + 2e-3
+            assert np.all(err <= bound), f"{spec.name} {what}: worst {np.max(err - bound):.3e} over bound"
+        # the rotary key is copied bit for bit; the padding rows of the last tile are zeros
+        assert np.array_equal(kr_bits[b, :L], rows[:, spec.d_c:])
+        pad = (L + 127) // 128 * 128
+        assert not np.any(k[b, L:pad]) and not np.any(v[b, L:pad]) and not np.any(kr_bits[b, L:pad])
+
+
+@pytest.mark.parametrize("spec", CASES, ids=IDS)
+def test_prefill_attention_matches_oracle(spec):
+    inp = mi.make_prefill_inputs(spec, with_kv=True)
+    dev = upload(inp)
+    kn, vv, kr = (bits_to_device(x) for x in (inp.k_nope_bits, inp.v_bits, inp.k_rope_bits))
+    o, lse = mla.mla_prefill_attention(dev["qn"], dev["qr"], kn, vv, kr, dev["sl"],
+                                       max_blocks_per_seq=inp.cache.max_blocks,
+                                       softmax_scale=spec.softmax_scale, rope_base=spec.rope_base)
+    assert mla.mla_check_status() == mla.MLA_OK
+    o, lse = o.double().cpu().numpy(), lse.double().cpu().numpy()
+    for b in range(spec.B):
+        want_o, want_lse = orc.prefill_attention(
+            f64(inp.q_nope_bits[b]), f64(inp.q_rope_bits[b]), positions(inp, b), f64(inp.k_nope_bits[b]),
+            f64(inp.v_bits[b]), f64(inp.k_rope_bits[b]), spec.softmax_scale, spec.rope_base)
+        assert_decode_close(o[b], want_o, what=f"{spec.name} b={b}")
+        np.testing.assert_allclose(lse[b], want_lse, rtol=0, atol=2e-2)
+
+
+@pytest.mark.parametrize("spec", CASES, ids=IDS)
+def test_prefill_chain_matches_oracle(spec):
+    inp = mi.make_prefill_inputs(spec)
+    dev = upload(inp)
+    k, v, kr = mla.mla_prefill_kv(dev["pool"], dev["bt"], dev["sl"], dev["wuk"], dev["wuv"], H=spec.H)
+    o, lse = mla.mla_prefill_attention(dev["qn"], dev["qr"], k, v, kr, dev["sl"],
+                                       max_blocks_per_seq=inp.cache.max_blocks,
+                                       softmax_scale=spec.softmax_scale, rope_base=spec.rope_base)
+    assert mla.mla_check_status() == mla.MLA_OK
+    o, lse = o.double().cpu().numpy(), lse.double().cpu().numpy()
+    for b in range(spec.B):
+        want_o, want_lse = oracle_chain(inp, b)
+        assert_decode_close(o[b], want_o, what=f"{spec.name} b={b}")
+        np.testing.assert_allclose(lse[b], want_lse, rtol=0, atol=2e-2)
+
+
+def test_prefill_bad_length_reports_and_writes_zeros():
+    spec = mi.PrefillSpec("pf_bad_len", seed=64, B=2, H=4, T_q=5, seqlens=(5, 300))
+    inp = mi.make_prefill_inputs(spec, with_kv=True)
+    dev = upload(inp)
+    kn, vv, kr = (bits_to_device(x) for x in (inp.k_nope_bits, inp.v_bits, inp.k_rope_bits))
+    sl = dev["sl"].clone()
+    sl[0] = 4                                   # fewer rows than new tokens
+    o, lse = mla.mla_prefill_attention(dev["qn"], dev["qr"], kn, vv, kr, sl,
+                                       max_blocks_per_seq=inp.cache.max_blocks,
+                                       softmax_scale=spec.softmax_scale)
+    assert mla.mla_check_status() == mla.MLA_ERR_BAD_INDEX
+    assert not torch.any(o[0]) and not torch.any(lse[0])
+    want_o, _ = orc.prefill_attention(
+        f64(inp.q_nope_bits[1]), f64(inp.q_rope_bits[1]), positions(inp, 1), f64(inp.k_nope_bits[1]),
+        f64(inp.v_bits[1]), f64(inp.k_rope_bits[1]), spec.softmax_scale, spec.rope_base)
+    assert_decode_close(o[1].double().cpu().numpy(), want_o, what="valid sequence next to a bad one")
+
+
+def test_prefill_rejects_unsupported_and_bad_args():
+    spec = CASES[0]
+    inp = mi.make_prefill_inputs(spec, with_kv=True)
+    dev = upload(inp)
+    kn, vv, kr = (bits_to_device(x) for x in (inp.k_nope_bits, inp.v_bits, inp.k_rope_bits))
+    with pytest.raises(mla.MLAError) as ei:
+        mla.mla_prefill_attention(dev["qn"], dev["qr"], kn, vv, kr, dev["sl"],
+                                  max_blocks_per_seq=inp.cache.max_blocks, softmax_scale=0.0)
+    assert ei.value.status == mla.MLA_ERR_INVALID_ARG
+    with pytest.raises(mla.MLAError) as ei:
+        mla.mla_prefill_kv(dev["pool"].float(), dev["bt"], dev["sl"], dev["wuk"].float(),
+                           dev["wuv"].float(), H=spec.H)
+    assert ei.value.status == mla.MLA_ERR_UNSUPPORTED
+
+
+@pytest.mark.slow
+def test_prefill_full_size_sampled():
+    """The bench workload (one 4096-token prompt, 128 heads), every output of
+    the rebuild checked on sampled rows and the attention on sampled queries."""
+    spec = mi.V2_PREFILL
+    inp = mi.make_prefill_inputs(spec)
+    dev = upload(inp)
+    k, v, kr = mla.mla_prefill_kv(dev["pool"], dev["bt"], dev["sl"], dev["wuk"], dev["wuv"], H=spec.H)
+    o, lse = mla.mla_prefill_attention(dev["qn"], dev["qr"], k, v, kr, dev["sl"],
+                                       max_blocks_per_seq=inp.cache.max_blocks,
+                                       softmax_scale=spec.softmax_scale, rope_base=spec.rope_base)
+    assert mla.mla_check_status() == mla.MLA_OK
+    rows = f64(inp.cache.seq_rows(0))
+    want_k, want_v, want_kr = orc.rebuild_kv(rows, spec.H, f64(inp.w_uk_bits), f64(inp.w_uv_bits), spec.d_c)
+    rng = np.random.default_rng(11)
+    sample_rows = np.concatenate([[0, 127, 128, 4095], rng.integers(0, 4096, 12)])
+    kk, vv = k[0, sample_rows].float().cpu().numpy(), v[0, sample_rows].float().cpu().numpy()
+    for got, want in ((kk, want_k[sample_rows]), (vv, want_v[sample_rows])):
+        assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 2e-3)
+    queries = np.concatenate([[0, 1, 127, 128, 4095], rng.integers(0, 4096, 7)])
+    pos = positions(inp, 0)[queries]
+    want_o, want_lse = orc.prefill_attention(f64(inp.q_nope_bits[0, queries]), f64(inp.q_rope_bits[0, queries]),
+                                             pos, want_k, want_v, want_kr, spec.softmax_scale, spec.rope_base)
+    assert_decode_close(o[0, queries].double().cpu().numpy(), want_o, what="full-size sampled queries")
+    np.testing.assert_allclose(lse[0, queries].double().cpu().numpy(), want_lse, rtol=0, atol=2e-2)
