@@ -489,18 +489,253 @@ def run_mla(args, spec):
     return 0
 
 
+# --------------------------------------------------------------------------
+# prefill over rebuilt per-head keys and values
+# --------------------------------------------------------------------------
+
+PREFILL_METRIC = "MLA prefill TFLOP/s (rebuild of per-head K/V + causal attention), % of B300 bf16 peak"
+
+
+def prefill_work(spec: mi.PrefillSpec, seqlens: np.ndarray):
+    """FLOPs the method must do: the rebuild of k = W^UK_h c and v = W^UV_h c
+    for every cached row and head (2 products of d_c x d_h), and per (query,
+    visible key, head) a (d_h + d_r)-wide score and a d_h-wide value sum."""
+    L = seqlens.astype(np.int64)
+    rebuild = int(L.sum()) * spec.H * 2 * (2 * spec.d_c * spec.d_h)
+    vis = sum(int(l) - spec.T_q + t + 1 for l in L for t in range(spec.T_q))
+    attn = 2 * spec.H * vis * (spec.d_h + spec.d_r + spec.d_h)
+    return dict(rebuild_flops=rebuild, attn_flops=attn, flops=rebuild + attn)
+
+
+def prefill_config(spec, note):
+    return {"workload": spec.name, "global_batch": spec.B, "seq_len": spec.seqlen,
+            "heads": spec.H, "q_tokens": spec.T_q, "d_c": spec.d_c, "d_h": spec.d_h,
+            "d_rope": spec.d_r, "page": mi.PAGE, "cache_dtype": "bf16",
+            "softmax_scale": spec.softmax_scale, "l2": note, "parallelism": "replicas"}
+
+
+def time_prefill_oracle(inp, queries):
+    """The fp64 oracle on the rebuild of the whole prompt and the attention of
+    the given query tokens of sequence 0; returns (seconds, flops)."""
+    import oracle as orc
+    s, c = inp.spec, inp.cache
+    f64 = lambda b: mi.bf16_bits_to_f32(b).reshape(b.shape).astype(np.float64)  # noqa: E731
+    L = int(c.seqlens[0])
+    pos = np.arange(L - s.T_q, L)[queries]
+    t0 = time.perf_counter()
+    k, v, kr = orc.rebuild_kv(f64(c.seq_rows(0)), s.H, f64(inp.w_uk_bits), f64(inp.w_uv_bits), s.d_c)
+    orc.prefill_attention(f64(inp.q_nope_bits[0, queries]), f64(inp.q_rope_bits[0, queries]), pos,
+                          k, v, kr, s.softmax_scale, s.rope_base)
+    dt = time.perf_counter() - t0
+    flops = L * s.H * 4 * s.d_c * s.d_h + 2 * s.H * int((pos + 1).sum()) * (2 * s.d_h + s.d_r)
+    return dt, flops
+
+
+def prefill_cpu_sample(inp, budget_s):
+    rng = np.random.default_rng(0)
+    done_s, done_f, nq = 0.0, 0, 0
+    while done_s < budget_s:
+        qs = rng.integers(0, inp.spec.T_q, 64)
+        dt, fl = time_prefill_oracle(inp, qs)
+        done_s += dt
+        done_f += fl
+        nq += len(qs)
+    return done_s, done_f, nq
+
+
+def run_prefill_reference(args, spec):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    inp = mi.make_prefill_inputs(spec)
+    for _ in range(args.warmup):
+        time_prefill_oracle(inp, np.arange(4))
+    tot_s, tot_f = 0.0, 0
+    rng = np.random.default_rng(1)
+    for _ in range(args.steps):
+        dt, fl = time_prefill_oracle(inp, rng.integers(0, spec.T_q, 16))
+        tot_s += dt
+        tot_f += fl
+    value = tot_f / tot_s / 1e12
+    sample = (f"per step: the rebuild of all {spec.seqlen} rows x {spec.H} heads and the "
+              f"attention of 16 random query tokens of the prompt")
+    line = {"impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": prefill_config(spec, "fp64 numpy oracle on host cores"),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_prefill(args, spec):
+    import torch
+    rank, world, local, dist = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    import head_latent_attention_28_b300 as mla
+    dev = torch.device("cuda", local)
+    rspec = mi.PrefillSpec(**{**spec.__dict__, "seed": spec.seed + rank})
+    inp = mi.make_prefill_inputs(rspec)
+    work = prefill_work(rspec, inp.cache.seqlens)
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+    pool, qn, qr = up(inp.cache.pool_bits), up(inp.q_nope_bits), up(inp.q_rope_bits)
+    wuk, wuv = up(inp.w_uk_bits), up(inp.w_uv_bits)
+    bt = torch.from_numpy(inp.cache.block_table).to(dev)
+    sl = torch.from_numpy(inp.cache.seqlens).to(dev)
+    mb = inp.cache.max_blocks
+    R = mla.mla_prefill_kv_rows(mb)
+    B, T_q, H, d_h = qn.shape
+    kv = (torch.empty((B, R, H, d_h), device=dev, dtype=torch.bfloat16),
+          torch.empty((B, R, H, d_h), device=dev, dtype=torch.bfloat16),
+          torch.empty((B, R, spec.d_r), device=dev, dtype=torch.bfloat16))
+    o = torch.empty((B, T_q, H, d_h), device=dev, dtype=torch.float32)
+    lse = torch.empty((B, T_q, H), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev)
+
+    def rebuild():
+        mla.mla_prefill_kv(pool, bt, sl, wuk, wuv, H=H, out=kv, stream=stream)
+
+    def attend(q_nope=qn, q_rope=qr):
+        mla.mla_prefill_attention(q_nope, q_rope, *kv, sl, max_blocks_per_seq=mb,
+                                  softmax_scale=spec.softmax_scale, rope_base=spec.rope_base,
+                                  o=o, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        rebuild()
+        attend()
+    if mla.mla_check_status(stream) != mla.MLA_OK:
+        raise SystemExit("prefill failed")
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier(dist, local)
+    torch.cuda.synchronize(dev)
+    with sampler:
+        sampler.mark("start")
+        ev0.record(stream)
+        for _ in range(args.steps):
+            rebuild()
+            attend()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        sampler.mark("end")
+    barrier(dist, local)
+    ms_max = max_over_ranks(dist, ev0.elapsed_time(ev1))
+    if mla.mla_check_status(stream) != mla.MLA_OK:
+        raise SystemExit("prefill reported a device error in the timed region")
+
+    # per-kernel durations on the launching stream
+    K2 = max(args.steps, 10)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K2)]
+    torch.cuda.synchronize(dev)
+    for i in range(K2):
+        evs[i][0].record(stream)
+        rebuild()
+        evs[i][1].record(stream)
+        attend()
+        evs[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    kv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    at_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+
+    # end to end: the prompt's queries in from pinned host memory, o and lse back
+    qn_h, qr_h = qn.cpu().pin_memory(), qr.cpu().pin_memory()
+    sl_h = sl.cpu().pin_memory()
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    qn_d, qr_d, sl_d = torch.empty_like(qn), torch.empty_like(qr), torch.empty_like(sl)
+    h2d = (qn_h.numel() + qr_h.numel()) * 2 + sl_h.numel() * 4
+    d2h = (o_h.numel() + lse_h.numel()) * 4
+
+    def e2e_step():
+        qn_d.copy_(qn_h, non_blocking=True)
+        qr_d.copy_(qr_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        mla.mla_prefill_kv(pool, bt, sl_d, wuk, wuv, H=H, out=kv, stream=stream)
+        mla.mla_prefill_attention(qn_d, qr_d, *kv, sl_d, max_blocks_per_seq=mb,
+                                  softmax_scale=spec.softmax_scale, rope_base=spec.rope_base,
+                                  o=o, lse=lse, stream=stream)
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(dist, local)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1))
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+    peaks, peak_src = load_peaks()
+    total_flops = work["flops"] * world * args.steps
+    value = total_flops / (ms_max / 1e3) / 1e12
+    at_tflops = work["attn_flops"] / (at_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": at_tflops, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": at_tflops / peaks["bf16_tflops"],
+                "traffic": profiled_traffic("prefill_tc.cu", spec.name),
+                "kernel": "prefill_tc.cu (prefill_attn_kernel)", "kernel_ms": at_ms,
+                "rebuild_ms": kv_ms,
+                "rebuild_tflops": work["rebuild_flops"] / (kv_ms / 1e3) / 1e12,
+                "peak_source": peak_src + " (burst; kernel timed alone)",
+                "step_frac_of_peak": value / world / peaks["bf16_tflops"]}
+    line = {
+        "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded normal draws, shuffled block table)",
+        "config": prefill_config(spec, "the rebuilt K/V of each step (%d MB) exceed L2" %
+                                 (sum(x.numel() for x in kv) * 2 // 10**6)),
+        "tokens_per_s": spec.B * spec.T_q * world * args.steps / (ms_max / 1e3),
+        "roofline": roofline,
+        "e2e": {"value": total_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / args.steps,
+                "note": "per step: q_nope, q_rope and lengths copied in from pinned host "
+                        "memory, o and lse copied back; cache and weights resident"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        sec, fl, nq = prefill_cpu_sample(inp, args.cpu_budget)
+        line["cpu_baseline"] = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
+                                "kind": "oracle",
+                                "sample": f"fp64 numpy: the rebuild of all rows and the attention "
+                                          f"of {nq} random query tokens, {sec:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["mla", "reference"], default="mla")
-    ap.add_argument("--workload", default=mi.V2_DECODE.name, choices=sorted(mi.DECODE_WORKLOADS))
+    ap.add_argument("--workload", default=mi.V2_DECODE.name,
+                    choices=sorted(mi.DECODE_WORKLOADS) + sorted(mi.PREFILL_WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload in mi.PREFILL_WORKLOADS:
+        pspec = mi.PREFILL_WORKLOADS[args.workload]
+        return run_prefill_reference(args, pspec) if args.impl == "reference" else run_prefill(args, pspec)
     spec = mi.DECODE_WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, spec)
