@@ -590,8 +590,8 @@ def run_prefill(args, spec):
     mb = inp.cache.max_blocks
     R = mla.mla_prefill_kv_rows(mb)
     B, T_q, H, d_h = qn.shape
-    kv = (torch.empty((B, R, H, d_h), device=dev, dtype=torch.bfloat16),
-          torch.empty((B, R, H, d_h), device=dev, dtype=torch.bfloat16),
+    kv = (torch.empty((B, H, R, d_h), device=dev, dtype=torch.bfloat16),
+          torch.empty((B, H, R, d_h), device=dev, dtype=torch.bfloat16),
           torch.empty((B, R, spec.d_r), device=dev, dtype=torch.bfloat16))
     o = torch.empty((B, T_q, H, d_h), device=dev, dtype=torch.float32)
     lse = torch.empty((B, T_q, H), device=dev, dtype=torch.float32)

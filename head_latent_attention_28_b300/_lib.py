@@ -348,7 +348,7 @@ def mla_prefill_kv_rows(max_blocks_per_seq) -> int:
 
 
 def mla_prefill_kv(kv_cache, block_table, seqlens, w_uk, w_uv, *, H, out=None, stream=None):
-    """Rebuild k_nope = W^UK_h c_s, v = W^UV_h c_s ([B, R, H, d_h] bf16) and copy
+    """Rebuild k_nope = W^UK_h c_s, v = W^UV_h c_s ([B, H, R, d_h] bf16) and copy
     k_rope = R_s k^R_s ([B, R, d_r]) for every cached row.  Returns
     (k_nope, v, k_rope)."""
     num_blocks, page, D = kv_cache.shape
@@ -360,8 +360,8 @@ def mla_prefill_kv(kv_cache, block_table, seqlens, w_uk, w_uv, *, H, out=None, s
     R = mla_prefill_kv_rows(max_blocks)
     if out is None:
         dev = kv_cache.device
-        out = (torch.empty((B, R, H, d_h), device=dev, dtype=kv_cache.dtype),
-               torch.empty((B, R, H, d_h), device=dev, dtype=kv_cache.dtype),
+        out = (torch.empty((B, H, R, d_h), device=dev, dtype=kv_cache.dtype),
+               torch.empty((B, H, R, d_h), device=dev, dtype=kv_cache.dtype),
                torch.empty((B, R, d_r), device=dev, dtype=kv_cache.dtype))
     k_nope, v, k_rope = out
     st = lib().mla_prefill_kv(
@@ -384,8 +384,8 @@ def mla_prefill_attention(q_nope, q_rope, k_nope, v, k_rope, seqlens, *, max_blo
     if q_rope.shape[:3] != (B, T_q, H) or seqlens.shape != (B,):
         raise ValueError("shape mismatch")
     R = mla_prefill_kv_rows(max_blocks_per_seq)
-    if k_nope.shape != (B, R, H, d_h) or v.shape != (B, R, H, d_h) or k_rope.shape != (B, R, d_r):
-        raise ValueError("K/V buffers must be [B, R, H, d_h] and [B, R, d_r]")
+    if k_nope.shape != (B, H, R, d_h) or v.shape != (B, H, R, d_h) or k_rope.shape != (B, R, d_r):
+        raise ValueError("K/V buffers must be [B, H, R, d_h] and [B, R, d_r]")
     dev = q_nope.device
     if o is None:
         o = torch.empty((B, T_q, H, d_h), device=dev, dtype=torch.float32)

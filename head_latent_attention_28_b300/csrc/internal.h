@@ -91,7 +91,7 @@ struct PrefillKvArgs {
   const void* w_uk; const void* w_uv;   // [H * d_h, d_c]
   int H, d_h;
   int R;                                // rows per sequence of the outputs
-  void* k_nope; void* v;                // [B, R, H, d_h]
+  void* k_nope; void* v;                // [B, H, R, d_h] (head-major)
   void* k_rope;                         // [B, R, d_r]
   unsigned* err;
 };

@@ -456,7 +456,7 @@ int mla_prefill_kv(const void* kv_cache, int dtype, const int32_t* block_table,
       !al16(k_nope) || !al16(v) || !al16(k_rope))
     return MLA_ERR_INVALID_ARG;
   const int R = mla::prefill_kv_rows(max_blocks_per_seq);
-  if (B > 65535 || H > 65535 * 8 || (long long)B * R * H * d_h >= (1LL << 40) ||
+  if (B > 65535 || H > 65535 * 8 || (long long)B * R * H >= (1LL << 31) ||
       (long long)num_blocks * MLA_PAGE_SIZE >= (1LL << 31) || (long long)B * R >= (1LL << 31))
     return MLA_ERR_UNSUPPORTED;
   mla::PrefillKvArgs a{kv_cache, block_table, seqlens, B, max_blocks_per_seq, num_blocks, d_c, d_r,
@@ -483,7 +483,8 @@ int mla_prefill_attention(const void* q_nope, const void* q_rope, int dtype, con
       !al16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return MLA_ERR_INVALID_ARG;
   const int R = mla::prefill_kv_rows(max_blocks_per_seq);
-  if (B > 65535 || H > 65535 || (long long)B * T_q >= (1LL << 31) || (long long)B * R >= (1LL << 31) ||
+  if (B > 65535 || H > 65535 || (long long)B * T_q >= (1LL << 31) ||
+      (long long)B * H * R >= (1LL << 31) ||
       (long long)(T_q + 127) / 128 > 0x7fffffffLL)
     return MLA_ERR_UNSUPPORTED;
   mla::PrefillAttnArgs a{q_nope, q_rope, k_nope, v, k_rope, seqlens, B, T_q, H, d_h, d_r, R,

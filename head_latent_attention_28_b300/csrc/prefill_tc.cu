@@ -19,7 +19,7 @@
 //    (256 x 512) in 64-column chunks; tcgen05.mma with M = 128 rows, N = 256,
 //    K = 512 accumulates both products of a head in TMEM (two buffers, so the
 //    epilogue of one head overlaps the MMAs of the next).  Four warps convert
-//    to bf16 and write k_nope[b, s, h, :] and v[b, s, h, :]; rows past the
+//    to bf16 and write k_nope[b, h, s, :] and v[b, h, s, :]; rows past the
 //    sequence end inside its last tile are written as zeros.  The first head
 //    group also copies the rotated rotary key R_s k^R_s of each row.
 //  * prefill_attn_kernel: one CTA per (128-token query tile, head, sequence),
@@ -220,7 +220,7 @@ prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_
       if (!warp_ok(mbar_wait(&d_full[d], (hh >> 1) & 1, abort_flag, kPfWaitNs), abort_flag, a.err))
         break;
       tc_fence_after();
-      const size_t off = (orow * a.H + (h0 + hh)) * a.d_h;
+      const size_t off = (((size_t)b * a.H + (h0 + hh)) * a.R + row) * a.d_h;
       __nv_bfloat16* kd = static_cast<__nv_bfloat16*>(a.k_nope) + off;
       __nv_bfloat16* vd = static_cast<__nv_bfloat16*>(a.v) + off;
 #pragma unroll 1
@@ -276,10 +276,12 @@ constexpr int kAtStages = 2;
 constexpr int kAtOffK = kAtQ;
 constexpr int kAtOffV = kAtOffK + kAtStages * kAtK;
 constexpr int kAtSmem = kAtOffV + kAtStages * kAtV + 1024;
-// TMEM columns: two score buffers, the output, two probability buffers (bf16 pairs)
-constexpr uint32_t kTS = 0, kTO = 256, kTP = 384;
+constexpr int kAtThreads = 320;          // 10 warps: producer, MMA issuer, 2 x 4 row warps
+// TMEM columns: two score buffers (each half's probabilities overwrite the
+// first 32 columns of its half of the buffer), then the two halves' outputs
+constexpr uint32_t kTS = 0, kTO = 256;
 
-__global__ void __launch_bounds__(kPfThreads, 1)
+__global__ void __launch_bounds__(kAtThreads, 1)
 prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_kr,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ RopeFreqs fr) {
@@ -287,7 +289,8 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   __shared__ uint64_t q_full, q_ready, k_full[kAtStages], k_empty[kAtStages], v_full[kAtStages],
-      v_empty[kAtStages], s_full[2], s_free[2], p_full[2], pv_done[2], mma_final;
+      v_empty[kAtStages], s_full[2], p_full[2], pv_done[2], grp, mma_final;
+  __shared__ float row_m[2][128], row_l[2][128];   // per-half row statistics for the final merge
   __shared__ uint32_t tbase;
   __shared__ int abort_raw, never_raw;
   volatile int* abort_flag = &abort_raw;
@@ -307,7 +310,7 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
     abort_raw = 0;
     never_raw = 0;
     mbar_init(&q_full, 1);
-    mbar_init(&q_ready, 4);
+    mbar_init(&q_ready, 8);
     for (int s = 0; s < kAtStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -316,10 +319,10 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 4);
-      mbar_init(&p_full[s], 4);
+      mbar_init(&p_full[s], 8);
       mbar_init(&pv_done[s], 1);
     }
+    mbar_init(&grp, 8);
     mbar_init(&mma_final, 1);
     fence_mbar_init_cluster();
   }
@@ -331,7 +334,8 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
   uint8_t* sQ = smem;
   uint8_t* sK = smem + kAtOffK;
   uint8_t* sV = smem + kAtOffV;
-  const int krow0 = b * a.R;                   // the sequence's first row in the K/V buffers
+  const int krow0 = (b * a.H + h) * a.R;       // first row of (sequence, head) in k_nope and v
+  const int rrow0 = b * a.R;                   // first row of the sequence in k_rope
   const int n_tok = b * a.T_q + q0;            // the tile's first query row in q_nope
   uint32_t n_k = 0, n_v = 0;                   // producer: key and value tiles issued
   bool q_issued = false;
@@ -347,21 +351,21 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
       bool ok = true;
       for (int j = 0; ok && j < n_kt; ++j) {
         const uint32_t s = j & 1;
-        const int y = krow0 + 128 * j;
+        const int y = krow0 + 128 * j, yr = rrow0 + 128 * j;
         ok = j < 2 || mbar_wait(&k_empty[s], ((j >> 1) - 1) & 1, abort_flag, kPfWaitNs);
         if (!ok) break;
         uint8_t* kd = sK + s * kAtK;
         mbar_arrive_expect_tx(&k_full[s], kAtK);
-        tma_load_3d(kd, &tm_k, &k_full[s], 0, h, y, pol_kv);
-        tma_load_3d(kd + kBox16, &tm_k, &k_full[s], 64, h, y, pol_kv);
-        tma_load_2d(kd + 2 * kBox16, &tm_kr, &k_full[s], 0, y, pol_kv);
+        tma_load_2d(kd, &tm_k, &k_full[s], 0, y, pol_kv);
+        tma_load_2d(kd + kBox16, &tm_k, &k_full[s], 64, y, pol_kv);
+        tma_load_2d(kd + 2 * kBox16, &tm_kr, &k_full[s], 0, yr, pol_kv);
         ++n_k;
         ok = j < 2 || mbar_wait(&v_empty[s], ((j >> 1) - 1) & 1, abort_flag, kPfWaitNs);
         if (!ok) break;
         uint8_t* vd = sV + s * kAtV;
         mbar_arrive_expect_tx(&v_full[s], kAtV);
-        tma_load_3d(vd, &tm_v, &v_full[s], 0, h, y, pol_kv);
-        tma_load_3d(vd + kBox16, &tm_v, &v_full[s], 64, h, y, pol_kv);
+        tma_load_2d(vd, &tm_v, &v_full[s], 0, y, pol_kv);
+        tma_load_2d(vd + kBox16, &tm_v, &v_full[s], 64, y, pol_kv);
         ++n_v;
       }
       if (!ok) {
@@ -371,6 +375,9 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
     }
   } else if (warp == 1) {
     if (lane == 0 && n_kt > 0) {
+      // MMAs issued by one thread run in issue order: the scores of tile
+      // j + 2 overwrite the buffer that holds the probabilities of tile j only
+      // after the value MMAs of tile j (issued earlier) have read them
       const uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);   // Q, K both K-major
       const uint32_t idO = idesc_bf16_f32(128, 128, 0, 1);   // P from TMEM, V MN-major
       bool ok = mbar_wait(&q_full, 0, abort_flag, kPfWaitNs) &&
@@ -379,7 +386,6 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
         if (j < n_kt) {
           const uint32_t s = j & 1;
           ok = mbar_wait(&k_full[s], (j >> 1) & 1, abort_flag, kPfWaitNs);
-          if (ok && j >= 2) ok = mbar_wait(&s_free[s], ((j >> 1) - 1) & 1, abort_flag, kPfWaitNs);
           if (!ok) break;
           tc_fence_after();
           const uint8_t* kd = sK + s * kAtK;
@@ -400,11 +406,16 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
           if (!ok) break;
           tc_fence_after();
           const uint8_t* vd = sV + s * kAtV;
+          // half hf: keys 64 hf .. 64 hf + 63 of the tile, its probabilities in
+          // the first 32 columns of its half of the score buffer, into O_hf
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {   // 16 keys per step
-            const uint64_t bd = sdesc_sw128(smem_u32(vd + kk * 2048), kBox16, 1024);
-            mma_ts(tmem + kTO, tmem + kTP + s * 64 + kk * 8, bd, idO, (i > 0 || kk > 0) ? 1 : 0);
-          }
+          for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {   // 16 keys per step
+              const uint64_t bd = sdesc_sw128(smem_u32(vd + (4 * hf + k4) * 2048), kBox16, 1024);
+              mma_ts(tmem + kTO + hf * 128, tmem + kTS + s * 128 + hf * 64 + k4 * 8, bd, idO,
+                     (i > 0 || k4 > 0) ? 1 : 0);
+            }
           mma_commit(&v_empty[s]);
           mma_commit(&pv_done[s]);
         }
@@ -415,7 +426,10 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
       }
     }
   } else {
-    // row warps: thread = query row r of the tile (TMEM lane r)
+    // row warps: half hf (warps 2-5: keys 0-63 of every tile, warps 6-9: keys
+    // 64-127) runs its own online softmax over its keys into its own output
+    // accumulator O_hf; thread = query row r (TMEM lane r)
+    const int hf = (warp - 2) >> 2;
     const int q4 = warp & 3;
     const int r = 32 * q4 + lane;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
@@ -426,12 +440,12 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
     if (n_kt > 0) {
       // rotary half of the query, rotated by its position, into box 2 of the
       // query tile (K-major, 128-byte swizzle: 16-byte chunk c of row r sits at
-      // chunk c ^ (r & 7))
+      // chunk c ^ (r & 7)); half hf writes chunks 4 hf .. 4 hf + 3
       const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q_rope) + (qrow * a.H + h) * a.d_r;
       const uint64_t pos = (uint64_t)(int64_t)lim;
       uint8_t* qrow_s = sQ + 2 * kBox16 + r * 128;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {   // 16-byte chunk c: rotary pairs 4c .. 4c + 3
+      for (int c = 4 * hf; c < 4 * hf + 4; ++c) {   // 16-byte chunk c: rotary pairs 4c .. 4c + 3
         uint32_t w[4] = {0u, 0u, 0u, 0u};
         if (real) {
 #pragma unroll
@@ -459,24 +473,25 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
       ok = warp_ok(mbar_wait(&s_full[s], (j >> 1) & 1, abort_flag, kPfWaitNs), abort_flag, a.err);
       if (!ok) break;
       tc_fence_after();
-      float x0[64], x1[64];
-      tmem_ld64(tmem + lane_off + kTS + s * 128, x0);
-      tmem_ld64(tmem + lane_off + kTS + s * 128 + 64, x1);
+      const uint32_t sbuf = tmem + lane_off + kTS + s * 128 + hf * 64;
+      float x[64];
+      tmem_ld64(sbuf, x);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[s]);
-      const int key0 = 128 * j;
-      if (key0 + 127 > lim) {   // causal mask (and padding rows: every key)
+      const int key0 = 128 * j + 64 * hf;
+      if (key0 + 63 > lim) {   // causal mask (and padding rows: every key)
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          if (key0 + c > lim) x0[c] = -INFINITY;
-          if (key0 + 64 + c > lim) x1[c] = -INFINITY;
-        }
+        for (int c = 0; c < 64; ++c)
+          if (key0 + c > lim) x[c] = -INFINITY;
       }
-      float mt = -INFINITY;
+      float mq[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-      for (int c = 0; c < 64; ++c) mt = fmaxf(mt, fmaxf(x0[c], x1[c]));
+      for (int c = 4; c < 64; c += 4) {
+        mq[0] = fmaxf(mq[0], x[c]);
+        mq[1] = fmaxf(mq[1], x[c + 1]);
+        mq[2] = fmaxf(mq[2], x[c + 2]);
+        mq[3] = fmaxf(mq[3], x[c + 3]);
+      }
+      const float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       const float m_cand = fmaxf(m_run, mt * sl2);
       const bool grow = m_cand > m_run + kPfRescale;   // also the first finite maximum
       float alpha = 1.f;
@@ -484,7 +499,8 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
         alpha = (m_run == -INFINITY) ? 0.f : ex2f(m_run - m_cand);
         m_run = m_cand;
       }
-      // O holds the value sums of tiles < j: rescale the rows whose maximum grew
+      // O_hf holds this half's value sums of tiles < j: rescale the rows whose
+      // maximum grew, once the value MMAs of tile j - 1 are complete
       if (__any_sync(0xffffffffu, grow && l_run > 0.f)) {
         ok = warp_ok(mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, kPfWaitNs),
                      abort_flag, a.err);
@@ -493,71 +509,78 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float o[32];
-          tmem_ld32(tmem + lane_off + kTO + 32 * c, o);
+          const uint32_t oc = tmem + lane_off + kTO + hf * 128 + 32 * c;
+          tmem_ld32(oc, o);
           tmem_ld_wait();
           uint32_t u[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(o[e] * alpha);
-          tmem_st32(tmem + lane_off + kTO + 32 * c, u);
+          tmem_st32(oc, u);
         }
         tmem_st_wait();
       }
       l_run *= alpha;
       const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-      // the probability buffer s was last read by the value MMAs of tile j - 2
-      if (j >= 2) {
-        ok = warp_ok(mbar_wait(&pv_done[s], ((j >> 1) - 1) & 1, abort_flag, kPfWaitNs), abort_flag, a.err);
-        if (!ok) break;
-        tc_fence_after();
-      }
-      float sum = 0.f;
+      // probabilities as bf16 pairs over the first 32 columns of this half's
+      // scores (already read into registers)
+      float sq[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2f(fmaf(x0[2 * c], sl2, -mu)), p1 = ex2f(fmaf(x0[2 * c + 1], sl2, -mu));
-        sum += p0 + p1;
+        const float p0 = ex2f(fmaf(x[2 * c], sl2, -mu)), p1 = ex2f(fmaf(x[2 * c + 1], sl2, -mu));
+        sq[c & 3] += p0 + p1;
         pk[c] = pack_bf16x2(p0, p1);
       }
-      tmem_st32(tmem + lane_off + kTP + s * 64, pk);
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2f(fmaf(x1[2 * c], sl2, -mu)), p1 = ex2f(fmaf(x1[2 * c + 1], sl2, -mu));
-        sum += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
-      }
-      tmem_st32(tmem + lane_off + kTP + s * 64 + 32, pk);
+      tmem_st32(sbuf, pk);
       tmem_st_wait();
-      l_run += sum;
+      l_run += (sq[0] + sq[1]) + (sq[2] + sq[3]);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[s]);
     }
-    // epilogue: o = O / l, lse = (m + log2 l) ln 2 (the TMEM loads are
-    // warp-wide; padding rows store nothing)
+    // epilogue: merge the two halves, o = (O_0 a_0 + O_1 a_1) / (l_0 a_0 + l_1 a_1)
+    // with a_h = 2^(m_h - m), lse = (m + log2 l) ln 2.  Half hf writes output
+    // columns 64 hf .. 64 hf + 63; the TMEM loads are warp-wide, padding rows
+    // store nothing.
     if (ok && n_kt > 0)
       ok = warp_ok(mbar_wait(&pv_done[(n_kt - 1) & 1], ((n_kt - 1) >> 1) & 1, abort_flag, kPfWaitNs),
                    abort_flag, a.err);
+    row_m[hf][r] = m_run;
+    row_l[hf][r] = l_run;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&grp);
+    const bool merged = warp_ok(mbar_wait(&grp, 0, abort_flag, kPfWaitNs), abort_flag, a.err);
     float* orow = a.o + (qrow * a.H + h) * a.d_h;
-    if (ok && n_kt > 0) {
+    if (ok && merged && n_kt > 0) {
       tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float m0 = row_m[0][r], m1 = row_m[1][r];
+      float m = fmaxf(m0, m1);
+      if (m == -INFINITY) m = 0.f;   // padding rows
+      const float a0 = ex2f(m0 - m), a1 = ex2f(m1 - m);
+      const float l = row_l[0][r] * a0 + row_l[1][r] * a1;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float f0 = a0 * inv, f1 = a1 * inv;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float o[32];
-        tmem_ld32(tmem + lane_off + kTO + 32 * c, o);
+      for (int c = 0; c < 2; ++c) {
+        const int col = 64 * hf + 32 * c;
+        float o0[32], o1[32];
+        tmem_ld32(tmem + lane_off + kTO + col, o0);
+        tmem_ld32(tmem + lane_off + kTO + 128 + col, o1);
         tmem_ld_wait();
         if (t < a.T_q) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            reinterpret_cast<float4*>(orow + 32 * c)[i] =
-                make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+            reinterpret_cast<float4*>(orow + col)[i] =
+                make_float4(o0[4 * i] * f0 + o1[4 * i] * f1, o0[4 * i + 1] * f0 + o1[4 * i + 1] * f1,
+                            o0[4 * i + 2] * f0 + o1[4 * i + 2] * f1, o0[4 * i + 3] * f0 + o1[4 * i + 3] * f1);
         }
       }
-      if (t < a.T_q && a.lse) a.lse[qrow * a.H + h] = (m_run + log2f(l_run)) * kPfLn2;
+      if (hf == 0 && t < a.T_q && a.lse) a.lse[qrow * a.H + h] = (m + log2f(l)) * kPfLn2;
     } else if (bad && t < a.T_q) {
       // a sequence of invalid length: zeros (the error word says why)
-      for (int c = 0; c < 32; ++c) reinterpret_cast<float4*>(orow)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (a.lse) a.lse[qrow * a.H + h] = 0.f;
+      for (int c = 0; c < 16; ++c)
+        reinterpret_cast<float4*>(orow + 64 * hf)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (hf == 0 && a.lse) a.lse[qrow * a.H + h] = 0.f;
     }
   }
 
@@ -642,7 +665,7 @@ cudaError_t launch_prefill_attn(const PrefillAttnArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   CUtensorMap tm_q, tm_k, tm_kr, tm_v;
   const auto map3 = [&](CUtensorMap* tm, const void* base, long long rows) -> bool {
-    // [rows, H, 128] as a 3-D tensor: box of 64 dims x 1 head x 128 rows
+    // q_nope [B * T_q, H, 128] as a 3-D tensor: box of 64 dims x 1 head x 128 rows
     cuuint64_t dims[3] = {(cuuint64_t)a.d_h, (cuuint64_t)a.H, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)a.d_h * 2, (cuuint64_t)a.H * a.d_h * 2};
     cuuint32_t box[3] = {64, 1, 128};
@@ -652,9 +675,21 @@ cudaError_t launch_prefill_attn(const PrefillAttnArgs& a, cudaStream_t s) {
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   };
   const long long kv_rows = (long long)a.B * a.R;
-  if (!map3(&tm_q, a.q_nope, (long long)a.B * a.T_q) || !map3(&tm_k, a.k_nope, kv_rows) ||
-      !map3(&tm_v, a.v, kv_rows))
-    return cudaErrorInvalidValue;
+  if (!map3(&tm_q, a.q_nope, (long long)a.B * a.T_q)) return cudaErrorInvalidValue;
+  const void* kvs[2] = {a.k_nope, a.v};
+  CUtensorMap* kvm[2] = {&tm_k, &tm_v};
+  for (int i = 0; i < 2; ++i) {
+    // k_nope, v [B, H, R, d_h] as 2-D [B * H * R rows, d_h]: box of 64 dims x
+    // 128 rows, one contiguous 32 KB run per key tile of a head
+    cuuint64_t dims[2] = {(cuuint64_t)a.d_h, (cuuint64_t)kv_rows * a.H};
+    cuuint64_t strides[1] = {(cuuint64_t)a.d_h * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(kvm[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kvs[i]), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   {
     // k_rope [rows, 64]: box of 64 dims x 128 rows
     cuuint64_t dims[2] = {(cuuint64_t)a.d_r, (cuuint64_t)kv_rows};
@@ -670,7 +705,7 @@ cudaError_t launch_prefill_attn(const PrefillAttnArgs& a, cudaStream_t s) {
   e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAtSmem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.T_q + 127) / 128, a.H, a.B);
-  prefill_attn_kernel<<<grid, kPfThreads, kAtSmem, s>>>(a, tm_q, tm_k, tm_kr, tm_v, fr);
+  prefill_attn_kernel<<<grid, kAtThreads, kAtSmem, s>>>(a, tm_q, tm_k, tm_kr, tm_v, fr);
   return cudaGetLastError();
 }
 

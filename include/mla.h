@@ -351,14 +351,15 @@ int mla_decode_path(int T_q, int H, int d_c, int d_r, int dtype);
  *
  * Rebuilt buffers: R = mla_prefill_kv_rows(max_blocks_per_seq) rows per
  * sequence (64 * max_blocks_per_seq rounded up to a multiple of 128);
- * k_nope and v are bf16 [B, R, H, d_h], k_rope is bf16 [B, R, d_r]; row s of
- * sequence b is cached token s.  All device pointers, owned by the caller,
+ * k_nope and v are bf16 [B, H, R, d_h] (head-major: the keys of one head are
+ * contiguous), k_rope is bf16 [B, R, d_r]; row s of sequence b is cached
+ * token s.  All device pointers, owned by the caller,
  * 16-byte aligned.
  */
 int mla_prefill_kv_rows(int max_blocks_per_seq);   /* 0 for invalid input; host only */
 
 /*
- * mla_prefill_kv -- rebuild k_nope[b, s, h] = W^UK_h c_s, v[b, s, h] =
+ * mla_prefill_kv -- rebuild k_nope[b, h, s] = W^UK_h c_s, v[b, h, s] =
  * W^UV_h c_s and copy k_rope[b, s] = R_s k^R_s (the cached rotary key) for
  * every cached row s < seqlens[b] of every sequence, reading the paged cache
  * through block_table as mla_decode_paged does.  w_uk and w_uv are bf16

@@ -301,7 +301,7 @@ class PrefillInputs:
     w_uk_bits: np.ndarray        # uint16 [H * d_h, d_c]
     w_uv_bits: np.ndarray        # uint16 [H * d_h, d_c]
     # standalone key/value buffers for the attention call alone (with_kv=True):
-    # [B, R, H, d_h], [B, R, H, d_h], [B, R, d_r]; rows >= L_b are zero
+    # [B, H, R, d_h], [B, H, R, d_h], [B, R, d_r]; rows >= L_b are zero
     k_nope_bits: Optional[np.ndarray] = None
     v_bits: Optional[np.ndarray] = None
     k_rope_bits: Optional[np.ndarray] = None
@@ -332,13 +332,13 @@ def make_prefill_inputs(spec: PrefillSpec, with_kv: bool = False) -> PrefillInpu
     inp = PrefillInputs(spec, cache, q_nope, q_rope, w_uk, w_uv)
     if with_kv:
         R = prefill_kv_rows(cache.max_blocks)
-        k = draw((B, R, H, spec.d_h))
-        v = draw((B, R, H, spec.d_h))
+        k = draw((B, H, R, spec.d_h))
+        v = draw((B, H, R, spec.d_h))
         kr = draw((B, R, spec.d_r))
         for b in range(B):
             L = int(cache.seqlens[b])
-            k[b, L:] = 0
-            v[b, L:] = 0
+            k[b, :, L:] = 0
+            v[b, :, L:] = 0
             kr[b, L:] = 0
         inp.k_nope_bits, inp.v_bits, inp.k_rope_bits = k, v, kr
     return inp

@@ -67,8 +67,10 @@ def test_prefill_kv_matches_oracle(spec):
     k, v, kr = mla.mla_prefill_kv(dev["pool"], dev["bt"], dev["sl"], dev["wuk"], dev["wuv"], H=spec.H)
     assert mla.mla_check_status() == mla.MLA_OK
     R = mi.prefill_kv_rows(inp.cache.max_blocks)
-    assert k.shape == (spec.B, R, spec.H, spec.d_h) and R == mla.mla_prefill_kv_rows(inp.cache.max_blocks)
-    k, v = k.float().cpu().numpy(), v.float().cpu().numpy()
+    assert k.shape == (spec.B, spec.H, R, spec.d_h) and R == mla.mla_prefill_kv_rows(inp.cache.max_blocks)
+    # head-major buffers, compared as [b, s, h, :]
+    k = k.float().cpu().numpy().transpose(0, 2, 1, 3)
+    v = v.float().cpu().numpy().transpose(0, 2, 1, 3)
     kr_bits = kr.view(torch.int16).cpu().numpy().view(np.uint16)
     for b in range(spec.B):
         L = int(inp.cache.seqlens[b])
@@ -96,8 +98,9 @@ def test_prefill_attention_matches_oracle(spec):
     o, lse = o.double().cpu().numpy(), lse.double().cpu().numpy()
     for b in range(spec.B):
         want_o, want_lse = orc.prefill_attention(
-            f64(inp.q_nope_bits[b]), f64(inp.q_rope_bits[b]), positions(inp, b), f64(inp.k_nope_bits[b]),
-            f64(inp.v_bits[b]), f64(inp.k_rope_bits[b]), spec.softmax_scale, spec.rope_base)
+            f64(inp.q_nope_bits[b]), f64(inp.q_rope_bits[b]), positions(inp, b),
+            f64(inp.k_nope_bits[b]).transpose(1, 0, 2), f64(inp.v_bits[b]).transpose(1, 0, 2),
+            f64(inp.k_rope_bits[b]), spec.softmax_scale, spec.rope_base)
         assert_decode_close(o[b], want_o, what=f"{spec.name} b={b}")
         np.testing.assert_allclose(lse[b], want_lse, rtol=0, atol=2e-2)
 
@@ -131,8 +134,9 @@ def test_prefill_bad_length_reports_and_writes_zeros():
     assert mla.mla_check_status() == mla.MLA_ERR_BAD_INDEX
     assert not torch.any(o[0]) and not torch.any(lse[0])
     want_o, _ = orc.prefill_attention(
-        f64(inp.q_nope_bits[1]), f64(inp.q_rope_bits[1]), positions(inp, 1), f64(inp.k_nope_bits[1]),
-        f64(inp.v_bits[1]), f64(inp.k_rope_bits[1]), spec.softmax_scale, spec.rope_base)
+        f64(inp.q_nope_bits[1]), f64(inp.q_rope_bits[1]), positions(inp, 1),
+        f64(inp.k_nope_bits[1]).transpose(1, 0, 2), f64(inp.v_bits[1]).transpose(1, 0, 2),
+        f64(inp.k_rope_bits[1]), spec.softmax_scale, spec.rope_base)
     assert_decode_close(o[1].double().cpu().numpy(), want_o, what="valid sequence next to a bad one")
 
 
@@ -167,7 +171,8 @@ def test_prefill_full_size_sampled():
     want_k, want_v, want_kr = orc.rebuild_kv(rows, spec.H, f64(inp.w_uk_bits), f64(inp.w_uv_bits), spec.d_c)
     rng = np.random.default_rng(11)
     sample_rows = np.concatenate([[0, 127, 128, 4095], rng.integers(0, 4096, 12)])
-    kk, vv = k[0, sample_rows].float().cpu().numpy(), v[0, sample_rows].float().cpu().numpy()
+    kk = k[0][:, sample_rows].float().cpu().numpy().transpose(1, 0, 2)
+    vv = v[0][:, sample_rows].float().cpu().numpy().transpose(1, 0, 2)
     for got, want in ((kk, want_k[sample_rows]), (vv, want_v[sample_rows])):
         assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 2e-3)
     queries = np.concatenate([[0, 1, 127, 128, 4095], rng.integers(0, 4096, 7)])
