@@ -166,3 +166,43 @@ def test_row_groups_per_kernel():
     # the tensor-core path takes any row count for d_c = 512, d_r = 64, bf16
     assert mla.lib().mla_decode_path(2, 128, 512, 64, mla.MLA_BF16) == 1
     assert mla.lib().mla_decode_path(2, 128, 512, 64, mla.MLA_F32) == 0
+
+
+def test_prefill_rows_and_host_checks():
+    lib = mla.lib()
+    # rows per sequence of the rebuilt K/V: 64 * max_blocks rounded up to 128
+    assert [mla.mla_prefill_kv_rows(m) for m in (1, 2, 3, 64, 65)] == [128, 128, 256, 4096, 4224]
+    assert mla.mla_prefill_kv_rows(0) == 0
+    P = 16  # a non-null, 16-byte aligned dummy address; never dereferenced
+    kv = dict(cache=P, dt=1, bt=P, sl=P, B=1, d_c=512, d_r=64, page=64, maxb=4, nb=4,
+              wuk=P, wuv=P, H=8, d_h=128, k=P, v=P, kr=P, s=None)
+
+    def call_kv(**kw):
+        a = dict(kv, **kw)
+        return lib.mla_prefill_kv(a["cache"], a["dt"], a["bt"], a["sl"], a["B"], a["d_c"], a["d_r"],
+                                  a["page"], a["maxb"], a["nb"], a["wuk"], a["wuv"], a["H"], a["d_h"],
+                                  a["k"], a["v"], a["kr"], a["s"])
+    for bad in (dict(cache=None), dict(bt=None), dict(sl=None), dict(wuk=None), dict(wuv=P + 8),
+                dict(k=None), dict(v=None), dict(kr=None), dict(B=-1), dict(H=0), dict(page=32),
+                dict(maxb=0), dict(nb=0), dict(dt=7)):
+        assert call_kv(**bad) == mla.MLA_ERR_INVALID_ARG, bad
+    for unsup in (dict(dt=0), dict(d_c=256), dict(d_r=32), dict(d_h=64)):
+        assert call_kv(**unsup) == mla.MLA_ERR_UNSUPPORTED, unsup
+    assert call_kv(B=0) == mla.MLA_OK          # nothing to do, no device touched
+
+    at = dict(qn=P, qr=P, dt=1, k=P, v=P, kr=P, sl=P, B=1, T_q=4, H=8, d_h=128, d_r=64, maxb=4,
+              base=10000.0, scale=0.07, o=P, lse=None, s=None)
+
+    def call_at(**kw):
+        a = dict(at, **kw)
+        return lib.mla_prefill_attention(a["qn"], a["qr"], a["dt"], a["k"], a["v"], a["kr"], a["sl"],
+                                         a["B"], a["T_q"], a["H"], a["d_h"], a["d_r"], a["maxb"],
+                                         a["base"], a["scale"], a["o"], a["lse"], a["s"])
+    for bad in (dict(qn=None), dict(qr=None), dict(k=None), dict(v=P + 4), dict(kr=None),
+                dict(sl=None), dict(o=None), dict(lse=P + 2), dict(T_q=0), dict(H=0), dict(B=-1),
+                dict(maxb=0), dict(scale=0.0), dict(scale=-1.0), dict(scale=float("inf")),
+                dict(base=0.0), dict(dt=7)):
+        assert call_at(**bad) == mla.MLA_ERR_INVALID_ARG, bad
+    for unsup in (dict(dt=0), dict(d_h=64), dict(d_r=16)):
+        assert call_at(**unsup) == mla.MLA_ERR_UNSUPPORTED, unsup
+    assert call_at(B=0) == mla.MLA_OK
