@@ -7,10 +7,9 @@
 // ("Attention, Part 2: MQA, GQA and MLA", the MLA equations: the key of head
 // h is [W^UK_h c_s ; R_s k^R_s], its value W^UV_h c_s) brings that down to
 // 2 (d_h + d^R_h) + 2 d_h, plus 4 d_c d_h per (row, head) for the rebuild.
-// With T in the hundreds and more, attention over the rebuilt keys is the
-// cheaper way ("Multi-head latent attention (MLA)", section 2: the up-
-// projections may be applied to the cached latent or absorbed; the result is
-// the same).
+// Past a few dozen new tokens, attention over the rebuilt keys is the cheaper
+// way ("Multi-head latent attention (MLA)", section 2: the up-projections may
+// be applied to the cached latent or absorbed; the result is the same).
 //
 // Two kernels:
 //  * prefill_kv_kernel: one CTA per (sequence, 128-row tile, group of 8
@@ -24,14 +23,17 @@
 //    group also copies the rotated rotary key R_s k^R_s of each row.
 //  * prefill_attn_kernel: one CTA per (128-token query tile, head, sequence),
 //    heavy (late) tiles first.  Scores over d_h + d^R_h = 192 dims
-//    (M = 128 queries, N = 128 keys) into one of two TMEM buffers, a base-2
-//    online softmax with a lazy running max (the output is rescaled only when
-//    a row maximum grows by more than 2^8; exact after the final division),
-//    probabilities to TMEM as bf16 and O += P . V with P read from TMEM
-//    (tcgen05.mma A operand in tensor memory).  Key and value tiles stream
-//    through two-stage rings, so the scores of tile j + 1 run while the
-//    softmax of tile j does.  The query's rotary half is rotated on the fly
-//    (the same fixed-point angle table as the query absorption).
+//    (M = 128 queries, N = 128 keys) go into one of two TMEM buffers.  Two
+//    groups of four softmax warps split every key tile in halves of 64 keys;
+//    each half runs its own base-2 online softmax with a lazy running max
+//    (its output is rescaled only when a row maximum grows by more than 2^8;
+//    exact after the final division), writes its bf16 probabilities over its
+//    own scores in TMEM and accumulates O_h += P_h . V_h in its own TMEM
+//    accumulator (P read from TMEM as the tcgen05.mma A operand).  The halves
+//    merge once, at the end.  Key and value tiles stream through two-stage
+//    rings, so the scores of tile j + 1 run while the softmax of tile j does.
+//    The query's rotary half is rotated on the fly (the same fixed-point angle
+//    table as the query absorption).
 // Every mbarrier wait is bounded (2 s): on expiry the kernel records
 // MLA_ERR_TIMEOUT, lets its copies and MMAs finish, frees TMEM and returns.
 #include <cuda.h>
