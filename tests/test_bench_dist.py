@@ -7,10 +7,12 @@ reduction, the whole-job aggregation, and that only rank 0 runs the reference
 arm.  No GPU is touched.
 """
 import importlib.util
+import json
 import os
 import socket
 import sys
 
+import numpy as np
 import pytest
 import torch.multiprocessing as mp
 
@@ -82,3 +84,34 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
                                     no_cpu_baseline=True)
     assert bench.run_reference(args, bench.mi.V2_DECODE) == 0
     assert capsys.readouterr().out == ""       # no work, no line on the other ranks
+
+
+def test_prefill_flop_count_matches_brute_force():
+    bench = _load_bench()
+    spec = bench.mi.PrefillSpec("tiny", seed=0, B=2, H=3, T_q=4, seqlens=(4, 9), d_h=8, d_c=16, d_r=4)
+    seqlens = np.array(spec.seqlens, dtype=np.int32)
+    w = bench.prefill_work(spec, seqlens)
+    rebuild = sum(L * spec.H * 2 * (2 * spec.d_c * spec.d_h) for L in spec.seqlens)
+    attn = 0
+    for L in spec.seqlens:
+        for t in range(spec.T_q):
+            for s in range(L):
+                if s <= L - spec.T_q + t:        # causal: keys up to the query's position
+                    attn += spec.H * (2 * (spec.d_h + spec.d_r) + 2 * spec.d_h)
+    assert w["rebuild_flops"] == rebuild and w["attn_flops"] == attn
+    assert w["flops"] == rebuild + attn
+
+
+def test_prefill_reference_arm_rank_zero_only_and_line(monkeypatch, capsys):
+    bench = _load_bench()
+    spec = bench.mi.PrefillSpec("tiny_prefill", seed=3, B=1, H=2, T_q=40, seqlens=(70,))
+    args = bench.argparse.Namespace(gpus=2, steps=1, warmup=3, impl="reference",
+                                    workload=spec.name, cpu_budget=1.0, no_cpu_baseline=True)
+    monkeypatch.setenv("RANK", "1")
+    assert bench.run_prefill_reference(args, spec) == 0
+    assert capsys.readouterr().out == ""
+    monkeypatch.setenv("RANK", "0")
+    assert bench.run_prefill_reference(args, spec) == 0
+    line = json.loads(capsys.readouterr().out)
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
