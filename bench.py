@@ -14,7 +14,13 @@ dominant kernel, an end-to-end figure through the public API with host
 buffers, the oracle timed on the host cores, and the SM clocks sampled
 during the timed region.
 
+With --workload prefill_b1_t4096_h128 a step is instead one prefill of a
+4096-token prompt over keys and values rebuilt from the latent cache
+(mla_prefill_kv + mla_prefill_attention, 128 heads), and `value` is its
+algorithmic TFLOP/s against the tensor-core roofline.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mla|reference]
+                  [--workload NAME]
 """
 
 from __future__ import annotations
