@@ -18,6 +18,7 @@ from ._lib import (  # noqa: F401
     mla_absorb_output, mla_absorb_query, mla_cache_append, mla_check_status,
     mla_decode_item_cost, mla_decode_num_workers, mla_decode_paged, mla_decode_paged_noalloc,
     mla_decode_row_groups, mla_decode_split_plan, mla_decode_step, mla_decode_workspace_size,
-    mla_prefill_attention, mla_prefill_kv, mla_prefill_kv_rows, mla_status_string)
+    mla_prefill_attention, mla_prefill_kv, mla_prefill_kv_rows, mla_prefill_use_rebuild,
+    mla_status_string)
 
 lib()  # load now: no silent fallback path exists

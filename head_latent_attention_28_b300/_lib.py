@@ -55,6 +55,7 @@ SIGNATURES = {
     "mla_decode_num_workers": (_I, [_I, _I, _I, _I, _I, _I]),
     "mla_decode_path": (_I, [_I, _I, _I, _I, _I]),
     "mla_prefill_kv_rows": (_I, [_I]),
+    "mla_prefill_use_rebuild": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "mla_prefill_kv": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P]),
     "mla_prefill_attention": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F,
                                    _P, _P, _P]),
@@ -345,6 +346,13 @@ def mla_decode_num_workers(B, T_q, H, d_c, d_r, dtype=torch.bfloat16) -> int:
 def mla_prefill_kv_rows(max_blocks_per_seq) -> int:
     """Rows per sequence R of the rebuilt K/V buffers (64 * max_blocks rounded up to 128)."""
     return int(lib().mla_prefill_kv_rows(int(max_blocks_per_seq)))
+
+
+def mla_prefill_use_rebuild(T_q, L, H, d_c=512, d_r=64, d_h=128, dtype=torch.bfloat16) -> int:
+    """1 if a chunk of T_q tokens over L rows is expected to run faster on the
+    rebuilt-key prefill path than on the absorbed decode, 0 if not, -1 if invalid."""
+    code = MLA_BF16 if dtype == torch.bfloat16 else MLA_F32
+    return int(lib().mla_prefill_use_rebuild(T_q, L, H, d_c, d_r, d_h, code))
 
 
 def mla_prefill_kv(kv_cache, block_table, seqlens, w_uk, w_uv, *, H, out=None, stream=None):

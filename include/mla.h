@@ -359,6 +359,22 @@ int mla_decode_path(int T_q, int H, int d_c, int d_r, int dtype);
 int mla_prefill_kv_rows(int max_blocks_per_seq);   /* 0 for invalid input; host only */
 
 /*
+ * mla_prefill_use_rebuild -- HOST helper: which way to run a chunk of T_q new
+ * tokens per sequence over sequences of L cached rows (the chunk included).
+ * Returns 1 when attention over rebuilt keys (mla_prefill_kv +
+ * mla_prefill_attention) is expected to be faster than the absorbed decode
+ * (mla_decode_paged with T_q query tokens), 0 when the absorbed decode is,
+ * or when the rebuild path does not support the shape, and -1 for invalid
+ * input.  The estimate uses whole-GPU costs measured on B300: about 3.0 us
+ * per group of 128 query rows and 4096 cached rows for the absorbed decode
+ * (each group streams the pages once); about 210 us per 4096 rows at 128
+ * heads for the rebuild, scaled by rows x heads; and 747 TFLOP/s for the
+ * attention over rebuilt keys.  At H = 128 it switches near T_q = 80.  Needs
+ * no device.
+ */
+int mla_prefill_use_rebuild(int T_q, int L, int H, int d_c, int d_r, int d_h, int dtype);
+
+/*
  * mla_prefill_kv -- rebuild k_nope[b, h, s] = W^UK_h c_s, v[b, h, s] =
  * W^UV_h c_s and copy k_rope[b, s] = R_s k^R_s (the cached rotary key) for
  * every cached row s < seqlens[b] of every sequence, reading the paged cache

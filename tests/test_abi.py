@@ -206,3 +206,21 @@ def test_prefill_rows_and_host_checks():
     for unsup in (dict(dt=0), dict(d_h=64), dict(d_r=16)):
         assert call_at(**unsup) == mla.MLA_ERR_UNSUPPORTED, unsup
     assert call_at(B=0) == mla.MLA_OK
+
+
+def test_prefill_path_choice():
+    use = mla.mla_prefill_use_rebuild
+    # a single new token, or a handful, stay on the absorbed decode; a prompt goes to the rebuild
+    assert use(1, 4096, 128) == 0 and use(16, 4096, 128) == 0 and use(64, 131072, 128) == 0
+    assert use(4096, 4096, 128) == 1 and use(512, 32768, 128) == 1
+    # at 128 heads the switch sits near 80 new tokens whatever the length
+    for L in (4096, 32768, 131072):
+        flips = [T for T in range(1, 200) if use(T, L, 128) == 1]
+        assert flips and 70 <= flips[0] <= 100, (L, flips[:3])
+        assert all(use(T, L, 128) == 1 for T in range(flips[0], 200))
+    # fewer heads form fewer 128-row groups, so the absorbed decode stays longer
+    assert use(64, 4096, 16) == 0 and use(1024, 4096, 16) == 1
+    # shapes the rebuild kernels do not take, and invalid input
+    assert use(4096, 4096, 128, d_h=64) == 0
+    assert use(4096, 4096, 128, dtype=torch.float32) == 0
+    assert use(0, 10, 8) == -1 and use(5, 4, 8) == -1 and use(1, 10, 0) == -1
