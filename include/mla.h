@@ -13,11 +13,17 @@
  *     (absorbed inference path), "Why position needs its own key".
  *   - "How DeepSeek Rewrote the Transformer" (zhichai.net), "Absorbed
  *     projections" (the value is the first d_c numbers of the key row).
+ * For prompts and long chunks it also rebuilds the per-head keys and values
+ * from the cached latent ("The MLA equations") and attends over them
+ * (mla_prefill_kv, mla_prefill_attention): the same result, fewer flops
+ * once a chunk has more than a few dozen tokens.
  *
  * Conventions shared by every call:
  *   - Every array pointer is a DEVICE pointer (cudaMalloc'd or torch
  *     memory) owned by the caller, row-major and contiguous, 16-byte
- *     aligned.  The library allocates no device memory.
+ *     aligned.  The library allocates no device memory at run time (the
+ *     scratch of mla_decode_paged_noalloc is a static array of the library
+ *     image).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Every call only enqueues work on it and returns; results are
  *     ready when the stream reaches that point.
