@@ -105,3 +105,27 @@ def test_prefill_special_cases():
     o2, l2 = orc.prefill_attention(q_n[:1], q_r[:1], pos[:1], k2, v2, kr2, 0.7, 10000.0)
     np.testing.assert_array_equal(o2[0], o1[0])
     np.testing.assert_array_equal(l2[0], l1[0])
+
+
+def test_prefill_inputs_are_seeded_and_laid_out():
+    import mla_inputs as mi
+    spec = mi.PrefillSpec("layout", seed=21, B=3, H=2, T_q=5, seqlens=(5, 70, 129), d_h=16,
+                          d_c=32, d_r=8)
+    a = mi.make_prefill_inputs(spec, with_kv=True)
+    b = mi.make_prefill_inputs(spec, with_kv=True)
+    for x, y in ((a.q_nope_bits, b.q_nope_bits), (a.w_uv_bits, b.w_uv_bits),
+                 (a.k_nope_bits, b.k_nope_bits), (a.cache.pool_bits, b.cache.pool_bits)):
+        assert np.array_equal(x, y)                       # same seed, same bits
+    R = mi.prefill_kv_rows(a.cache.max_blocks)
+    assert R % 128 == 0 and R >= 64 * a.cache.max_blocks
+    assert a.q_nope_bits.shape == (3, 5, 2, 16) and a.q_rope_bits.shape == (3, 5, 2, 8)
+    assert a.w_uk_bits.shape == (2 * 16, 32)
+    assert a.k_nope_bits.shape == (3, 2, R, 16) and a.k_rope_bits.shape == (3, R, 8)
+    for bi, L in enumerate(spec.seqlens):
+        assert not np.any(a.k_nope_bits[bi, :, L:]) and not np.any(a.v_bits[bi, :, L:])
+        assert not np.any(a.k_rope_bits[bi, L:]) and np.any(a.k_nope_bits[bi, :, :L])
+        # the paged pool holds exactly the logical rows of each sequence
+        rows = a.cache.seq_rows(bi)
+        for s in (0, L - 1):
+            blk = a.cache.block_table[bi, s // 64]
+            assert np.array_equal(a.cache.pool_bits[blk, s % 64], rows[s])
