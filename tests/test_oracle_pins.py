@@ -337,3 +337,39 @@ def test_absorb_output_against_explicit_values():
     o = np.stack([p[hh] @ vals[hh] for hh in range(H)]).reshape(1, -1)
     np.testing.assert_allclose(orc.absorb_output(o_lat, W_uv, W_o), o @ W_o.T,
                                rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# bfloat16 decoding: fixed bit patterns from the format's definition (1 sign,
+# 8 exponent bits with bias 127, 7 fraction bits), and torch's own decoding
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits,value", [
+    (0x3F80, 1.0),                 # exponent 127, fraction 0
+    (0xC000, -2.0),                # sign, exponent 128
+    (0x3FC0, 1.5),                 # fraction 0b1000000 = 1/2
+    (0x4049, 3.140625),            # 2 * (1 + 73/128)
+    (0x0001, 2.0 ** -133),         # smallest subnormal: 2^-126 * 2^-7
+    (0x0080, 2.0 ** -126),         # smallest normal
+    (0x7F7F, (2 - 2 ** -7) * 2.0 ** 127),   # largest finite
+    (0x8000, -0.0),
+    (0x7F80, math.inf),
+    (0xFF80, -math.inf),
+])
+def test_bf16_to_f64_fixed_patterns(bits, value):
+    got = orc.bf16_to_f64(np.array([bits], dtype=np.uint16))
+    assert got.dtype == np.float64
+    assert got[0] == value
+    assert math.copysign(1.0, got[0]) == math.copysign(1.0, value)
+
+
+def test_bf16_to_f64_nan_and_random_bits_match_torch():
+    assert np.isnan(orc.bf16_to_f64(np.array([0x7FC0, 0xFFC1], dtype=np.uint16))).all()
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 1 << 16, size=50000, dtype=np.uint16)
+    got = orc.bf16_to_f64(bits)
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    finite = np.isfinite(want)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    assert np.array_equal(got[finite], want[finite])
+    assert np.array_equal(got[~finite & ~np.isnan(want)], want[~finite & ~np.isnan(want)])
