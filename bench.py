@@ -338,78 +338,180 @@ def workload_config(spec, l2_note):
 # the GPU arm
 # --------------------------------------------------------------------------
 
+def device_time_ms(fn, K, stream, dev):
+    """Mean device time of K back-to-back calls of fn(i), from one pair of
+    CUDA events on the launching stream.  A sleep kernel queued first lets
+    the host enqueue ahead, so host call overhead stays outside the window."""
+    import torch
+    torch.cuda.synchronize(dev)
+    torch.cuda._sleep(4_000_000)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / K
+
+
+def host_enqueue_us(fn, K, dev):
+    """Host-clock time of one call (argument checks, marshalling, launches),
+    with the device busy so that no call waits for it."""
+    import torch
+    torch.cuda.synchronize(dev)
+    torch.cuda._sleep(20_000_000)
+    t0 = time.perf_counter()
+    for i in range(K):
+        fn(i)
+    dt = time.perf_counter() - t0
+    torch.cuda.synchronize(dev)
+    return 1e6 * dt / K
+
+
+class DecodeBench:
+    """One decode workload resident on the device: the cache (with enough
+    copies to exceed L2, rotated between steps), queries, block table,
+    lengths, workspace and outputs."""
+
+    def __init__(self, spec, dev, rank=0):
+        import torch
+        import head_latent_attention_28_b300 as mla
+        self.mla, self.dev = mla, dev
+        self.spec = mi.DecodeSpec(**{**spec.__dict__, "seed": spec.seed + rank})
+        self.inp = mi.make_decode_inputs(self.spec)
+        self.work = algorithmic_work(self.spec, self.inp.seqlens)
+
+        def up(bits):
+            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+        self.q = up(self.inp.q_bits)
+        pool0 = up(self.inp.pool_bits)
+        self.n_copies = max(2, math.ceil(3 * L2_BYTES / (pool0.numel() * 2)))
+        self.pools = [pool0] + [pool0.clone() for _ in range(self.n_copies - 1)]
+        self.pool_mb = self.n_copies * pool0.numel() * 2 / 1e6
+        self.bt = torch.from_numpy(self.inp.block_table).to(dev)
+        self.sl = torch.from_numpy(self.inp.seqlens).to(dev)
+        B, T_q, H, D = self.q.shape
+        s = self.spec
+        self.ws = mla.alloc_workspace(B, T_q, H, s.d_c, s.d_r, torch.bfloat16, dev)
+        self.o = torch.empty((B, T_q, H, s.d_c), device=dev, dtype=torch.float32)
+        self.lse = torch.empty((B, T_q, H), device=dev, dtype=torch.float32)
+        self.stream = torch.cuda.current_stream(dev)
+        self.kw = dict(d_c=s.d_c, softmax_scale=s.softmax_scale, causal=s.causal,
+                       workspace=self.ws, o_lat=self.o, lse=self.lse, stream=self.stream)
+        self.tc = mla.lib().mla_decode_path(T_q, H, s.d_c, s.d_r, mla.MLA_BF16) == 1
+        self.kernel_file = "decode_tc.cu" if self.tc else "decode_generic.cu"
+        self.workers = mla.lib().mla_decode_num_workers(B, T_q, H, s.d_c, s.d_r, mla.MLA_BF16)
+
+    def step(self, i, stage="both"):
+        self.mla.mla_decode_paged(self.q, self.pools[i % self.n_copies], self.bt, self.sl,
+                                  stage=stage, **self.kw)
+
+    def check(self, what):
+        st = self.mla.mla_check_status(self.stream)
+        if st != self.mla.MLA_OK:
+            raise SystemExit(f"{self.spec.name}: {what}: {self.mla.mla_status_string(st)}")
+
+    def kernel_times(self, K):
+        """(decode kernel ms, merge kernel ms, host enqueue us per call), each
+        from back-to-back launches of that kernel alone."""
+        main_ms = device_time_ms(lambda i: self.step(i, "partial"), K, self.stream, self.dev)
+        comb_ms = device_time_ms(lambda i: self.step(i, "combine"), K, self.stream, self.dev)
+        host_us = host_enqueue_us(self.step, min(K, 200), self.dev)
+        self.check("kernel timing")
+        return main_ms, comb_ms, host_us
+
+    def roofline(self, step_ms, main_ms, comb_ms, peaks, peak_src):
+        w = self.work
+        t_mem = w["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        t_tc = w["flops"] / (peaks["bf16_tflops"] * 1e12)
+        hbm = t_mem >= t_tc
+        achieved = (w["bytes"] / (main_ms / 1e3) / 1e9) if hbm else (w["flops"] / (main_ms / 1e3) / 1e12)
+        peak = peaks["hbm_gbs"] if hbm else peaks["bf16_tflops"]
+        return {"bound": "hbm" if hbm else "tensor", "achieved": achieved, "peak": peak,
+                "unit": "GB/s" if hbm else "TFLOP/s", "frac": achieved / peak,
+                "traffic": profiled_traffic(self.kernel_file, self.spec.name),
+                "kernel": self.kernel_file, "kernel_ms": main_ms, "combine_ms": comb_ms,
+                "split_workers": self.workers,
+                "peak_source": peak_src + " (burst; kernel timed alone)",
+                "achieved_tflops": w["flops"] / (main_ms / 1e3) / 1e12,
+                "tensor_peak_tflops": peaks["bf16_tflops"],
+                "roofline_us": 1e6 * max(t_mem, t_tc),
+                "step_frac_of_roofline": max(t_mem, t_tc) / (step_ms / 1e3),
+                "kernel_time": "one event pair around back-to-back launches of the kernel alone, "
+                               "divided by their number"}
+
+
+def decode_subrecord(spec, dev, args, peaks, peak_src):
+    """Step, kernel, roofline and oracle figures of one more decode workload
+    (rank 0, one GPU)."""
+    db = DecodeBench(spec, dev)
+    K = max(args.steps, 20)
+    for i in range(args.warmup):
+        db.step(i)
+    db.check("warm-up")
+    step_ms = device_time_ms(db.step, K, db.stream, dev)
+    db.check("timed steps")
+    main_ms, comb_ms, host_us = db.kernel_times(K)
+    rf = db.roofline(step_ms, main_ms, comb_ms, peaks, peak_src)
+    w = db.work
+    rec = {"step_us": 1e3 * step_ms, "kernel_us": 1e3 * main_ms, "combine_us": 1e3 * comb_ms,
+           "host_enqueue_us": host_us, "steps": K,
+           "value": w["bytes"] / (step_ms / 1e3) / 1e9, "unit": "GB/s",
+           "tflops": w["flops"] / (step_ms / 1e3) / 1e12,
+           "tokens_per_s": spec.B * spec.T_q / (step_ms / 1e3),
+           "roofline": rf, "config": workload_config(db.spec, f"{db.n_copies} cache copies "
+                                                             f"({db.pool_mb:.0f} MB) rotated")}
+    if main_ms > step_ms * 1.001:
+        raise SystemExit(f"{spec.name}: kernel time {main_ms} ms exceeds the step time {step_ms} ms")
+    if not args.no_cpu_baseline:
+        rec["cpu_baseline"] = cpu_baseline(db.inp, args.cpu_budget / 2)
+    del db
+    import torch
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_mla(args, spec):
     import torch
     rank, world, local, dist = dist_setup(args.gpus)
     torch.cuda.set_device(local)
     import head_latent_attention_28_b300 as mla
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
     dev = torch.device("cuda", local)
 
     # rank r draws its own batch (same shapes, seed + r)
-    rspec = mi.DecodeSpec(**{**spec.__dict__, "seed": spec.seed + rank})
-    inp = mi.make_decode_inputs(rspec)
-    work = algorithmic_work(rspec, inp.seqlens)
-
-    def up(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
-    q = up(inp.q_bits)
-    pool0 = up(inp.pool_bits)
-    n_copies = max(3, math.ceil(3 * L2_BYTES / pool0.numel() / 2))
-    pools = [pool0] + [pool0.clone() for _ in range(n_copies - 1)]
-    bt = torch.from_numpy(inp.block_table).to(dev)
-    sl = torch.from_numpy(inp.seqlens).to(dev)
-    B, T_q, H, D = q.shape
-    ws = mla.alloc_workspace(B, T_q, H, spec.d_c, spec.d_r, torch.bfloat16, dev)
-    o = torch.empty((B, T_q, H, spec.d_c), device=dev, dtype=torch.float32)
-    lse = torch.empty((B, T_q, H), device=dev, dtype=torch.float32)
-    stream = torch.cuda.current_stream(dev)
-    kw = dict(d_c=spec.d_c, softmax_scale=spec.softmax_scale, causal=spec.causal,
-              workspace=ws, o_lat=o, lse=lse, stream=stream)
-
-    def step(i, stage="both"):
-        mla.mla_decode_paged(q, pools[i % n_copies], bt, sl, stage=stage, **kw)
-
+    db = DecodeBench(spec, dev, rank)
+    work, stream = db.work, db.stream
     for i in range(args.warmup):
-        step(i)
-    st = mla.mla_check_status(stream)
-    if st != mla.MLA_OK:
-        raise SystemExit(f"decode failed: {mla.mla_status_string(st)}")
+        db.step(i)
+    db.check("warm-up")
 
-    # ---- timed region: K whole steps
+    # ---- timed region: K whole steps, back to back on one stream
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     barrier(dist, local)
     torch.cuda.synchronize(dev)
     with sampler:
+        torch.cuda._sleep(4_000_000)   # the host enqueues ahead; the window starts at ev0
         sampler.mark("start")
         ev0.record(stream)
         for i in range(args.steps):
-            step(i)
+            db.step(i)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         sampler.mark("end")
     barrier(dist, local)
     ms = ev0.elapsed_time(ev1)
     ms_max = max_over_ranks(dist, ms)
-    if mla.mla_check_status(stream) != mla.MLA_OK:
-        raise SystemExit("decode reported a device error in the timed region")
+    db.check("timed region")
 
-    # ---- per-kernel durations (same stream, events around each launch)
-    K2 = max(args.steps, 20)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K2)]
-    torch.cuda.synchronize(dev)
-    for i in range(K2):
-        evs[i][0].record(stream)
-        step(i, "partial")
-        evs[i][1].record(stream)
-        step(i, "combine")
-        evs[i][2].record(stream)
-    torch.cuda.synchronize(dev)
-    main_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    comb_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    # ---- the dominant kernel and the merge, each timed alone
+    main_ms, comb_ms, host_us = db.kernel_times(max(args.steps, 20))
+    step_ms = ms / args.steps
+    if main_ms > step_ms * 1.001:
+        raise SystemExit(f"kernel time {main_ms:.4f} ms exceeds the step time {step_ms:.4f} ms")
 
     # ---- end to end through the public API with pinned host buffers
+    q, bt, sl, o, lse = db.q, db.bt, db.sl, db.o, db.lse
     q_h = q.cpu().pin_memory()
     bt_h = bt.cpu().pin_memory()
     sl_h = sl.cpu().pin_memory()
@@ -423,9 +525,9 @@ def run_mla(args, spec):
         q_d.copy_(q_h, non_blocking=True)
         bt_d.copy_(bt_h, non_blocking=True)
         sl_d.copy_(sl_h, non_blocking=True)
-        mla.mla_decode_paged(q_d, pools[i % n_copies], bt_d, sl_d, d_c=spec.d_c,
+        mla.mla_decode_paged(q_d, db.pools[i % db.n_copies], bt_d, sl_d, d_c=spec.d_c,
                              softmax_scale=spec.softmax_scale, causal=spec.causal,
-                             workspace=ws, o_lat=o, lse=lse, stream=stream)
+                             workspace=db.ws, o_lat=o, lse=lse, stream=stream)
         o_h.copy_(o, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
 
@@ -440,6 +542,7 @@ def run_mla(args, spec):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1))
+    db.check("end-to-end steps")
 
     if rank != 0:
         if dist is not None:
@@ -447,38 +550,20 @@ def run_mla(args, spec):
         return 0
 
     peaks, peak_src = load_peaks()
-    per_step_s = ms_max / 1e3 / args.steps
     total_bytes = work["bytes"] * world * args.steps
     value = total_bytes / (ms_max / 1e3) / 1e9
     tflops = work["flops"] * world * args.steps / (ms_max / 1e3) / 1e12
-    t_mem = work["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_tc = work["flops"] / (peaks["bf16_tflops"] * 1e12)
-    tc = mla.lib().mla_decode_path(T_q, H, spec.d_c, spec.d_r, mla.MLA_BF16) == 1
-    kernel_file = "decode_tc.cu" if tc else "decode_generic.cu"
-    achieved_gbs = work["bytes"] / (main_ms / 1e3) / 1e9
-    workers = mla.lib().mla_decode_num_workers(B, T_q, H, spec.d_c, spec.d_r, mla.MLA_BF16)
-    roofline = {"bound": "hbm" if t_mem >= t_tc else "tensor",
-                "achieved": achieved_gbs if t_mem >= t_tc else work["flops"] / (main_ms / 1e3) / 1e12,
-                "peak": peaks["hbm_gbs"] if t_mem >= t_tc else peaks["bf16_tflops"],
-                "unit": "GB/s" if t_mem >= t_tc else "TFLOP/s",
-                "traffic": profiled_traffic(kernel_file, spec.name),
-                "kernel": kernel_file, "kernel_ms": main_ms, "combine_ms": comb_ms,
-                "split_workers": workers,
-                "peak_source": peak_src + " (burst; kernel timed alone)",
-                "achieved_tflops": work["flops"] / (main_ms / 1e3) / 1e12,
-                "tensor_peak_tflops": peaks["bf16_tflops"],
-                "step_roofline_us": 1e6 * max(t_mem, t_tc),
-                "step_frac_of_roofline": max(t_mem, t_tc) / per_step_s}
-    roofline["frac"] = roofline["achieved"] / roofline["peak"]
+    roofline = db.roofline(ms_max / args.steps, main_ms, comb_ms, peaks, peak_src)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded normal draws, shuffled block table)",
-        "config": workload_config(spec, f"inputs larger than L2: {n_copies} cache copies "
-                                        f"({n_copies * pool0.numel() * 2 / 1e6:.0f} MB) rotated"),
+        "config": workload_config(db.spec, f"inputs larger than L2: {db.n_copies} cache copies "
+                                           f"({db.pool_mb:.0f} MB) rotated"),
         "tflops": tflops, "tokens_per_s": spec.B * spec.T_q * world * args.steps / (ms_max / 1e3),
         "roofline": roofline,
+        "host_enqueue_us": host_us,
         "e2e": {"value": total_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / args.steps,
@@ -488,7 +573,18 @@ def run_mla(args, spec):
         "clocks": sampler.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(db.inp, args.cpu_budget)
+    del db, q_d, bt_d, sl_d
+    torch.cuda.empty_cache()
+    if world == 1 and not args.no_extra:
+        # the other workloads of the scope table, from the same run
+        extra = {}
+        for name in sorted(mi.DECODE_WORKLOADS):
+            if name != spec.name:
+                extra[name] = decode_subrecord(mi.DECODE_WORKLOADS[name], dev, args, peaks, peak_src)
+        for name, pspec in sorted(mi.PREFILL_WORKLOADS.items()):
+            extra[name] = prefill_subrecord(pspec, dev, args, peaks, peak_src)
+        line["configs"] = extra
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -577,84 +673,137 @@ def run_prefill_reference(args, spec):
     return 0
 
 
+class PrefillBench:
+    """One prefill workload resident on the device: cache, queries, weights,
+    rebuilt K/V buffers and outputs."""
+
+    def __init__(self, spec, dev, rank=0):
+        import torch
+        import head_latent_attention_28_b300 as mla
+        self.mla, self.dev = mla, dev
+        self.spec = mi.PrefillSpec(**{**spec.__dict__, "seed": spec.seed + rank})
+        self.inp = inp = mi.make_prefill_inputs(self.spec)
+        self.work = prefill_work(self.spec, inp.cache.seqlens)
+
+        def up(bits):
+            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+        self.pool, self.qn, self.qr = up(inp.cache.pool_bits), up(inp.q_nope_bits), up(inp.q_rope_bits)
+        self.wuk, self.wuv = up(inp.w_uk_bits), up(inp.w_uv_bits)
+        self.bt = torch.from_numpy(inp.cache.block_table).to(dev)
+        self.sl = torch.from_numpy(inp.cache.seqlens).to(dev)
+        self.mb = inp.cache.max_blocks
+        R = mla.mla_prefill_kv_rows(self.mb)
+        B, T_q, H, d_h = self.qn.shape
+        self.H = H
+        self.kv = (torch.empty((B, H, R, d_h), device=dev, dtype=torch.bfloat16),
+                   torch.empty((B, H, R, d_h), device=dev, dtype=torch.bfloat16),
+                   torch.empty((B, R, spec.d_r), device=dev, dtype=torch.bfloat16))
+        self.o = torch.empty((B, T_q, H, d_h), device=dev, dtype=torch.float32)
+        self.lse = torch.empty((B, T_q, H), device=dev, dtype=torch.float32)
+        self.stream = torch.cuda.current_stream(dev)
+
+    def rebuild(self, i=0, sl=None):
+        self.mla.mla_prefill_kv(self.pool, self.bt, self.sl if sl is None else sl, self.wuk, self.wuv,
+                                H=self.H, out=self.kv, stream=self.stream)
+
+    def attend(self, i=0, q_nope=None, q_rope=None, sl=None):
+        s = self.spec
+        self.mla.mla_prefill_attention(self.qn if q_nope is None else q_nope,
+                                       self.qr if q_rope is None else q_rope, *self.kv,
+                                       self.sl if sl is None else sl, max_blocks_per_seq=self.mb,
+                                       softmax_scale=s.softmax_scale, rope_base=s.rope_base,
+                                       o=self.o, lse=self.lse, stream=self.stream)
+
+    def step(self, i=0):
+        self.rebuild()
+        self.attend()
+
+    def check(self, what):
+        if self.mla.mla_check_status(self.stream) != self.mla.MLA_OK:
+            raise SystemExit(f"prefill: {what}: device error")
+
+    def kernel_times(self, K):
+        kv_ms = device_time_ms(self.rebuild, K, self.stream, self.dev)
+        at_ms = device_time_ms(self.attend, K, self.stream, self.dev)
+        self.check("kernel timing")
+        return kv_ms, at_ms
+
+    def roofline(self, at_ms, kv_ms, step_ms, peaks, peak_src):
+        w = self.work
+        at_tflops = w["attn_flops"] / (at_ms / 1e3) / 1e12
+        return {"bound": "tensor", "achieved": at_tflops, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": at_tflops / peaks["bf16_tflops"],
+                "traffic": profiled_traffic("prefill_tc.cu", self.spec.name),
+                "kernel": "prefill_tc.cu (prefill_attn_kernel)", "kernel_ms": at_ms,
+                "rebuild_ms": kv_ms,
+                "rebuild_tflops": w["rebuild_flops"] / (kv_ms / 1e3) / 1e12,
+                "peak_source": peak_src + " (burst; kernel timed alone)",
+                "step_frac_of_peak": w["flops"] / (step_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                "kernel_time": "one event pair around back-to-back launches of the kernel alone, "
+                               "divided by their number"}
+
+
+def prefill_subrecord(spec, dev, args, peaks, peak_src):
+    pb = PrefillBench(spec, dev)
+    K = max(min(args.steps, 50), 10)
+    for _ in range(args.warmup):
+        pb.step()
+    pb.check("warm-up")
+    step_ms = device_time_ms(pb.step, K, pb.stream, dev)
+    kv_ms, at_ms = pb.kernel_times(K)
+    w = pb.work
+    rec = {"step_us": 1e3 * step_ms, "attention_kernel_us": 1e3 * at_ms, "rebuild_kernel_us": 1e3 * kv_ms,
+           "steps": K, "value": w["flops"] / (step_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+           "tokens_per_s": spec.B * spec.T_q / (step_ms / 1e3),
+           "roofline": pb.roofline(at_ms, kv_ms, step_ms, peaks, peak_src),
+           "config": prefill_config(pb.spec, "the rebuilt K/V of each step exceed L2")}
+    if not args.no_cpu_baseline:
+        sec, fl, nq = prefill_cpu_sample(pb.inp, args.cpu_budget / 2)
+        rec["cpu_baseline"] = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
+                               "kind": "oracle",
+                               "sample": f"fp64 numpy: the rebuild of all rows and the attention "
+                                         f"of {nq} random query tokens, {sec:.1f} s"}
+    del pb
+    import torch
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_prefill(args, spec):
     import torch
     rank, world, local, dist = dist_setup(args.gpus)
     torch.cuda.set_device(local)
-    import head_latent_attention_28_b300 as mla
     dev = torch.device("cuda", local)
-    rspec = mi.PrefillSpec(**{**spec.__dict__, "seed": spec.seed + rank})
-    inp = mi.make_prefill_inputs(rspec)
-    work = prefill_work(rspec, inp.cache.seqlens)
-
-    def up(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
-    pool, qn, qr = up(inp.cache.pool_bits), up(inp.q_nope_bits), up(inp.q_rope_bits)
-    wuk, wuv = up(inp.w_uk_bits), up(inp.w_uv_bits)
-    bt = torch.from_numpy(inp.cache.block_table).to(dev)
-    sl = torch.from_numpy(inp.cache.seqlens).to(dev)
-    mb = inp.cache.max_blocks
-    R = mla.mla_prefill_kv_rows(mb)
-    B, T_q, H, d_h = qn.shape
-    kv = (torch.empty((B, H, R, d_h), device=dev, dtype=torch.bfloat16),
-          torch.empty((B, H, R, d_h), device=dev, dtype=torch.bfloat16),
-          torch.empty((B, R, spec.d_r), device=dev, dtype=torch.bfloat16))
-    o = torch.empty((B, T_q, H, d_h), device=dev, dtype=torch.float32)
-    lse = torch.empty((B, T_q, H), device=dev, dtype=torch.float32)
-    stream = torch.cuda.current_stream(dev)
-
-    def rebuild():
-        mla.mla_prefill_kv(pool, bt, sl, wuk, wuv, H=H, out=kv, stream=stream)
-
-    def attend(q_nope=qn, q_rope=qr):
-        mla.mla_prefill_attention(q_nope, q_rope, *kv, sl, max_blocks_per_seq=mb,
-                                  softmax_scale=spec.softmax_scale, rope_base=spec.rope_base,
-                                  o=o, lse=lse, stream=stream)
-
+    pb = PrefillBench(spec, dev, rank)
+    work, stream = pb.work, pb.stream
     for _ in range(args.warmup):
-        rebuild()
-        attend()
-    if mla.mla_check_status(stream) != mla.MLA_OK:
-        raise SystemExit("prefill failed")
+        pb.step()
+    pb.check("warm-up")
 
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     barrier(dist, local)
     torch.cuda.synchronize(dev)
     with sampler:
+        torch.cuda._sleep(4_000_000)
         sampler.mark("start")
         ev0.record(stream)
         for _ in range(args.steps):
-            rebuild()
-            attend()
+            pb.step()
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         sampler.mark("end")
     barrier(dist, local)
     ms_max = max_over_ranks(dist, ev0.elapsed_time(ev1))
-    if mla.mla_check_status(stream) != mla.MLA_OK:
-        raise SystemExit("prefill reported a device error in the timed region")
-
-    # per-kernel durations on the launching stream
-    K2 = max(args.steps, 10)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K2)]
-    torch.cuda.synchronize(dev)
-    for i in range(K2):
-        evs[i][0].record(stream)
-        rebuild()
-        evs[i][1].record(stream)
-        attend()
-        evs[i][2].record(stream)
-    torch.cuda.synchronize(dev)
-    kv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    at_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    pb.check("timed region")
+    kv_ms, at_ms = pb.kernel_times(max(args.steps, 10))
 
     # end to end: the prompt's queries in from pinned host memory, o and lse back
-    qn_h, qr_h = qn.cpu().pin_memory(), qr.cpu().pin_memory()
-    sl_h = sl.cpu().pin_memory()
-    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    qn_d, qr_d, sl_d = torch.empty_like(qn), torch.empty_like(qr), torch.empty_like(sl)
+    qn_h, qr_h = pb.qn.cpu().pin_memory(), pb.qr.cpu().pin_memory()
+    sl_h = pb.sl.cpu().pin_memory()
+    o_h = torch.empty(pb.o.shape, dtype=pb.o.dtype).pin_memory()
+    lse_h = torch.empty(pb.lse.shape, dtype=pb.lse.dtype).pin_memory()
+    qn_d, qr_d, sl_d = torch.empty_like(pb.qn), torch.empty_like(pb.qr), torch.empty_like(pb.sl)
     h2d = (qn_h.numel() + qr_h.numel()) * 2 + sl_h.numel() * 4
     d2h = (o_h.numel() + lse_h.numel()) * 4
 
@@ -662,12 +811,10 @@ def run_prefill(args, spec):
         qn_d.copy_(qn_h, non_blocking=True)
         qr_d.copy_(qr_h, non_blocking=True)
         sl_d.copy_(sl_h, non_blocking=True)
-        mla.mla_prefill_kv(pool, bt, sl_d, wuk, wuv, H=H, out=kv, stream=stream)
-        mla.mla_prefill_attention(qn_d, qr_d, *kv, sl_d, max_blocks_per_seq=mb,
-                                  softmax_scale=spec.softmax_scale, rope_base=spec.rope_base,
-                                  o=o, lse=lse, stream=stream)
-        o_h.copy_(o, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        pb.rebuild(sl=sl_d)
+        pb.attend(q_nope=qn_d, q_rope=qr_d, sl=sl_d)
+        o_h.copy_(pb.o, non_blocking=True)
+        lse_h.copy_(pb.lse, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -688,24 +835,15 @@ def run_prefill(args, spec):
     peaks, peak_src = load_peaks()
     total_flops = work["flops"] * world * args.steps
     value = total_flops / (ms_max / 1e3) / 1e12
-    at_tflops = work["attn_flops"] / (at_ms / 1e3) / 1e12
-    roofline = {"bound": "tensor", "achieved": at_tflops, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": at_tflops / peaks["bf16_tflops"],
-                "traffic": profiled_traffic("prefill_tc.cu", spec.name),
-                "kernel": "prefill_tc.cu (prefill_attn_kernel)", "kernel_ms": at_ms,
-                "rebuild_ms": kv_ms,
-                "rebuild_tflops": work["rebuild_flops"] / (kv_ms / 1e3) / 1e12,
-                "peak_source": peak_src + " (burst; kernel timed alone)",
-                "step_frac_of_peak": value / world / peaks["bf16_tflops"]}
     line = {
         "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded normal draws, shuffled block table)",
-        "config": prefill_config(spec, "the rebuilt K/V of each step (%d MB) exceed L2" %
-                                 (sum(x.numel() for x in kv) * 2 // 10**6)),
+        "config": prefill_config(pb.spec, "the rebuilt K/V of each step (%d MB) exceed L2" %
+                                 (sum(x.numel() for x in pb.kv) * 2 // 10**6)),
         "tokens_per_s": spec.B * spec.T_q * world * args.steps / (ms_max / 1e3),
-        "roofline": roofline,
+        "roofline": pb.roofline(at_ms, kv_ms, ms_max / args.steps, peaks, peak_src),
         "e2e": {"value": total_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / args.steps,
@@ -715,7 +853,7 @@ def run_prefill(args, spec):
         "clocks": sampler.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
-        sec, fl, nq = prefill_cpu_sample(inp, args.cpu_budget)
+        sec, fl, nq = prefill_cpu_sample(pb.inp, args.cpu_budget)
         line["cpu_baseline"] = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
                                 "kind": "oracle",
                                 "sample": f"fp64 numpy: the rebuild of all rows and the attention "
@@ -729,13 +867,15 @@ def run_prefill(args, spec):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["mla", "reference"], default="mla")
-    ap.add_argument("--workload", default=mi.V2_DECODE.name,
+    ap.add_argument("--workload", default=mi.RAGGED_SERVING.name,
                     choices=sorted(mi.DECODE_WORKLOADS) + sorted(mi.PREFILL_WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the per-workload sub-records of the other configurations")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

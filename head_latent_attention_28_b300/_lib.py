@@ -23,6 +23,7 @@ MLA_ERR_CUDA = 3
 MLA_ERR_WORKSPACE = 4
 MLA_ERR_TIMEOUT = 5
 MLA_ERR_BAD_INDEX = 6
+MLA_ERR_BAD_RECORD = 7
 MLA_F32 = 0
 MLA_BF16 = 1
 PAGE_SIZE = 64
@@ -45,6 +46,7 @@ SIGNATURES = {
     "mla_status_string": (ctypes.c_char_p, [_I]),
     "mla_last_cuda_error": (ctypes.c_char_p, []),
     "mla_check_status": (_I, [_P]),
+    "mla_test_set_wait_fault": (_I, [_I, ctypes.c_uint]),
     "mla_version": (_I, []),
     "mla_decode_split_plan": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "mla_decode_item_cost": (_I, [_I, _I, _I, _I, _I]),
@@ -413,6 +415,13 @@ def mla_prefill_attention(q_nope, q_rope, k_nope, v, k_rope, seqlens, *, max_blo
 def mla_check_status(stream=None) -> int:
     """Wait for the stream and return (and clear) the device error status."""
     return int(lib().mla_check_status(_stream(stream)))
+
+
+def mla_test_set_wait_fault(skip_load: int, wait_us: int = 1000) -> None:
+    """Test hook: make tensor-core decode launches skip the load of page
+    `skip_load` of split worker 0 with bounded waits of `wait_us` (0 turns
+    the hook off); see include/mla.h."""
+    _check(lib().mla_test_set_wait_fault(int(skip_load), int(wait_us)), "mla_test_set_wait_fault")
 
 
 def mla_status_string(status: int) -> str:

@@ -12,6 +12,7 @@ constexpr int kPage = 64;  // tokens per cache block
 // bits of the per-device error word
 constexpr unsigned kErrBadIndex = 1u;  // block id or sequence length out of range
 constexpr unsigned kErrTimeout = 2u;   // a bounded wait gave up
+constexpr unsigned kErrBadRecord = 4u; // the merge found no consistent split record
 
 enum DType { F32 = 0, BF16 = 1 };
 
@@ -60,21 +61,26 @@ __host__ __device__ inline void part_pages(long long x0, long long x1, long long
   *j1 = (int)(b < 0 ? 0 : b > P ? P : b);
 }
 
-// Workspace layout for rows = T_q*H query rows per sequence.
+// Workspace layout for rows = T_q*H query rows per sequence, W split
+// workers and msg_bytes of message ring per worker (the tensor-core kernel
+// passes each page's probabilities from the score CTA to the value CTA
+// through it; the CUDA-core kernel uses none).
 struct WsLayout {
   size_t meta_off;   // int2 [B]: (first worker, last worker) of each sequence
   size_t lse_off;    // float [(B + W) * rows]
   size_t o_off;      // float [(B + W) * rows * d_c]
+  size_t msg_off;    // W * msg_bytes
   size_t total;
 };
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-inline WsLayout ws_layout(int B, int rows, int d_c, int W) {
+inline WsLayout ws_layout(int B, int rows, int d_c, int W, size_t msg_bytes = 0) {
   WsLayout L;
   size_t slots = (size_t)B + (size_t)W;
   L.meta_off = 0;
   L.lse_off = align_up(sizeof(int) * 2 * (size_t)B, 256);
   L.o_off = align_up(L.lse_off + sizeof(float) * slots * rows, 256);
-  L.total = align_up(L.o_off + sizeof(float) * slots * rows * (size_t)d_c, 256);
+  L.msg_off = align_up(L.o_off + sizeof(float) * slots * rows * (size_t)d_c, 1024);
+  L.total = align_up(L.msg_off + (size_t)W * msg_bytes, 256);
   return L;
 }
 
@@ -94,6 +100,7 @@ struct DecodeArgs {
   int2* meta;
   float* ws_lse;
   float* ws_o;
+  unsigned char* msg;         // per-worker message rings (tensor-core kernel)
   int W;                      // number of split workers
   int item_cost;              // C of the split partition (units per work item)
   // Row groups: the tensor-core kernel handles at most 128 query rows of a
@@ -105,6 +112,12 @@ struct DecodeArgs {
   int G;
   int SR;
   unsigned* err;              // device error word
+  // Test hook (zero in normal calls): when skip_load > 0 the tensor-core
+  // kernel leaves out the shared-memory load of the skip_load-th page of
+  // worker 0, so that the wait for it runs out after wait_ns and the call
+  // reports MLA_ERR_TIMEOUT.
+  int skip_load;
+  unsigned long long wait_ns; // budget of every bounded wait (0: the default)
 };
 
 __device__ __forceinline__ float load_as_float(const float* p, size_t i) { return p[i]; }

@@ -307,8 +307,8 @@ __global__ void __launch_bounds__(CT) combine_kernel(DecodeArgs a) {
   if (m.x == m.y) return;  // finished by its only worker
   if (m.x < 0 || m.y < m.x || m.y >= a.W) {
     // no consistent merge record (the partial pass gave up before writing
-    // it): report and write zeros rather than follow it
-    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(a.err, kErrTimeout);
+    // it, or no partial pass ran): report and write zeros rather than follow it
+    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(a.err, kErrBadRecord);
     V z;
     zero_vec(z);
     for (int idx = threadIdx.x; idx < nr * dc4; idx += CT) {

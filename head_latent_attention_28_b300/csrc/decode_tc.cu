@@ -10,39 +10,51 @@
 // softmax, value sum over the latents; "How DeepSeek Rewrote the Transformer":
 // the value is the first d_c numbers of the cached row).
 //
-// How (B300-specific).  One split worker is a cluster of two CTAs on two SMs:
-//  * CTA 0, the score CTA, streams its pages from HBM two at a time through a
-//    ring of six 16 KB cells (cell c of a page pair = the 64-dim box c of
-//    both pages, so one N=128 MMA covers both pages), and computes
-//    S = Q . C^T (M=128 rows, N=128 tokens, K=576) with tcgen05.mma into one of
-//    two TMEM score buffers.  The latent part of the query (K 0..511) is the A
-//    operand in tensor memory, the rotary part (K 512..575) sits in shared
-//    memory.  Eight softmax warps (one page of the pair per half) run a
-//    base-2 online softmax with a lazy running max (the output is rescaled
-//    only when a row max grows by more than 2^8; exact after the final
-//    division) and round the probabilities to bf16.  Each page's probabilities
-//    and per-row rescale factors are staged in shared memory in the layout the
-//    value CTA's MMA reads and moved there with one bulk copy (a contiguous
-//    copy runs at twice the rate of per-row remote stores; its bytes complete
-//    the receiver's barrier).
-//  * CTA 1, the value CTA, keeps the full 128 x 512 fp32 output in tensor
-//    memory (all 512 columns), streams the 512 latent dims of the same pages
-//    in half-page units through a 3-deep ring (the second read of a page is
-//    an L2 hit) and accumulates O += P . V with tcgen05.mma (A = P from shared
-//    memory, B = V MN-major, N = 256 per half).  The probabilities arrive in
-//    a ring of six 18 KB units (one per page, two when the page also sends
-//    the low bf16 parts of its probabilities).  Four warps apply row rescales
-//    and zero the rows of a last page past the sequence end (0 x NaN would
-//    poison O); eight warps write the normalised output with TMA tensor
-//    stores (or the split's partial output, merged later).
+// How (B300-specific).  One split worker is a cluster of two CTAs on two SMs.
+// The output accumulator (128 x 512 fp32) fills a whole SM's tensor memory,
+// and the score side needs the latent query (256 columns) and score buffers
+// in tensor memory, so the two halves of the work sit on different SMs:
+//  * CTA 0, the score CTA, loads each 64-token page with ONE 4-D TMA copy
+//    (72 KB; small boxes cost a fixed ~0.2-0.4 us each on this part, so nine
+//    8 KB boxes per page could not keep up with HBM) into a ring of three
+//    page slots, and keeps a few pages ahead in L2 with bulk prefetches.  The
+//    4-D box lays a page out as [8-token group][64-dim chunk][8 tokens][64
+//    dims] with 128-byte swizzle, so each (group, chunk) is one 1 KB
+//    swizzle atom and an MMA operand over the page's 64 tokens is a uniform
+//    stride of 9 KB.  Scores S = Q . C^T (M = 128 rows, N = 64 tokens,
+//    K = 576) go into one of two tensor-memory buffers; the whole query (512
+//    latent + 64 rotary dims) is the A operand in tensor memory.  Eight
+//    softmax warps (two per 32-row quarter, 32 tokens each) run a base-2
+//    online softmax with a lazy running max (the output is rescaled only
+//    when a row max grows by more than 2^8; exact after the final division)
+//    and round the probabilities to bf16.  Each page's probabilities, per-row
+//    rescale factors and a header are written straight from registers into
+//    this worker's message ring in global memory (L2), in the swizzled layout
+//    the value CTA's MMA reads; a heavy page (a probability not small
+//    against its row's running sum) also sends the low bf16 parts.  The
+//    message's flags go to the value CTA with one remote store and an
+//    mbarrier arrive (release at cluster scope).
+//  * CTA 1, the value CTA, keeps the 128 x 512 fp32 output in tensor memory,
+//    loads the 512 latent dims of the same pages (an L2 hit) as two 32 KB
+//    4-D boxes per page into a ring of four, loads each page's message (one
+//    or two 18 KB units) into a ring of four shared-memory units, and
+//    accumulates O += P . V with tcgen05.mma (A = P from shared memory, B = V
+//    MN-major, N = 256).  Four warps apply row rescales and zero the rows of
+//    a last page past the sequence end (0 x NaN would poison O); eight warps
+//    write the normalised output with TMA tensor stores (or the split's
+//    partial output, merged later).
 //  * Each worker takes a contiguous range of the cost-weighted split
 //    partition (common.cuh): work items are (sequence, row group, page
-//    range), planned on the device in batches of up to 64.
-// The data flow is one-way (score CTA -> value CTA), so the distributed-
-// shared-memory latency is pipelined, never on a round trip.
+//    range), planned on the device in batches of up to 32.
+// Distributed shared memory carries only flags and arrivals (it moves ~30
+// GB/s per SM pair on this part); bulk data moves through L2.
 // Every mbarrier wait is bounded (2 s): on expiry the kernel records
-// MLA_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
+// MLA_ERR_TIMEOUT, drains its copies and MMAs, frees tensor memory and
+// returns.
 #include <cuda.h>
+
+#include <atomic>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -54,35 +66,29 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 320;            // 10 warps
+constexpr int kThreads = 352;            // 11 warps
 constexpr int kRows = 128;               // query rows per work item (one row group)
-constexpr int kBox = 8192;               // 64 tokens x 64 dims x bf16
-constexpr int kCell = 2 * kBox;          // score CTA: box c of both pages of a pair
-constexpr int kCells = 6;                // score CTA: ring depth (cells); measured on B300:
-                                         // 6 is best (8: 1% slower, 4: 3% slower)
-constexpr int kVUnit = 4 * kBox;         // value CTA: 256 latent dims of one page
-constexpr int kVUnits = 3;               // value CTA: ring depth (half pages)
+constexpr int kPageBytes = kPage * 576 * 2;   // 73,728: one page, [tg 8][chunk 9][8][64]
+constexpr int kSlots = 3;                // score CTA: page ring
+constexpr int kVHalf = 32768;            // value CTA: 256 latent dims of a page, [tg 8][chunk 4][8][64]
+constexpr int kVSlots = 4;               // value CTA: ring of half pages
 constexpr int kPBytes = kRows * 64 * 2;  // bf16 probabilities of one page (K-major, SW128)
 constexpr int kInfoBytes = 16 + kRows * 8;       // header + (alpha, l) per row
-constexpr int kPMsgBytes = kPBytes + kInfoBytes; // bytes delivered per page (one bulk copy)
-// Probability messages travel in 18 KB units: a page takes one unit (its bf16
-// probabilities, header and per-row factors) or two (then the second one
-// carries the low bf16 parts).  Both CTAs advance the same unit counter.
-constexpr int kPUnitBytes = 18432;
-constexpr int kPUnits = 6;               // units in the value CTA's ring
-constexpr int kStgPageBytes = 2 * kPUnitBytes;   // score CTA staging per page (hi unit, lo unit)
-// shared-memory map (offsets from the 1 KB aligned base)
-constexpr int kOffQr = 0;                // score CTA: rotary query, 128 x 64 bf16 (K-major SW128)
-constexpr int kOffStg = 16384;           // score CTA: the step's two outgoing page messages
-constexpr int kOffCells = kOffStg + 2 * kStgPageBytes;   // score CTA: the cells
-constexpr int kOffV = 0;                 // value CTA: 3 half-page units
-constexpr int kOffP = kVUnits * kVUnit;  // value CTA: probability slots (score CTA writes them)
-constexpr int kScoreSmem = kOffCells + kCells * kCell;
+constexpr int kPMsgBytes = kPBytes + kInfoBytes; // bytes loaded per unit
+constexpr int kPUnitBytes = 18432;       // a message unit (in global memory and shared memory)
+constexpr int kPUnits = 4;               // value CTA: shared-memory units
+constexpr int kGSlots = 8;               // message ring: page slots per worker (hi and lo unit each)
+constexpr int kPrefetch = 3;             // pages kept ahead in L2
+constexpr int kOffV = 0;
+constexpr int kOffP = kVSlots * kVHalf;
+constexpr int kScoreSmem = kSlots * kPageBytes;
 constexpr int kValueSmem = kOffP + kPUnits * kPUnitBytes;
 constexpr int kSmemBytes = (kScoreSmem > kValueSmem ? kScoreSmem : kValueSmem) + 1024;
-constexpr int kMaxItems = 64;            // work items planned per batch
-// TMEM columns (score CTA): score buffers 2 x 128 at [0, 256), latent query at [256, 512)
-constexpr uint32_t kTmemQ = 256;
+constexpr int kMaxItems = 32;            // work items planned per batch
+// TMEM columns (score CTA): latent query [0, 256), rotary query [256, 288),
+// score buffers [384, 448) and [448, 512)
+constexpr uint32_t kTmemQr = 256;
+constexpr uint32_t kTmemS = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -91,12 +97,18 @@ constexpr uint32_t kFlagRescale = 1u;    // rows rescaled before this page's val
 constexpr uint32_t kFlagLo = 2u;         // the low bf16 parts of the probabilities follow
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-static_assert(kPMsgBytes <= kPUnitBytes, "probability unit too small");
+static_assert(kPMsgBytes <= kPUnitBytes, "message unit too small");
 static_assert(kPMsgBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
-static_assert(kOffCells % 1024 == 0, "SW128 operands need 1 KB alignment");
+static_assert(kPageBytes % 1024 == 0 && kVHalf % 1024 == 0, "SW128 operands need 1 KB alignment");
 static_assert(kOffP % 1024 == 0 && kPUnitBytes % 1024 == 0, "SW128 operands need 1 KB alignment");
-static_assert(8 * 2048 <= kPBytes, "epilogue staging lives in a probability slot");
-static_assert(4 * 4096 <= kPBytes, "four epilogue boxes fit in a unit's probability area");
+static_assert(8 * 2048 <= kPBytes, "epilogue staging lives in a probability unit");
+static_assert(kPrefetch < 32, "the prefetch cursor looks at most one block-id chunk ahead");
+
+}  // namespace
+
+size_t tc_msg_bytes_per_worker() { return (size_t)kGSlots * 2 * kPUnitBytes; }
+
+namespace {
 
 struct Item {
   int b, j0, j1;            // sequence, page range [j0, j1)
@@ -107,31 +119,38 @@ struct Item {
 
 struct SmemCtl {
   // score CTA
-  uint64_t cell_full[kCells], cell_empty[kCells];
+  uint64_t slot_full[kSlots], slot_empty[kSlots];
   uint64_t s_full[2], s_free[2];
-  uint64_t q_ready, pfree[kPUnits];
+  uint64_t q_ready;
+  uint64_t q_free;             // the scores of an item are complete: its query may be overwritten
+  uint64_t gfree[kGSlots];     // a message slot may be rewritten (value CTA arrives)
+  uint64_t written[8];         // the softmax warps wrote page g's message ([g % 8], count 4)
   // value CTA
-  uint64_t v_full[kVUnits], v_empty[kVUnits];
-  uint64_t p_recv[kPUnits];    // a unit's bytes arrived
+  uint64_t v_full[kVSlots], v_empty[kVSlots];
+  uint64_t p_ready[kGSlots];   // the score CTA wrote a page's message (remote arrive)
+  uint64_t p_recv[kPUnits];    // a unit's bytes arrived in shared memory
+  uint64_t unit_free[kPUnits]; // a unit may be reloaded
   uint64_t pv_done[kPUnits];   // value MMAs of the page whose first unit sits here completed
+  uint64_t rows_seen[kPUnits]; // all row warps have read the header and factors in a unit
   uint64_t resc_done, vz_done;
   uint64_t o_free;          // the epilogue has read O: the next item may overwrite it
   uint64_t epi_go;          // O of the item is final (value row warps -> other warps)
-  uint64_t epi_done;        // all epilogue warps are done with the staging slot
-  uint64_t rows_seen[kPUnits];  // all row warps have read the header and factors in a unit
+  uint64_t epi_done;        // all epilogue warps are done with the staging units
   // both
-  uint64_t grp, mma_final;
+  uint64_t mma_final;
+  uint32_t pflag_in[kGSlots];  // value CTA: header flags of a page (remote store by the score CTA)
   uint32_t tmem_base;
   int abort;
   int never;                // stays 0: abort flag for the final drain waits
-  int n_batch, n_total;
+  int n_batch, n_total, n_flat;
   int scan[kThreads / 32];
-  float rowx[2][kRows];     // score CTA: per-half row maxima of a step
-  float rowl[2][kRows];     // score CTA: per-half row sums (last step of an item)
-  // score CTA: header flags of a page, indexed by page mod 2 x slots: a word
-  // is reset by the leader after the step that sent it and written again three
-  // steps later, so the two never race
-  uint32_t pflags[6];
+  int item_flat[kMaxItems + 1];   // first page (in the batch's page order) of each item
+  // score CTA: header flags of page g at [g % 8], gathered with atomicOr; a
+  // word is read and reset by the signaler after the page's `written`
+  // barrier and written again eight pages later
+  uint32_t pflags[8];
+  uint32_t uflags[kPUnits];    // value CTA: header flags of the page loaded into a unit
+  float lrow[kRows];           // value CTA: row sums of an item (row warps -> epilogue warps)
   uint32_t epi_unit;        // value CTA: first unit of the item's last page (for the epilogue)
   Item items[kMaxItems];
 };
@@ -221,11 +240,27 @@ __device__ void plan_batch(const DecodeArgs& a, int w, int offset, SmemCtl* ctl)
     n_total = count;
     n_batch = min(kMaxItems, max(0, count - offset));
   }
+  __syncthreads();
   if (tid == 0) {
     ctl->n_total = n_total;
     ctl->n_batch = n_batch;
+    int f = 0;
+    for (int i = 0; i < n_batch; ++i) {
+      ctl->item_flat[i] = f;
+      f += ctl->items[i].j1 - ctl->items[i].j0;
+    }
+    ctl->item_flat[n_batch] = f;
+    ctl->n_flat = f;
   }
   __syncthreads();
+}
+
+// block id of the batch's f-th page (0 <= f < n_flat)
+__device__ __forceinline__ int block_of(const DecodeArgs& a, const SmemCtl* ctl, int n_items, int f) {
+  int ii = 0;
+  while (ii + 1 < n_items && ctl->item_flat[ii + 1] <= f) ++ii;
+  const Item& it = ctl->items[ii];
+  return __ldg(a.block_table + (size_t)it.b * a.max_blocks + it.j0 + (f - ctl->item_flat[ii]));
 }
 
 __device__ __forceinline__ void fail(SmemCtl* ctl, unsigned* err) {
@@ -234,80 +269,126 @@ __device__ __forceinline__ void fail(SmemCtl* ctl, unsigned* err) {
 }
 
 // every lane of the warp waits; true only if all of them saw the phase complete
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, kWaitNs));
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t budget) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, budget));
 }
 
-// the same, with acquire at cluster scope (bytes or arrivals from the peer CTA)
-__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, abort, kWaitNs));
-}
-
-// barrier among the warps of a role, with a bounded wait (a plain bar.sync
-// could not give up if a warp left after a timeout)
-__device__ __forceinline__ bool group_sync(uint64_t* grp, uint32_t& phase, volatile int* abort) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(grp);
-  const bool done = warp_wait(grp, phase & 1, abort);
-  ++phase;
-  return done;
+// the same, with acquire at cluster scope (arrivals from the peer CTA)
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  uint64_t budget) {
+  return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, abort, budget));
 }
 
 __device__ __forceinline__ uint32_t lo_half_f(uint32_t u) { return u << 16; }
 __device__ __forceinline__ uint32_t hi_half_f(uint32_t u) { return u & 0xffff0000u; }
 
+// The query row r of an item into tensor memory, one half of it: half 0
+// the latent dims [0, 256) and rotary dims [512, 544), half 1 the latent dims
+// [256, 512) and rotary dims [544, 576).  Latent dim d goes to column d / 2,
+// rotary dim 512 + e to column 256 + e / 2 (bf16 pairs).  Padding rows are
+// zero.  The warp arrives on `ready` when its part is in.
+__device__ __forceinline__ void load_query_row(const DecodeArgs& a, const Item& it, int rows, uint32_t tmem,
+                                               uint32_t lane_off, int r, int half, uint64_t* ready) {
+  const int rb = kRows * it.g;
+  const bool real = r < min(kRows, rows - rb);
+  const uint4* src = reinterpret_cast<const uint4*>(
+      static_cast<const __nv_bfloat16*>(a.q) + ((size_t)it.b * rows + rb + (real ? r : 0)) * a.D);
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int c2 = 0; c2 < 2; ++c2) {
+    uint4 x[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) x[u] = real ? __ldg(src + half * 32 + c2 * 16 + u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint32_t v[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        v[4 * u] = x[8 * c + u].x; v[4 * u + 1] = x[8 * c + u].y;
+        v[4 * u + 2] = x[8 * c + u].z; v[4 * u + 3] = x[8 * c + u].w;
+      }
+      tmem_st32(tmem + lane_off + half * 128 + 64 * c2 + 32 * c, v);
+    }
+  }
+  {
+    uint32_t v[16];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint4 x = real ? __ldg(src + 64 + 4 * half + u) : make_uint4(0u, 0u, 0u, 0u);
+      v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
+    }
+    tmem_st16(tmem + lane_off + kTmemQr + 16 * half, v);
+  }
+  tmem_st_wait();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(ready);
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
-decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool,
-                 const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_ws) {
+decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page,
+                 const __grid_constant__ CUtensorMap tm_vhalf, const __grid_constant__ CUtensorMap tm_o,
+                 const __grid_constant__ CUtensorMap tm_ws) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ SmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* pslots = smem + kOffP;                  // value CTA: probability slots
+  uint8_t* pslots = smem + kOffP;                  // value CTA: probability units
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();         // 0: score CTA, 1: value CTA
   const int w = (int)cluster_id_x();
   volatile int* abort_flag = &ctl.abort;
+  const uint64_t wait_ns = a.wait_ns ? a.wait_ns : kWaitNs;
+  // this worker's message ring: page slot s holds a hi unit and a lo unit
+  unsigned char* gmsg = a.msg + (size_t)w * kGSlots * 2 * kPUnitBytes;
 
   if (threadIdx.x == 0) {
     ctl.abort = 0;
     ctl.never = 0;
-    for (int i = 0; i < kCells; ++i) {
-      mbar_init(&ctl.cell_full[i], 1);
-      mbar_init(&ctl.cell_empty[i], 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&ctl.slot_full[i], 1);
+      mbar_init(&ctl.slot_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.s_full[i], 1);
-      mbar_init(&ctl.s_free[i], 8);
+      mbar_init(&ctl.s_free[i], 4);
     }
-    for (int i = 0; i < kVUnits; ++i) {
+    for (int i = 0; i < kGSlots; ++i) {
+      mbar_init(&ctl.gfree[i], 1);
+      mbar_init(&ctl.p_ready[i], 1);
+      ctl.pflag_in[i] = 0;
+    }
+    for (int i = 0; i < kVSlots; ++i) {
       mbar_init(&ctl.v_full[i], 1);
       mbar_init(&ctl.v_empty[i], 1);
     }
     for (int i = 0; i < kPUnits; ++i) {
-      mbar_init(&ctl.pfree[i], 1);
       mbar_init(&ctl.p_recv[i], 1);
+      mbar_init(&ctl.unit_free[i], 1);
       mbar_init(&ctl.pv_done[i], 1);
       mbar_init(&ctl.rows_seen[i], 4);
-      ctl.pflags[i] = 0;
     }
+    for (int i = 0; i < 8; ++i) ctl.pflags[i] = 0;
     mbar_init(&ctl.q_ready, 8);
+    mbar_init(&ctl.q_free, 1);
     mbar_init(&ctl.resc_done, 4);
     mbar_init(&ctl.vz_done, 4);
     mbar_init(&ctl.o_free, 8);
     mbar_init(&ctl.epi_go, 4);
     mbar_init(&ctl.epi_done, 8);
-    mbar_init(&ctl.grp, 8);
+    for (int i = 0; i < 8; ++i) mbar_init(&ctl.written[i], 4);
     mbar_init(&ctl.mma_final, 1);
-    if (rank == 1)     // the first pages' probabilities will arrive
-      for (int i = 0; i < kPUnits; ++i) mbar_arrive_expect_tx(&ctl.p_recv[i], kPMsgBytes);
     fence_mbar_init_cluster();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_pool);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_page);
+    tma_prefetch_desc(&tm_vhalf);
+  }
   if (warp == 1) tmem_alloc(&ctl.tmem_base, 512);
   tc_fence_before();
   __syncthreads();
@@ -322,16 +403,17 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
                                   // always run 128 rows, the rest are zero padding)
   const int cap = a.max_blocks * kPage;
 
-  uint32_t g_prod = 0, g_issue = 0;    // producer: cells (score) or units (value) issued
-  uint32_t g_cell = 0;                 // score MMA: cells consumed
-  uint32_t g_step = 0;                 // score CTA: page-pair steps (MMA and softmax)
-  uint32_t g_page = 0;                 // pages (score softmax, value MMA and warps)
+  uint32_t g_prod = 0;                 // producer: pages walked (loads of both CTAs)
+  uint32_t g_issue = 0;                // producer: score CTA: 1 + last page loaded; value CTA: halves loaded
+  uint32_t g_page = 0;                 // pages (score MMA and softmax, value MMA and warps)
+  uint32_t g_load = 0;                 // value message loader: pages
+  uint32_t un_l = 0;                   // value message loader: units loaded
+  uint32_t g_sig = 0;                  // score signaler: pages signalled
   uint32_t it_cnt = 0;                 // items (MMA issuers, value warps)
-  uint32_t grp_phase = 0, n_resc = 0, n_vz = 0;
+  uint32_t n_resc = 0, n_vz = 0;
   // probability-unit counters: they run on across planning batches, like the
   // mbarrier phases they index
   uint32_t un = 0;                     // value MMA: units consumed
-  uint32_t un_s = 0;                   // score leader: units sent
   // value row warps: units seen, and per unit slot the parity of the next
   // phase of its page barriers (pv_done, rows_seen advance only when the slot
   // holds a page's first unit)
@@ -344,164 +426,144 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
 
     if (warp == 0) {
       // ============================================================ producer
-      // (the whole warp walks the loop; lane 0 issues barriers and copies)
+      // The whole warp walks the batch's pages in order; lane k holds the
+      // block ids of pages 32c + k of the current chunk c and of the next one
+      // (loaded a chunk ahead), lane 0 issues the copies.
+      const int total = ctl.n_flat;
       const uint64_t pol = policy_evict_first();
-      for (int ii = 0; ii < n_items; ++ii) {
+      int cur = lane < total ? block_of(a, &ctl, n_items, lane) : -1;
+      int nxt = 32 + lane < total ? block_of(a, &ctl, n_items, 32 + lane) : -1;
+      if (rank == 0) {
+        for (int f = 0; f < kPrefetch && f < total; ++f) {
+          const int bp = __shfl_sync(0xffffffffu, cur, f);
+          if (lane == 0 && bp >= 0 && bp < a.num_blocks) tma_prefetch_l2_4d(&tm_page, 0, 0, 0, bp * 8);
+        }
+      }
+      for (int f = 0; f < total; ++f) {
         if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-        const Item it = ctl.items[ii];
-        for (int jb = it.j0; jb < it.j1; jb += 32) {
-          if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-          const int jj = jb + lane;
-          int blk = -1;
-          if (jj < it.j1) blk = a.block_table[(size_t)it.b * a.max_blocks + jj];
-          const int nj = min(32, it.j1 - jb);
+        if ((f & 31) == 0 && f > 0) {
+          cur = nxt;
+          nxt = f + 32 + lane < total ? block_of(a, &ctl, n_items, f + 32 + lane) : -1;
+        }
+        const int pf = f + kPrefetch;
+        const int bpf = __shfl_sync(0xffffffffu, (pf >> 5) == (f >> 5) ? cur : nxt, pf & 31);
+        const int bk = __shfl_sync(0xffffffffu, cur, f & 31);
+        if (lane == 0) {
+          const bool ok = bk >= 0 && bk < a.num_blocks;
+          // an invalid block is read past the pool's end: TMA fills zeros
+          const int y = (ok ? bk : a.num_blocks) * 8;
           if (rank == 0) {
-            // page pairs (pairs start at j0, so they never straddle a 32-page chunk)
-            for (int k = 0; k < nj; k += 2) {
-              const bool two = k + 1 < nj;
-              const int bA = __shfl_sync(0xffffffffu, blk, k);
-              const int bB = __shfl_sync(0xffffffffu, blk, two ? k + 1 : k);
-              if (lane == 0) {
-                const bool okA = bA >= 0 && bA < a.num_blocks;
-                const bool okB = bB >= 0 && bB < a.num_blocks;
-                if (!okA || (two && !okB)) atomicOr(a.err, kErrBadIndex);
-                // an invalid block is read past the pool's end: TMA fills zeros
-                const int yA = okA ? bA * kPage : a.num_blocks * kPage;
-                const int yB = okB ? bB * kPage : a.num_blocks * kPage;
-                for (int c = 0; c < 9; ++c) {
-                  if (*abort_flag) break;
-                  const uint32_t sl = g_prod % kCells;
-                  if (g_prod >= (uint32_t)kCells &&
-                      !mbar_wait(&ctl.cell_empty[sl], ((g_prod / kCells) - 1) & 1, abort_flag, kWaitNs)) {
-                    fail(&ctl, a.err);
-                    break;
-                  }
-                  uint8_t* dst = smem + kOffCells + sl * kCell;
-                  mbar_arrive_expect_tx(&ctl.cell_full[sl], two ? kCell : kBox);
-                  tma_load_2d(dst, &tm_pool, &ctl.cell_full[sl], 64 * c, yA, pol);
-                  if (two) tma_load_2d(dst + kBox, &tm_pool, &ctl.cell_full[sl], 64 * c, yB, pol);
-                  ++g_prod;
-                  ++g_issue;
-                }
-              }
-              __syncwarp();
+            if (!ok) atomicOr(a.err, kErrBadIndex);
+            if (pf < total && bpf >= 0 && bpf < a.num_blocks) tma_prefetch_l2_4d(&tm_page, 0, 0, 0, bpf * 8);
+            const uint32_t sl = g_prod % kSlots;
+            if (g_prod >= (uint32_t)kSlots &&
+                !mbar_wait(&ctl.slot_empty[sl], ((g_prod / kSlots) - 1) & 1, abort_flag, wait_ns)) {
+              fail(&ctl, a.err);
+            } else if (!(a.skip_load > 0 && w == 0 && g_prod + 1 == (uint32_t)a.skip_load)) {
+              mbar_arrive_expect_tx(&ctl.slot_full[sl], kPageBytes);
+              tma_load_4d(smem + sl * kPageBytes, &tm_page, &ctl.slot_full[sl], 0, 0, 0, y, pol);
+              g_issue = g_prod + 1;
             }
           } else {
-            for (int k = 0; k < nj; ++k) {
-              const int bk = __shfl_sync(0xffffffffu, blk, k);
-              if (lane == 0) {
-                const bool valid = bk >= 0 && bk < a.num_blocks;
-                const int y = valid ? bk * kPage : a.num_blocks * kPage;
-                for (int nh = 0; nh < 2; ++nh) {
-                  if (*abort_flag) break;
-                  const uint32_t sl = g_prod % kVUnits;
-                  if (g_prod >= (uint32_t)kVUnits &&
-                      !mbar_wait(&ctl.v_empty[sl], ((g_prod / kVUnits) - 1) & 1, abort_flag, kWaitNs)) {
-                    fail(&ctl, a.err);
-                    break;
-                  }
-                  uint8_t* dst = smem + kOffV + sl * kVUnit;
-                  mbar_arrive_expect_tx(&ctl.v_full[sl], kVUnit);
-                  for (int bx = 0; bx < 4; ++bx)
-                    tma_load_2d(dst + bx * kBox, &tm_pool, &ctl.v_full[sl], 64 * (4 * nh + bx), y, pol);
-                  ++g_prod;
-                  ++g_issue;
-                }
+            for (int nh = 0; nh < 2; ++nh) {
+              const uint32_t u = 2 * g_prod + nh, vs = u % kVSlots;
+              if (u >= (uint32_t)kVSlots &&
+                  !mbar_wait(&ctl.v_empty[vs], ((u / kVSlots) - 1) & 1, abort_flag, wait_ns)) {
+                fail(&ctl, a.err);
+                break;
               }
-              __syncwarp();
+              mbar_arrive_expect_tx(&ctl.v_full[vs], kVHalf);
+              tma_load_4d(smem + kOffV + vs * kVHalf, &tm_vhalf, &ctl.v_full[vs], 0, 0, 4 * nh, y, pol);
+              ++g_issue;
             }
           }
         }
+        ++g_prod;
+        __syncwarp();
       }
     } else if (warp == 1) {
       // ============================================================ MMA issuer
       if (lane == 0) {
         if (rank == 0) {
-          const uint32_t idS2 = idesc_bf16_f32(128, 128, 0, 0);
-          const uint32_t idS1 = idesc_bf16_f32(128, 64, 0, 0);
-          const uint8_t* qr = smem + kOffQr;
+          const uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);
+          uint32_t g = g_page;
           for (int ii = 0; ii < n_items && !*abort_flag; ++ii) {
             const Item it = ctl.items[ii];
             const int n = it.j1 - it.j0;
-            bool ok = mbar_wait(&ctl.q_ready, it_cnt & 1, abort_flag, kWaitNs);
-            for (int k = 0; ok && k < n; k += 2) {
-              const uint32_t sb = g_step & 1;
-              const uint32_t id = (k + 1 < n) ? idS2 : idS1;
-              if (g_step >= 2) ok = mbar_wait(&ctl.s_free[sb], ((g_step >> 1) - 1) & 1, abort_flag, kWaitNs);
-              for (int c = 0; ok && c < 9; ++c) {
-                const uint32_t sl = g_cell % kCells;
-                ok = mbar_wait(&ctl.cell_full[sl], (g_cell / kCells) & 1, abort_flag, kWaitNs);
-                if (!ok) break;
-                tc_fence_after();
-                const uint8_t* cp = smem + kOffCells + sl * kCell;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  const int kk = 4 * c + q;
-                  const uint64_t bd = sdesc_sw128(smem_u32(cp + q * 32), 16, 1024);
-                  if (c < 8)
-                    mma_ts(tmem + sb * 128, tmem + kTmemQ + kk * 8, bd, id, kk > 0);
-                  else
-                    mma_ss(tmem + sb * 128, sdesc_sw128(smem_u32(qr + q * 32), 16, 1024), bd, id, 1);
-                }
-                mma_commit(&ctl.cell_empty[sl]);
-                ++g_cell;
-              }
+            bool ok = mbar_wait(&ctl.q_ready, it_cnt & 1, abort_flag, wait_ns);
+            for (int k = 0; ok && k < n; ++k, ++g) {
+              const uint32_t sb = g & 1, sl = g % kSlots;
+              if (g >= 2) ok = mbar_wait(&ctl.s_free[sb], ((g >> 1) - 1) & 1, abort_flag, wait_ns);
+              if (ok) ok = mbar_wait(&ctl.slot_full[sl], (g / kSlots) & 1, abort_flag, wait_ns);
               if (!ok) break;
+              tc_fence_after();
+              // B = the page's tokens (K-major SW128, 8-token groups 9 KB
+              // apart); chunk c starts 1 KB further, a K-step of 16 dims 32 B
+              const uint64_t b0 = sdesc_sw128(smem_u32(smem + sl * kPageBytes), 16, 9216);
+              const uint32_t d = tmem + kTmemS + 64 * sb;
+#pragma unroll
+              for (int c = 0; c < 9; ++c)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_ts(d, tmem + (uint32_t)(8 * (4 * c + kk)), b0 + (uint64_t)(64 * c + 2 * kk), idS,
+                         (c | kk) ? 1u : 0u);
+              mma_commit(&ctl.slot_empty[sl]);
               mma_commit(&ctl.s_full[sb]);
-              ++g_step;
             }
             if (!ok) { fail(&ctl, a.err); break; }
+            mma_commit(&ctl.q_free);
             ++it_cnt;
           }
+          g_page = g;
         } else {
           const uint32_t idPV = idesc_bf16_f32(128, 256, 0, 1);
+          const uint32_t peer_gfree = mapa(smem_u32(&ctl.gfree[0]), 0);   // + 8 * slot
           for (int ii = 0; ii < n_items && !*abort_flag; ++ii) {
             const Item it = ctl.items[ii];
             const int L = a.seqlens[it.b];
             const int Pb = pages_of(L, a.T_q, cap);
             // the previous item's epilogue must have read O before it is overwritten
-            bool ok = it_cnt == 0 || mbar_wait(&ctl.o_free, (it_cnt - 1) & 1, abort_flag, kWaitNs);
+            bool ok = it_cnt == 0 || mbar_wait(&ctl.o_free, (it_cnt - 1) & 1, abort_flag, wait_ns);
             for (int i = 0; ok && i < it.j1 - it.j0; ++i) {
               const uint32_t g = g_page + i, slot = un % kPUnits;
               const int j = it.j0 + i;
-              ok = mbar_wait_cluster(&ctl.p_recv[slot], (un / kPUnits) & 1, abort_flag, kWaitNs);
+              ok = mbar_wait(&ctl.p_recv[slot], (un / kPUnits) & 1, abort_flag, wait_ns);
               if (!ok) break;
-              fence_proxy_async_smem();
               const uint8_t* ps = pslots + slot * kPUnitBytes;
-              const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(ps + kPBytes);
-              if ((flags & 1u) && i > 0) {          // rows rescaled by the value warps
-                ok = mbar_wait(&ctl.resc_done, n_resc & 1, abort_flag, kWaitNs);
+              const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(&ctl.uflags[slot]);
+              const bool lo = (flags & kFlagLo) != 0;
+              const uint8_t* pl = pslots + ((un + 1) % kPUnits) * kPUnitBytes;   // low parts' unit
+              if (lo) ok = mbar_wait(&ctl.p_recv[(un + 1) % kPUnits], ((un + 1) / kPUnits) & 1, abort_flag, wait_ns);
+              if (!ok) break;
+              // the page's message slot in global memory has been read: the
+              // score CTA may write it again
+              mbar_arrive_remote(peer_gfree + 8 * (g % kGSlots));
+              if ((flags & kFlagRescale) && i > 0) {          // rows rescaled by the value warps
+                ok = mbar_wait(&ctl.resc_done, n_resc & 1, abort_flag, wait_ns);
                 ++n_resc;
               }
               if (ok && j == Pb - 1 && (L & (kPage - 1)) != 0) {   // tail rows zeroed
-                ok = mbar_wait(&ctl.vz_done, n_vz & 1, abort_flag, kWaitNs);
+                ok = mbar_wait(&ctl.vz_done, n_vz & 1, abort_flag, wait_ns);
                 ++n_vz;
               }
-              const bool lo = (flags & kFlagLo) != 0;
-              const uint8_t* pl = pslots + ((un + 1) % kPUnits) * kPUnitBytes;   // low parts' unit
-              if (ok && lo) {
-                ok = mbar_wait_cluster(&ctl.p_recv[(un + 1) % kPUnits], ((un + 1) / kPUnits) & 1, abort_flag, kWaitNs);
-                fence_proxy_async_smem();
-              }
               for (int nh = 0; ok && nh < 2; ++nh) {
-                const uint32_t u = 2 * g + nh, vs = u % kVUnits;
-                ok = mbar_wait(&ctl.v_full[vs], (u / kVUnits) & 1, abort_flag, kWaitNs);
+                const uint32_t u = 2 * g + nh, vs = u % kVSlots;
+                ok = mbar_wait(&ctl.v_full[vs], (u / kVSlots) & 1, abort_flag, wait_ns);
                 if (!ok) break;
                 tc_fence_after();
-                const uint8_t* vp = smem + kOffV + vs * kVUnit;
+                // B = V (MN-major SW128): 64-dim chunks 1 KB apart along N,
+                // 8-token groups 4 KB apart along K; a K-step is 16 tokens
+                const uint64_t bv = sdesc_sw128(smem_u32(smem + kOffV + vs * kVHalf), 1024, 4096);
+                const uint64_t ah = sdesc_sw128(smem_u32(ps), 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {   // 64 tokens, K-step 16
-                  const uint64_t ad = sdesc_sw128(smem_u32(ps + kk * 32), 16, 1024);
-                  const uint64_t bd = sdesc_sw128(smem_u32(vp + kk * 2048), kBox, 1024);
-                  mma_ss(tmem + nh * 256, ad, bd, idPV, (i > 0 || kk > 0) ? 1 : 0);
-                }
+                for (int kk = 0; kk < 4; ++kk)   // 64 tokens, K-step 16
+                  mma_ss(tmem + nh * 256, ah + (uint64_t)(2 * kk), bv + (uint64_t)(512 * kk), idPV,
+                         (i > 0 || kk > 0) ? 1u : 0u);
                 if (lo) {
+                  const uint64_t al = sdesc_sw128(smem_u32(pl), 16, 1024);
 #pragma unroll
-                  for (int kk = 0; kk < 4; ++kk) {   // the same V rows, A = low parts
-                    const uint64_t ad = sdesc_sw128(smem_u32(pl + kk * 32), 16, 1024);
-                    const uint64_t bd = sdesc_sw128(smem_u32(vp + kk * 2048), kBox, 1024);
-                    mma_ss(tmem + nh * 256, ad, bd, idPV, 1);
-                  }
+                  for (int kk = 0; kk < 4; ++kk)   // the same V rows, A = low parts
+                    mma_ss(tmem + nh * 256, al + (uint64_t)(2 * kk), bv + (uint64_t)(512 * kk), idPV, 1u);
                 }
                 mma_commit(&ctl.v_empty[vs]);
               }
@@ -516,18 +578,16 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
         }
       }
       __syncwarp();
-    } else if (rank == 0) {
+    } else if (rank == 0 && warp <= 5) {
       // ============================================================ softmax (score CTA)
-      // warp w: TMEM lane quarter w & 3 (32 rows); half 0 (warps 2-5) takes the
-      // first page of each pair, half 1 (warps 6-9) the second
+      // warp w owns TMEM lane quarter w & 3: rows 32 (w & 3) .. + 31, one row
+      // per thread over all 64 tokens of a page, so a row's running max and
+      // sum live in one thread and the four warps need no barrier among
+      // themselves; each arrives on the page's `written` barrier once its
+      // rows of the message are out
       const int q4 = warp & 3;
-      const int half = warp >= 6 ? 1 : 0;
       const int r = 32 * q4 + lane;
       const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-      const uint32_t peer_p = mapa(smem_u32(pslots), 1);               // value CTA's slots
-      const uint32_t peer_precv = mapa(smem_u32(&ctl.p_recv[0]), 1);   // + 8 * slot
-      const bool leader = threadIdx.x == 64;
-      uint8_t* qr = smem + kOffQr;
       for (int ii = 0; ii < n_items; ++ii) {
         if (__any_sync(0xffffffffu, *abort_flag)) break;
         const Item it = ctl.items[ii];
@@ -538,56 +598,25 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
         // padding rows (r >= rows_g) see no token at all
         const int lim = r >= rows_g ? -1 : a.causal ? (L - a.T_q + t) : (L - 1);
         const int n = it.j1 - it.j0;
-        // the query row: latent dims -> TMEM (half 0: [0, 256), half 1: [256, 512)),
-        // rotary dims -> shared memory (K-major SW128; half h: 16-byte chunks 4h..4h+3)
-        {
-          const bool real = r < rows_g;
-          const uint4* src = reinterpret_cast<const uint4*>(
-              static_cast<const __nv_bfloat16*>(a.q) + ((size_t)it.b * rows + rb + (real ? r : 0)) * a.D);
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint4 x = real ? __ldg(src + half * 32 + c * 8 + u) : make_uint4(0u, 0u, 0u, 0u);
-              v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
-            }
-            tmem_st32(tmem + lane_off + kTmemQ + half * 128 + 32 * c, v);
-          }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int ch = 4 * half + c;
-            *reinterpret_cast<uint4*>(qr + r * 128 + ((ch ^ (r & 7)) << 4)) =
-                real ? __ldg(src + 64 + ch) : make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_smem();
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl.q_ready);
-        }
-        float m_run = -INFINITY, l_half = 0.f;
+        load_query_row(a, it, rows, tmem, lane_off, r, 0, &ctl.q_ready);
+        float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int k = 0; k < n; k += 2) {
-          const bool two = k + 1 < n;
-          const bool has = half == 0 || two;           // this half's page exists
-          const uint32_t sb = g_step & 1;
-          const uint32_t gA = g_page;
-          const int jh = it.j0 + k + half;
-          const bool last_step = k + 2 >= n;
-          int bk = -1;
-          if (has) bk = __ldg(a.block_table + (size_t)it.b * a.max_blocks + jh);
-          const bool page_ok = has && bk >= 0 && bk < a.num_blocks;
-          if (!warp_wait(&ctl.s_full[sb], (g_step >> 1) & 1, abort_flag)) { ok = false; break; }
+        for (int k = 0; k < n; ++k) {
+          const uint32_t g = g_page + k, sb = g & 1, gs = g % kGSlots;
+          const int j = it.j0 + k;
+          const bool last_page = k + 1 == n;
+          const int bk = __ldg(a.block_table + (size_t)it.b * a.max_blocks + j);
+          const bool page_ok = bk >= 0 && bk < a.num_blocks;
+          if (!warp_wait(&ctl.s_full[sb], (g >> 1) & 1, abort_flag, wait_ns)) { ok = false; break; }
           tc_fence_after();
           float x[64];
-          tmem_ld64(tmem + lane_off + sb * 128 + 64 * half, x);
+          tmem_ld64(tmem + lane_off + kTmemS + 64 * sb, x);
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl.s_free[sb]);     // score buffer reusable
-          // mask (tokens past the visible range, a missing page, a bad block id)
-          const int tok0 = jh * kPage;
+          // mask (tokens past the visible range, a bad block id, padding rows)
+          const int tok0 = j * kPage;
           if (!page_ok || tok0 + 63 > L - a.T_q || r >= rows_g) {
             const int lim_page = page_ok ? lim : -1;
 #pragma unroll
@@ -596,39 +625,33 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
           float mx = x[0];
 #pragma unroll
           for (int q = 1; q < 64; ++q) mx = fmaxf(mx, x[q]);
-          ctl.rowx[half][r] = mx;
-          const uint32_t fh = (gA + half) % 6;   // this half's page flags
-          {
-            // Precision of the bf16 probabilities: a page whose largest
-            // probability is not small against the row sum so far also sends
-            // the low bf16 parts (p - bf16(p)).  Tested conservatively, before
-            // the rows' maxima are merged: against this half's own running sum
-            // and the previous reference (both can only make the test pass more
-            // often than with the merged values).
-            // The item's last page always sends them: its two units then give
-            // the value CTA's epilogue its staging space.
-            const bool heavy = has && ex2(mx * sl2 - m_run) >= l_half;
-            const bool item_last = has && last_step && half == (two ? 1 : 0);
-            if ((__any_sync(0xffffffffu, heavy) || item_last) && lane == 0) atomicOr(&ctl.pflags[fh], kFlagLo);
-          }
-          if (leader) bulk_wait_read0();   // the previous step's copies have read the staging
-          if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { ok = false; break; }   // [A]
-          const float m_page = fmaxf(mx, ctl.rowx[half ^ 1][r]) * sl2;
+          const float m_page = mx * sl2;
           const float m_new = fmaxf(m_run, m_page);
           const bool need = m_new > m_run + kRescaleThreshold;
           float alpha = 1.f;
           if (need) {
             alpha = ex2(m_run - m_new);     // 0 when m_run = -inf
             m_run = m_new;
-            l_half *= alpha;
+            l_run *= alpha;
           }
-          uint8_t* stg = smem + kOffStg + half * kStgPageBytes;   // this half's page message
-          if (has) {
-            // probabilities, rounded to bf16 (and, for a heavy page, the
-            // residual rounded again); l sums exactly what the value MMA sees.
-            // Rows are staged in the layout the value CTA's MMA reads
-            // (K-major SW128: 16-byte chunk c of row r at c ^ (r & 7)).
-            const bool lo = (ctl.pflags[fh] & kFlagLo) != 0;
+          // Precision of the bf16 probabilities: a page whose largest
+          // probability is not small against the row's sum so far also sends
+          // the low bf16 parts (p - bf16(p)).  The item's last page always
+          // sends them: its two units then give the value CTA's epilogue its
+          // staging space.
+          // (Every page's low parts are written, so that the flag may come
+          // from any of the four warps.)
+          const bool lo = __any_sync(0xffffffffu, ex2(m_page - m_run) >= l_run) || last_page;
+          // the page's message slot must have been read by the value CTA
+          if (g >= (uint32_t)kGSlots &&
+              !warp_wait_cluster(&ctl.gfree[gs], ((g / kGSlots) - 1) & 1, abort_flag, wait_ns)) { ok = false; break; }
+          unsigned char* msg = gmsg + (size_t)gs * 2 * kPUnitBytes;
+          {
+            // probabilities rounded to bf16, and the residuals rounded again
+            // (the low parts).  Rows are written in the layout the value
+            // CTA's MMA reads (K-major SW128: 16-byte chunk c of row r at
+            // c ^ (r & 7)).  The running sum here only guides the choice of
+            // the low parts; the value CTA sums what its MMAs use.
             float psum = 0.f;
             const float neg_m = -m_run;
 #pragma unroll
@@ -641,77 +664,110 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
                 const float p1 = x1 == -INFINITY ? 0.f : ex2(fmaf(x1, sl2, neg_m));
                 pk[e] = pack_bf16x2(p0, p1);
                 const float h0 = __uint_as_float(lo_half_f(pk[e])), h1 = __uint_as_float(hi_half_f(pk[e]));
-                psum += h0 + h1;
-                if (lo) {
-                  pl[e] = pack_bf16x2(p0 - h0, p1 - h1);
-                  psum += __uint_as_float(lo_half_f(pl[e])) + __uint_as_float(hi_half_f(pl[e]));
-                }
+                psum += p0 + p1;
+                pl[e] = pack_bf16x2(p0 - h0, p1 - h1);
               }
               const int off = r * 128 + ((c ^ (r & 7)) << 4);
-              *reinterpret_cast<uint4*>(stg + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              if (lo) *reinterpret_cast<uint4*>(stg + kPUnitBytes + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+              *reinterpret_cast<uint4*>(msg + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              *reinterpret_cast<uint4*>(msg + kPUnitBytes + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
             }
-            l_half += psum;
+            l_run += psum;
           }
-          if (__any_sync(0xffffffffu, need) && k > 0 && lane == 0 && half == 0)
-            atomicOr(&ctl.pflags[gA % 6], kFlagRescale);
-          float l_tot = 0.f;
-          if (last_step) {
-            ctl.rowl[half][r] = l_half;
-            if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { ok = false; break; }
-            l_tot = ctl.rowl[0][r] + ctl.rowl[1][r];
-            if (half == 0 && r < rows_g) {
-              const float lse = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
-              const int wslot = it.vb + w;
-              if (it.flags & 1) { if (a.lse) a.lse[(size_t)it.b * rows + rb + r] = lse; }
-              else a.ws_lse[(size_t)wslot * a.SR + r] = lse;
-              if (r == 0 && it.j0 == 0) a.meta[it.vb] = make_int2(it.w_first, it.w_last);
-            }
+          // per-row (alpha, m): the rescale factor that applies before this
+          // page's value MMA, and the reference max the page's
+          // probabilities are relative to (base 2, scaled)
+          *reinterpret_cast<float2*>(msg + kPBytes + 16 + r * 8) = make_float2(alpha, m_run);
+          fence_proxy_async_global();      // the value CTA reads the message with a bulk copy
+          // flags of the page (gathered from the four warps), then this
+          // warp's rows are out
+          const bool resc = __any_sync(0xffffffffu, need) && k > 0;
+          if (lane == 0) {
+            const uint32_t fl = (lo ? kFlagLo : 0u) | (resc ? kFlagRescale : 0u);
+            if (fl) atomicOr(&ctl.pflags[g & 7], fl);
           }
-          // per-row (alpha, l): the rescale factor rides on the pair's first
-          // page; l (the row sum) on the item's last page
-          if (has) {
-            const bool last_page = last_step && half == (two ? 1 : 0);
-            *reinterpret_cast<float2*>(stg + kPBytes + 16 + r * 8) =
-                make_float2(half == 0 ? alpha : 1.f, last_page ? l_tot : 0.f);
-            fence_proxy_async_smem();      // the bulk copy reads the staging
-          }
-          if (!group_sync(&ctl.grp, grp_phase, abort_flag)) { ok = false; break; }   // [B]
-          // headers (flags gathered from all warps of each page), then per unit
-          // one bulk copy into the value CTA's ring once the value CTA has freed
-          // that unit; its bytes complete the unit's barrier there.  Only this
-          // thread waits here: the staging is local, so the softmax of the
-          // next step runs while the value CTA catches up.
-          if (leader) {
-            bool fr = true;
-            for (uint32_t e = 0; e < (two ? 2u : 1u) && fr; ++e) {
-              uint8_t* st = smem + kOffStg + e * kStgPageBytes;
-              const uint32_t fi = (gA + e) % 6;
-              const uint32_t fl = ctl.pflags[fi];
-              ctl.pflags[fi] = 0u;              // ready for page gA + e + 6
-              *reinterpret_cast<uint4*>(st + kPBytes) = make_uint4(fl, 0u, 0u, 0u);
-              fence_proxy_async_smem();
-              for (uint32_t part = 0; part < ((fl & kFlagLo) ? 2u : 1u) && fr; ++part) {
-                const uint32_t ui = un_s++, us = ui % kPUnits;
-                if (ui >= (uint32_t)kPUnits)
-                  fr = mbar_wait_cluster(&ctl.pfree[us], ((ui / kPUnits) - 1) & 1, abort_flag, kWaitNs);
-                if (fr)
-                  bulk_copy_to_peer(peer_p + us * kPUnitBytes, st + part * kPUnitBytes, kPMsgBytes,
-                                    peer_precv + 8 * us);
-              }
-            }
-            bulk_commit();
-            if (!fr) fail(&ctl, a.err);
-          }
-          g_page += two ? 2 : 1;
-          ++g_step;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.written[g & 7]);
         }
         if (!ok) { fail(&ctl, a.err); break; }
+        g_page += n;
       }
+    } else if (rank == 0 && warp == 10) {
+      // ============================================================ signaler (score CTA)
+      // once the four softmax warps have written page g's message: its flags
+      // into the value CTA's shared memory, then an arrival at cluster scope
+      // there, which releases every write of the message (they happen before
+      // it through the `written` barrier)
+      if (lane == 0) {
+        const uint32_t peer_pready = mapa(smem_u32(&ctl.p_ready[0]), 1);   // + 8 * slot
+        const uint32_t peer_pflag = mapa(smem_u32(&ctl.pflag_in[0]), 1);   // + 4 * slot
+        const int total = ctl.n_flat;
+        for (int f = 0; f < total && !*abort_flag; ++f) {
+          const uint32_t g = g_sig, gs = g % kGSlots;
+          if (!mbar_wait(&ctl.written[g & 7], (g >> 3) & 1, abort_flag, wait_ns)) {
+            fail(&ctl, a.err);
+            break;
+          }
+          const uint32_t fl = *reinterpret_cast<volatile uint32_t*>(&ctl.pflags[g & 7]);
+          ctl.pflags[g & 7] = 0u;              // ready for page g + 8
+          st_cluster_u32(peer_pflag + 4 * gs, fl);
+          mbar_arrive_remote(peer_pready + 8 * gs);
+          ++g_sig;
+        }
+      }
+      __syncwarp();
+    } else if (rank == 0) {
+      // score CTA warps 6-9: the second half of each item's query rows
+      const int q4 = warp & 3;
+      const int r = 32 * q4 + lane;
+      const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+      for (int ii = 0; ii < n_items; ++ii) {
+        if (__any_sync(0xffffffffu, *abort_flag)) break;
+        const Item it = ctl.items[ii];
+        // the previous item's scores, which read the query, are complete
+        // (one phase of q_free per item; these warps are never more than one
+        // item ahead, because the scores of an item wait for its query)
+        if (it_cnt > 0 && !warp_wait(&ctl.q_free, (it_cnt - 1) & 1, abort_flag, wait_ns)) { fail(&ctl, a.err); break; }
+        load_query_row(a, it, rows, tmem, lane_off, r, 1, &ctl.q_ready);
+        ++it_cnt;
+      }
+    } else if (warp == 10) {
+      // ============================================================ value CTA: message loader
+      // page g's message: one unit, or two when its flags say that the low
+      // parts follow; each goes to the next shared-memory unit once the value
+      // warps have freed it
+      if (lane == 0) {
+        const int total = ctl.n_flat;
+        for (int f = 0; f < total && !*abort_flag; ++f) {
+          const uint32_t g = g_load, gs = g % kGSlots;
+          if (!mbar_wait_cluster(&ctl.p_ready[gs], (g / kGSlots) & 1, abort_flag, wait_ns)) {
+            fail(&ctl, a.err);
+            break;
+          }
+          fence_proxy_async_global();
+          const uint32_t fl = *reinterpret_cast<volatile uint32_t*>(&ctl.pflag_in[gs]);
+          const unsigned char* msg = gmsg + (size_t)gs * 2 * kPUnitBytes;
+          bool ok = true;
+          for (uint32_t e = 0; e < ((fl & kFlagLo) ? 2u : 1u); ++e) {
+            const uint32_t su = un_l % kPUnits;
+            if (un_l >= (uint32_t)kPUnits &&
+                !mbar_wait(&ctl.unit_free[su], ((un_l / kPUnits) - 1) & 1, abort_flag, wait_ns)) {
+              ok = false;
+              break;
+            }
+            ctl.uflags[su] = fl;   // read by the value warps after the unit's bytes arrive
+            mbar_arrive_expect_tx(&ctl.p_recv[su], kPMsgBytes);
+            bulk_load_g2s(pslots + su * kPUnitBytes, msg + e * kPUnitBytes, kPMsgBytes, &ctl.p_recv[su]);
+            ++un_l;
+          }
+          if (!ok) { fail(&ctl, a.err); break; }
+          ++g_load;
+        }
+      }
+      __syncwarp();
     } else {
       // ============================================================ value CTA warps
       // warps 2-5 ("row warps"): page bookkeeping, row rescales, tail zeroing;
-      // all eight: the epilogue, warp w writing rows 32 (w & 3) .. + 31 and
+      // warps 2-9: the epilogue, warp w writing rows 32 (w & 3) .. + 31 and
       // output columns [256 * (w >= 6), + 256)
       const int q4 = warp & 3;
       const int ch = warp >= 6 ? 1 : 0;
@@ -719,7 +775,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
       const int r = 32 * q4 + lane;
       const int tq = threadIdx.x - 64;             // 0..127 (row warps)
       const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-      const uint32_t peer_pfree = mapa(smem_u32(&ctl.pfree[0]), 0);   // + 8 * unit slot
+      float l_row = 0.f;                           // row warps: row r's running sum
       for (int ii = 0; ii < n_items; ++ii) {
         if (__any_sync(0xffffffffu, *abort_flag)) break;
         const Item it = ctl.items[ii];
@@ -732,22 +788,57 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
             const uint32_t g = g_page + i, slot = un_v % kPUnits;
             const int j = it.j0 + i;
             uint8_t* ps = pslots + slot * kPUnitBytes;
-            if (!warp_wait_cluster(&ctl.p_recv[slot], (un_v / kPUnits) & 1, abort_flag)) { ok = false; break; }
-            const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(ps + kPBytes);
+            if (!warp_wait(&ctl.p_recv[slot], (un_v / kPUnits) & 1, abort_flag, wait_ns)) { ok = false; break; }
+            const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(&ctl.uflags[slot]);
             const bool lo = (flags & kFlagLo) != 0;
             const uint32_t par = (pvpar >> slot) & 1;
             const float* info = reinterpret_cast<const float*>(ps + kPBytes + 16);
+            if (lo && !warp_wait(&ctl.p_recv[(un_v + 1) % kPUnits], ((un_v + 1) / kPUnits) & 1, abort_flag, wait_ns)) {
+              ok = false;
+              break;
+            }
+            {
+              // the row sum of exactly what the value MMAs use: the bf16
+              // probabilities of this row (and their low parts)
+              const float2 am = reinterpret_cast<const float2*>(info)[r];
+              float srow = 0.f;
+              for (uint32_t e = 0; e < (lo ? 2u : 1u); ++e) {
+                const uint4* prow = reinterpret_cast<const uint4*>(pslots + ((un_v + e) % kPUnits) * kPUnitBytes + r * 128);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                  const uint4 v = prow[c];
+                  srow += __uint_as_float(lo_half_f(v.x)) + __uint_as_float(hi_half_f(v.x)) +
+                          __uint_as_float(lo_half_f(v.y)) + __uint_as_float(hi_half_f(v.y)) +
+                          __uint_as_float(lo_half_f(v.z)) + __uint_as_float(hi_half_f(v.z)) +
+                          __uint_as_float(lo_half_f(v.w)) + __uint_as_float(hi_half_f(v.w));
+                }
+              }
+              l_row = (i == 0 ? 0.f : l_row * am.x) + srow;
+              if (i == n - 1) {
+                // the item's last page: lse (natural log), the merge record,
+                // and the row sum for the epilogue warps
+                ctl.lrow[r] = l_row;
+                const int rb = kRows * it.g;
+                if (r < min(kRows, rows - rb)) {
+                  const float lse = l_row > 0.f ? (am.y + __log2f(l_row)) * kLn2 : -INFINITY;
+                  if (it.flags & 1) { if (a.lse) a.lse[(size_t)it.b * rows + rb + r] = lse; }
+                  else a.ws_lse[(size_t)(it.vb + w) * a.SR + r] = lse;
+                  if (r == 0 && it.j0 == 0) a.meta[it.vb] = make_int2(it.w_first, it.w_last);
+                }
+              }
+            }
             if (j == Pb - 1 && (L & (kPage - 1)) != 0) {
               // last page: zero the V rows past the sequence end (they may hold NaN)
               const int nv = L & (kPage - 1);
-              const int per_box = (kPage - nv) * 8;    // 16-byte chunks per box
+              const int per_half = (kPage - nv) * 4 * 8;   // 16-byte pieces per half page
               for (int nh = 0; nh < 2 && ok; ++nh) {
-                const uint32_t u = 2 * g + nh, vs = u % kVUnits;
-                if (!warp_wait(&ctl.v_full[vs], (u / kVUnits) & 1, abort_flag)) { ok = false; break; }
-                uint4* vp = reinterpret_cast<uint4*>(smem + kOffV + vs * kVUnit);
-                for (int q = tq; q < 4 * per_box; q += kRows) {
-                  const int bx = q / per_box, rem = q - bx * per_box;
-                  vp[(bx * kBox + (nv + rem / 8) * 128) / 16 + (rem & 7)] = make_uint4(0, 0, 0, 0);
+                const uint32_t u = 2 * g + nh, vs = u % kVSlots;
+                if (!warp_wait(&ctl.v_full[vs], (u / kVSlots) & 1, abort_flag, wait_ns)) { ok = false; break; }
+                uint4* vp = reinterpret_cast<uint4*>(smem + kOffV + vs * kVHalf);
+                for (int q = tq; q < per_half; q += kRows) {
+                  const int tk = nv + q / 32, rem = q & 31;      // token, (chunk, piece)
+                  const int cc = rem >> 3, pc = rem & 7;
+                  vp[((tk >> 3) * 4096 + cc * 1024 + (tk & 7) * 128) / 16 + pc] = make_uint4(0, 0, 0, 0);
                 }
               }
               if (!ok) break;
@@ -755,9 +846,9 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
               __syncwarp();
               if (lane == 0) mbar_arrive(&ctl.vz_done);
             }
-            if ((flags & 1u) && i > 0) {
+            if ((flags & kFlagRescale) && i > 0) {
               // rescale O rows before this page's value MMA: O holds pages < j
-              if (!warp_wait(&ctl.pv_done[prev_slot], prev_par, abort_flag)) { ok = false; break; }
+              if (!warp_wait(&ctl.pv_done[prev_slot], prev_par, abort_flag, wait_ns)) { ok = false; break; }
               tc_fence_after();
               const float alpha = info[2 * r];
 #pragma unroll 1
@@ -784,16 +875,12 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl.rows_seen[slot]);
             // this page's value MMA done
-            if (!warp_wait(&ctl.pv_done[slot], par, abort_flag)) { ok = false; break; }
+            if (!warp_wait(&ctl.pv_done[slot], par, abort_flag, wait_ns)) { ok = false; break; }
             if (i < n - 1) {
-              // the page's units may be refilled once every row warp is past its header
+              // the page's units may be reloaded once every row warp is past its header
               if (threadIdx.x == 64) {
-                if (mbar_wait(&ctl.rows_seen[slot], par, abort_flag, kWaitNs)) {
-                  for (uint32_t e = 0; e < (lo ? 2u : 1u); ++e) {
-                    const uint32_t us = (un_v + e) % kPUnits;
-                    mbar_arrive_expect_tx(&ctl.p_recv[us], kPMsgBytes);
-                    mbar_arrive_remote(peer_pfree + 8 * us);
-                  }
+                if (mbar_wait(&ctl.rows_seen[slot], par, abort_flag, wait_ns)) {
+                  for (uint32_t e = 0; e < (lo ? 2u : 1u); ++e) mbar_arrive(&ctl.unit_free[(un_v + e) % kPUnits]);
                 } else {
                   fail(&ctl, a.err);
                 }
@@ -812,7 +899,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
             un_v += lo ? 2 : 1;
           }
         }
-        if (ok && !warp_wait(&ctl.epi_go, it_cnt & 1, abort_flag)) ok = false;
+        if (ok && !warp_wait(&ctl.epi_go, it_cnt & 1, abort_flag, wait_ns)) ok = false;
         if (!ok) { fail(&ctl, a.err); break; }
         // ---- epilogue: normalise and write the item's 128 x 512 output, each
         // warp staging 32 rows x 16 columns at a time for full-sector writes
@@ -821,8 +908,8 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
         if (eu == 0xffffffffu) { fail(&ctl, a.err); break; }   // cannot happen: the last page sends low parts
         uint8_t* ps_last = pslots + (eu % kPUnits) * kPUnitBytes;
         uint8_t* ps_lo = pslots + ((eu + 1) % kPUnits) * kPUnitBytes;
-        const float l_row = reinterpret_cast<const float*>(ps_last + kPBytes + 16)[2 * r + 1];
-        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+        const float l_fin = ctl.lrow[r];
+        const float inv = l_fin > 0.f ? 1.f / l_fin : 0.f;
         const bool whole = it.flags & 1;
         const int rb = kRows * it.g;                            // first row of the row group
         const int grp_rows = min(32, min(kRows, rows - rb) - 32 * q4);   // real rows of this warp's group
@@ -833,7 +920,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
         __syncwarp();
         if (grp_rows == 32) {
           // whole 32-row group: 32 x 32 fp32 boxes staged (SW128) in the
-          // slot's probability areas (not its factors) and written by TMA
+          // units' probability areas (not their factors) and written by TMA
           const CUtensorMap* tmo = whole ? &tm_o : &tm_ws;
           const int row0 = (whole ? it.b * rows + rb : (it.vb + w) * a.SR) + 32 * q4;
           const int wi = warp - 2;
@@ -856,7 +943,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
               bulk_commit();
             }
           }
-          if (lane == 0) bulk_wait_read0();         // staging free before the slot is handed back
+          if (lane == 0) bulk_wait_read0();         // staging free before the units are handed back
           __syncwarp();
         }
         // a warp's own 4 KB of the two units (the same region its TMA boxes
@@ -893,13 +980,9 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
           mbar_arrive(&ctl.epi_done);
         }
         if (threadIdx.x == 64) {
-          // hand the staging slot back once every epilogue warp is done with it
-          if (mbar_wait(&ctl.epi_done, it_cnt & 1, abort_flag, kWaitNs)) {
-            for (uint32_t e = 0; e < 2; ++e) {
-              const uint32_t us = (eu + e) % kPUnits;
-              mbar_arrive_expect_tx(&ctl.p_recv[us], kPMsgBytes);
-              mbar_arrive_remote(peer_pfree + 8 * us);
-            }
+          // hand the staging units back once every epilogue warp is done with them
+          if (mbar_wait(&ctl.epi_done, it_cnt & 1, abort_flag, wait_ns)) {
+            for (uint32_t e = 0; e < 2; ++e) mbar_arrive(&ctl.unit_free[(eu + e) % kPUnits]);
           } else {
             fail(&ctl, a.err);
           }
@@ -916,19 +999,36 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
 
   // the merge pass may start launching now (it waits for this grid's completion)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // ---- drain: all MMAs complete, all TMA loads and bulk copies done, then free TMEM
-  if (rank == 0 && threadIdx.x == 64) bulk_wait0();
-  if (rank == 1 && warp >= 2 && lane == 0) bulk_wait0();   // output stores complete
+  // ---- drain: all MMAs complete, all copies done, then free TMEM
+  if (rank == 1 && warp >= 2 && warp <= 9 && lane == 0) bulk_wait0();   // output stores complete
   if (warp == 1 && lane == 0) {
     mma_commit(&ctl.mma_final);
-    if (!mbar_wait(&ctl.mma_final, 0, &ctl.never, kWaitNs)) atomicOr(a.err, kErrTimeout);
+    if (!mbar_wait(&ctl.mma_final, 0, &ctl.never, wait_ns)) atomicOr(a.err, kErrTimeout);
   }
   if (warp == 0 && lane == 0) {
-    const uint32_t nring = rank == 0 ? kCells : kVUnits;
-    uint64_t* full = rank == 0 ? ctl.cell_full : ctl.v_full;
-    for (uint32_t k = 0; k < nring && k < g_issue; ++k) {
-      const uint32_t g = g_issue - 1 - k;
-      if (!mbar_wait(&full[g % nring], (g / nring) & 1, &ctl.never, kWaitNs)) atomicOr(a.err, kErrTimeout);
+    // the last copies issued into each ring slot have landed
+    if (rank == 0) {
+      // pages are loaded in order; a skipped load (test hook) leaves a gap
+      for (uint32_t k = 0; k < (uint32_t)kSlots && k < g_issue; ++k) {
+        const uint32_t g = g_issue - 1 - k;
+        if (a.skip_load > 0 && w == 0 && g + 1 == (uint32_t)a.skip_load) continue;
+        if (!mbar_wait(&ctl.slot_full[g % kSlots], (g / kSlots) & 1, &ctl.never, wait_ns))
+          atomicOr(a.err, kErrTimeout);
+      }
+    } else {
+      const uint32_t nu = g_issue;
+      for (uint32_t k = 0; k < (uint32_t)kVSlots && k < nu; ++k) {
+        const uint32_t u = nu - 1 - k;
+        if (!mbar_wait(&ctl.v_full[u % kVSlots], (u / kVSlots) & 1, &ctl.never, wait_ns))
+          atomicOr(a.err, kErrTimeout);
+      }
+    }
+  }
+  if (rank == 1 && warp == 10 && lane == 0) {
+    for (uint32_t k = 0; k < (uint32_t)kPUnits && k < un_l; ++k) {
+      const uint32_t u = un_l - 1 - k;
+      if (!mbar_wait(&ctl.p_recv[u % kPUnits], (u / kPUnits) & 1, &ctl.never, wait_ns))
+        atomicOr(a.err, kErrTimeout);
     }
   }
   tc_fence_before();
@@ -941,21 +1041,24 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_pool
   cluster_wait();
 }
 
-CUresult (*g_encode)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                     const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
-                     CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                     CUtensorMapFloatOOBfill) = nullptr;
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+std::once_flag g_encode_once;
+TensorMapEncodeFn g_encode = nullptr;
+cudaError_t g_encode_err = cudaSuccess;
 
 cudaError_t get_encode() {
-  if (g_encode) return cudaSuccess;
-  void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                   cudaEnableDefault, &q);
-  if (e != cudaSuccess) return e;
-  if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
-  g_encode = reinterpret_cast<decltype(g_encode)>(fn);
-  return cudaSuccess;
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e == cudaSuccess && (q != cudaDriverEntryPointSuccess || !fn)) e = cudaErrorNotSupported;
+    if (e == cudaSuccess) g_encode = reinterpret_cast<TensorMapEncodeFn>(fn);
+    g_encode_err = e;
+  });
+  return g_encode_err;
 }
 
 cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
@@ -972,7 +1075,31 @@ cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t r
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-int g_max_clusters[64] = {};
+// The pool [num_blocks, 64, 576] bf16 seen as 4-D: (64 dims of a chunk,
+// 8 tokens of a group, 9 chunks, num_blocks * 8 groups).  A box of `chunks`
+// chunks starting at chunk c0 and 8 groups is one page (or its latent
+// half), laid out [group][chunk][token][dim] in shared memory.
+cudaError_t make_page_map(CUtensorMap* m, const void* pool, long long num_blocks, uint32_t chunks) {
+  cuuint64_t dims[4] = {64, 8, 9, (cuuint64_t)num_blocks * 8};
+  cuuint64_t strides[3] = {576 * 2, 64 * 2, 8 * 576 * 2};
+  cuuint32_t box[4] = {64, 8, chunks, 8};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims, strides,
+                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+constexpr int kMaxDev = 64;
+std::atomic<int> g_max_clusters[kMaxDev];
+std::atomic<bool> g_attr_set[kMaxDev];
+
+cudaError_t set_smem_attr(int dev) {
+  if (dev >= 0 && dev < kMaxDev && g_attr_set[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDev) g_attr_set[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 }  // namespace
 
@@ -982,37 +1109,33 @@ bool tc_supported(int dtype, int H, int T_q, int d_c, int d_r) {
 }
 
 int tc_item_cost(int rows) {
-  // Fixed cost of one work item, in pages: the worker loads the item's query
-  // rows through the same SM port that streams the pages, and the value CTA
-  // drains 128 x 512 fp32 of output before the next item may start.  Measured
-  // on B300 by sweeping the cost: about five pages' time at 128 query rows,
-  // three at 32.
+  // Fixed cost of one work item, in pages: the score CTA loads the item's
+  // query rows into tensor memory before its first scores, and the value CTA
+  // drains 128 x 512 fp32 of output before the next item may start.
   return 2 + (3 * rows + 64) / 128;
 }
 
 int tc_workers(int num_sms) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
-  if (!g_max_clusters[dev]) {
-    int n = 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_sms);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2; attr.val.clusterDim.y = 1; attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel, &cfg) != cudaSuccess || n < 1) {
-      cudaGetLastError();
-      n = num_sms / 2;
-    }
-    g_max_clusters[dev] = n;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return num_sms / 2;
+  int n = g_max_clusters[dev].load(std::memory_order_acquire);
+  if (n > 0) return n;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2; attr.val.clusterDim.y = 1; attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (set_smem_attr(dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = num_sms / 2;
   }
-  return g_max_clusters[dev];
+  g_max_clusters[dev].store(n, std::memory_order_release);
+  return n;
 }
 
 cudaError_t tensor_map_encoder(TensorMapEncodeFn* fn) {
@@ -1024,17 +1147,22 @@ cudaError_t tensor_map_encoder(TensorMapEncodeFn* fn) {
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
-  if ((long long)a.num_blocks * kPage >= (1LL << 31)) return cudaErrorInvalidValue;
-  CUtensorMap tm_pool, tm_o, tm_ws;
-  e = make_map(&tm_pool, a.cache, (uint64_t)a.D, (uint64_t)a.num_blocks * kPage, 64, 64);
+  if ((long long)a.num_blocks * 8 >= (1LL << 31)) return cudaErrorInvalidValue;
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = set_smem_attr(dev);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tm_page, tm_vhalf, tm_o, tm_ws;
+  e = make_page_map(&tm_page, a.cache, a.num_blocks, 9);
+  if (e != cudaSuccess) return e;
+  e = make_page_map(&tm_vhalf, a.cache, a.num_blocks, 4);
   if (e != cudaSuccess) return e;
   // outputs and split parts: [rows, 512] fp32, written in 32 x 32 boxes
   const uint64_t rows = (uint64_t)a.T_q * a.H;
   e = make_map(&tm_o, a.o, (uint64_t)a.d_c, (uint64_t)a.B * rows, 32, 32, true);
   if (e != cudaSuccess) return e;
   e = make_map(&tm_ws, a.ws_o, (uint64_t)a.d_c, ((uint64_t)a.B * a.G + a.W) * a.SR, 32, 32, true);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * a.W);
@@ -1046,7 +1174,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   attr.val.clusterDim.x = 2; attr.val.clusterDim.y = 1; attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, a, tm_pool, tm_o, tm_ws);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, a, tm_page, tm_vhalf, tm_o, tm_ws);
 }
 
 }  // namespace mla

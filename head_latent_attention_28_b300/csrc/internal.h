@@ -25,6 +25,7 @@ cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s);
 bool tc_supported(int dtype, int H, int T_q, int d_c, int d_r);
 int tc_workers(int num_sms);
 int tc_item_cost(int rows);   // the split partition's item cost C for this kernel
+size_t tc_msg_bytes_per_worker();   // message ring per split worker, in the workspace
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
 
 // Rotary frequencies as turns per position, base^(-2j/d_r) / (2 pi), in

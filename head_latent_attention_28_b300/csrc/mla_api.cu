@@ -1,6 +1,7 @@
 // C ABI entry points: host-side argument checks, workspace carving, kernel
 // selection, the per-device error word.  Declarations and the contract of
 // each call are in include/mla.h.
+#include <atomic>
 #include <cmath>
 #include <mutex>
 #include <stdio.h>
@@ -21,11 +22,16 @@ int g_num_sms[kMaxDevices] = {};
 
 thread_local char g_last_cuda[256] = "";
 
+// test hook of mla_test_set_wait_fault (zero: off)
+std::atomic<int> g_test_skip_load{0};
+std::atomic<unsigned long long> g_test_wait_ns{0};
+
 // Scratch of mla_decode_paged_noalloc: the split workspace (merge metadata,
 // partial log-sum-exps and outputs) in a file-scope device array instead of
-// caller memory.  32 MiB holds e.g. B = 32 sequences of 128 query rows with
-// d_c = 512 at 74 split workers (27.9 MB); larger shapes are rejected.
-constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+// caller memory.  64 MiB holds e.g. B = 32 sequences of 128 query rows with
+// d_c = 512 at 74 split workers (49.6 MB: 27.9 MB of partials and 21.8 MB of
+// the tensor-core kernel's message rings); larger shapes are rejected.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
 __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 void* g_scratch_ptr[kMaxDevices] = {};
 
@@ -53,22 +59,28 @@ int note_cuda(cudaError_t e) {
   return MLA_ERR_CUDA;
 }
 
-// Device address of the error word and SM count of the current device.
+// Device address of the error word and SM count of the current device
+// (looked up once per device; later calls read them without the lock).
+std::atomic<bool> g_dev_ready[kMaxDevices];
+
 cudaError_t device_info(unsigned** err, int* sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_err_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_mla_error);
-    if (e != cudaSuccess) return e;
-    int n = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    g_num_sms[dev] = n;
-    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  if (!g_dev_ready[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_mla_error);
+      if (e != cudaSuccess) return e;
+      int n = 0;
+      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      g_num_sms[dev] = n;
+      g_err_ptr[dev] = static_cast<unsigned*>(p);
+    }
+    g_dev_ready[dev].store(true, std::memory_order_release);
   }
   if (err) *err = g_err_ptr[dev];
   if (sms) *sms = g_num_sms[dev];
@@ -125,6 +137,7 @@ const char* mla_status_string(int s) {
     case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace missing or too small";
     case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a device wait gave up";
     case MLA_ERR_BAD_INDEX: return "MLA_ERR_BAD_INDEX: block id or sequence length out of range";
+    case MLA_ERR_BAD_RECORD: return "MLA_ERR_BAD_RECORD: the merge found no consistent split record";
     default: return "unknown mla status";
   }
 }
@@ -144,6 +157,15 @@ int mla_check_status(void* stream) {
   }
   if (v & mla::kErrTimeout) return MLA_ERR_TIMEOUT;
   if (v & mla::kErrBadIndex) return MLA_ERR_BAD_INDEX;
+  if (v & mla::kErrBadRecord) return MLA_ERR_BAD_RECORD;
+  return MLA_OK;
+}
+
+int mla_test_set_wait_fault(int skip_load, unsigned wait_us) {
+  if (skip_load < 0) return MLA_ERR_INVALID_ARG;
+  g_test_skip_load.store(skip_load, std::memory_order_relaxed);
+  g_test_wait_ns.store(skip_load > 0 ? 1000ull * (wait_us ? wait_us : 1000u) : 0ull,
+                       std::memory_order_relaxed);
   return MLA_OK;
 }
 
@@ -207,7 +229,8 @@ size_t mla_decode_workspace_size(int B, int T_q, int H, int d_c, int d_r, int dt
   int G = 1, SR = 1;
   decode_row_groups(dtype, T_q, H, d_c, d_r, &G, &SR);
   if ((long long)B * G > (1 << 30)) return 0;
-  return mla::ws_layout(B * G, SR, d_c, W).total;
+  const size_t msg = mla::tc_supported(dtype, H, T_q, d_c, d_r) ? mla::tc_msg_bytes_per_worker() : 0;
+  return mla::ws_layout(B * G, SR, d_c, W, msg).total;
 }
 
 int mla_decode_split_plan(const int32_t* seqlens_host, int B, int T_q, int max_blocks_per_seq,
@@ -294,7 +317,7 @@ int decode_impl(int stage, const void* q_lat, const void* kv_cache, int dtype,
   a.item_cost = decode_item_cost(dtype, T_q, H, d_c, d_r);
   decode_row_groups(dtype, T_q, H, d_c, d_r, &a.G, &a.SR);
   if ((long long)B * a.G > (1 << 30)) return MLA_ERR_INVALID_ARG;
-  const mla::WsLayout L = mla::ws_layout(B * a.G, a.SR, d_c, a.W);
+  const mla::WsLayout L = mla::ws_layout(B * a.G, a.SR, d_c, a.W, tc ? mla::tc_msg_bytes_per_worker() : 0);
   if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   a.q = q_lat; a.cache = kv_cache; a.block_table = block_table; a.seqlens = seqlens;
@@ -305,6 +328,9 @@ int decode_impl(int stage, const void* q_lat, const void* kv_cache, int dtype,
   a.meta = reinterpret_cast<int2*>(ws + L.meta_off);
   a.ws_lse = reinterpret_cast<float*>(ws + L.lse_off);
   a.ws_o = reinterpret_cast<float*>(ws + L.o_off);
+  a.msg = reinterpret_cast<unsigned char*>(ws + L.msg_off);
+  a.skip_load = g_test_skip_load.load(std::memory_order_relaxed);
+  a.wait_ns = g_test_wait_ns.load(std::memory_order_relaxed);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (stage & kStagePartial) {
     e = tc ? mla::launch_decode_tc(a, s) : mla::launch_decode_generic(a, s);

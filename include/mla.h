@@ -61,6 +61,9 @@ extern "C" {
 #define MLA_ERR_WORKSPACE   4  /* workspace NULL or smaller than required     */
 #define MLA_ERR_TIMEOUT     5  /* a device wait gave up (bounded spin)        */
 #define MLA_ERR_BAD_INDEX   6  /* device saw a bad block id or sequence length */
+#define MLA_ERR_BAD_RECORD  7  /* the merge found split records that no partial
+                                  pass wrote (a partial pass that gave up, or
+                                  mla_decode_combine without its partial pass) */
 
 /* dtype codes */
 #define MLA_F32  0
@@ -182,8 +185,8 @@ int mla_decode_paged(const void* q_lat, const void* kv_cache, int dtype,
  *
  * Same arguments and results as mla_decode_paged, minus workspace and
  * workspace_bytes.  The split workspace lives in a file-scope device array
- * of this library, 32 MiB per device: shapes whose
- * mla_decode_workspace_size(...) exceeds 32 MiB are rejected with
+ * of this library, 64 MiB per device: shapes whose
+ * mla_decode_workspace_size(...) exceeds 64 MiB are rejected with
  * MLA_ERR_WORKSPACE (nothing launched).  The call allocates nothing (no
  * cudaMalloc, no library that allocates); nothing in the scratch has to
  * start at zero, because the partial pass writes every record the merge
@@ -431,10 +434,28 @@ const char* mla_last_cuda_error(void);
 
 /*
  * mla_check_status -- wait for `stream`, then read and clear the current
- * device's error word.  Returns MLA_OK, MLA_ERR_BAD_INDEX, MLA_ERR_TIMEOUT
- * (timeout wins if both were recorded) or MLA_ERR_CUDA.
+ * device's error word.  Returns MLA_OK, MLA_ERR_TIMEOUT, MLA_ERR_BAD_INDEX,
+ * MLA_ERR_BAD_RECORD (the first of these three that was recorded, in this
+ * order) or MLA_ERR_CUDA.
  */
 int mla_check_status(void* stream);
+
+/*
+ * mla_test_set_wait_fault -- test hook for the bounded device waits (no
+ * counterpart in the pages; failure detection of this library).
+ *   skip_load > 0: every later tensor-core decode launch (mla_decode_paged,
+ *     its partial stage, mla_decode_step, mla_decode_paged_noalloc) leaves
+ *     out the shared-memory load of the skip_load-th page of split worker 0,
+ *     and every bounded wait of the kernel gives up after wait_us
+ *     microseconds (1000 if 0) instead of 2 s.  The wait for the missing page
+ *     then runs out: the kernel records MLA_ERR_TIMEOUT, drains its copies
+ *     and MMAs, frees its tensor memory and returns, and mla_check_status
+ *     reports MLA_ERR_TIMEOUT.  Outputs of such a call are unspecified.
+ *   skip_load == 0: back to normal operation.
+ * Process-wide (all devices, all host threads).  Returns MLA_OK, or
+ * MLA_ERR_INVALID_ARG for skip_load < 0.
+ */
+int mla_test_set_wait_fault(int skip_load, unsigned wait_us);
 
 /* Library ABI version (major * 100 + minor). */
 int mla_version(void);

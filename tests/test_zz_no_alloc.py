@@ -16,7 +16,7 @@ import mla_inputs as mi
 
 pytestmark = pytest.mark.gpu
 
-SCRATCH_BYTES = 32 << 20
+SCRATCH_BYTES = 64 << 20
 
 
 def _inputs(spec):
