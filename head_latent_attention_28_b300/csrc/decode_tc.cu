@@ -12,37 +12,43 @@
 //
 // How (B300-specific).  One split worker is a cluster of two CTAs on two SMs.
 // The output accumulator (128 x 512 fp32) fills a whole SM's tensor memory,
-// and the score side needs the latent query (256 columns) and score buffers
-// in tensor memory, so the two halves of the work sit on different SMs:
+// and the score side needs the query (288 columns) and score buffers in
+// tensor memory, so the two halves of the work sit on different SMs:
 //  * CTA 0, the score CTA, loads each 64-token page with ONE 4-D TMA copy
-//    (72 KB; small boxes cost a fixed ~0.2-0.4 us each on this part, so nine
-//    8 KB boxes per page could not keep up with HBM) into a ring of three
-//    page slots, and keeps a few pages ahead in L2 with bulk prefetches.  The
-//    4-D box lays a page out as [8-token group][64-dim chunk][8 tokens][64
-//    dims] with 128-byte swizzle, so each (group, chunk) is one 1 KB
-//    swizzle atom and an MMA operand over the page's 64 tokens is a uniform
-//    stride of 9 KB.  Scores S = Q . C^T (M = 128 rows, N = 64 tokens,
-//    K = 576) go into one of two tensor-memory buffers; the whole query (512
-//    latent + 64 rotary dims) is the A operand in tensor memory.  Eight
-//    softmax warps (two per 32-row quarter, 32 tokens each) run a base-2
-//    online softmax with a lazy running max (the output is rescaled only
-//    when a row max grows by more than 2^8; exact after the final division)
-//    and round the probabilities to bf16.  Each page's probabilities, per-row
-//    rescale factors and a header are written straight from registers into
-//    this worker's message ring in global memory (L2), in the swizzled layout
-//    the value CTA's MMA reads; a heavy page (a probability not small
-//    against its row's running sum) also sends the low bf16 parts.  The
-//    message's flags go to the value CTA with one remote store and an
-//    mbarrier arrive (release at cluster scope).
-//  * CTA 1, the value CTA, keeps the 128 x 512 fp32 output in tensor memory,
-//    loads the 512 latent dims of the same pages (an L2 hit) as two 32 KB
-//    4-D boxes per page into a ring of four, loads each page's message (one
-//    or two 18 KB units) into a ring of four shared-memory units, and
-//    accumulates O += P . V with tcgen05.mma (A = P from shared memory, B = V
-//    MN-major, N = 256).  Four warps apply row rescales and zero the rows of
-//    a last page past the sequence end (0 x NaN would poison O); eight warps
-//    write the normalised output with TMA tensor stores (or the split's
-//    partial output, merged later).
+//    (72 KB; every copy instruction costs a fixed ~0.3-0.5 us of the SM's
+//    copy engine on this part, so small boxes cannot keep up with HBM) into
+//    a ring of three page slots, and keeps three pages ahead in L2 with
+//    tensor prefetches.  The 4-D box lays a page out as [8-token group]
+//    [64-dim chunk][8 tokens][64 dims] with 128-byte swizzle, so each
+//    (group, chunk) is one 1 KB swizzle atom and an MMA operand over the
+//    page's 64 tokens is a uniform stride of 9 KB.  Scores S = Q . C^T
+//    (M = 128 rows, N = 64 tokens, K = 576: 36 MMAs issued from a rolled
+//    chunk loop, which keeps the issuing code small and resident in the
+//    instruction cache next to the softmax code) go into one of two
+//    tensor-memory buffers; the whole query is the A operand in tensor
+//    memory.  Two groups of four softmax warps take the even and the odd
+//    pages (one row per thread, all 64 tokens), run a base-2 online softmax
+//    with a lazy running max shared by the groups (the output is rescaled
+//    only when a row max grows by more than 2^8; exact after the final
+//    division) and round the probabilities to bf16.  Each page's
+//    probabilities and per-row info (reference max, sum of the rounded
+//    probabilities) are written from registers into this worker's message
+//    ring in global memory (L2), already in the swizzled layout the value
+//    CTA's MMA reads; a heavy page (a probability not small against its
+//    row's running sum) also sends the low bf16 parts.  A signaler warp sends
+//    the page's flags to the value CTA with one remote store and an mbarrier
+//    arrive (release at cluster scope).
+//  * CTA 1, the value CTA, keeps the 128 x 512 fp32 output in tensor memory.
+//    Its producer loads the 512 latent dims of the same pages (one 64 KB box
+//    per page, an L2 hit: the score CTA's copy marks them evict-last) into a
+//    ring of two, and copies each page's message with one or two bulk copies
+//    into a ring of three probability units and two low-part buffers.  The
+//    MMA warp accumulates O += P . V (A = P from shared memory, B = V
+//    MN-major, N = 256).  Four row warps zero the low parts of row quarters
+//    that sent none, apply row rescales, keep the row sums and zero the rows
+//    of a last page past the sequence end (0 x NaN would poison O); eight
+//    warps write the normalised output with TMA tensor stores (or the
+//    split's partial output, merged later).
 //  * Each worker takes a contiguous range of the cost-weighted split
 //    partition (common.cuh): work items are (sequence, row group, page
 //    range), planned on the device in batches of up to 32.
@@ -70,43 +76,43 @@ constexpr int kThreads = 352;            // 11 warps
 constexpr int kRows = 128;               // query rows per work item (one row group)
 constexpr int kPageBytes = kPage * 576 * 2;   // 73,728: one page, [tg 8][chunk 9][8][64]
 constexpr int kSlots = 3;                // score CTA: page ring
-constexpr int kVHalf = 32768;            // value CTA: 256 latent dims of a page, [tg 8][chunk 4][8][64]
-constexpr int kVSlots = 4;               // value CTA: ring of half pages
+constexpr int kVBytes = 65536;           // value CTA: the 512 latent dims of a page, [tg 8][chunk 8][8][64]
+constexpr int kVSlots = 2;               // value CTA: ring of pages
 constexpr int kPBytes = kRows * 64 * 2;  // bf16 probabilities of one page (K-major, SW128)
-constexpr int kInfoBytes = 16 + kRows * 8;       // header + (alpha, l) per row
-constexpr int kPMsgBytes = kPBytes + kInfoBytes; // bytes loaded per unit
-constexpr int kPUnitBytes = 18432;       // a message unit (in global memory and shared memory)
-constexpr int kPUnits = 4;               // value CTA: shared-memory units
-constexpr int kGSlots = 8;               // message ring: page slots per worker (hi and lo unit each)
+constexpr int kInfoBytes = kRows * 8;    // per row: the reference max of the page's probabilities and their sum
+constexpr int kHiBytes = kPBytes + kInfoBytes;   // 17,408: probabilities + row info
+constexpr int kHiUnits = 3;              // value CTA: units for the probabilities (page g in g % 3)
+constexpr int kLoBufs = 2;               // value CTA: buffers for low parts (heavy pages)
+constexpr int kMsgBytes = kHiBytes + kPBytes;    // a page's message: hi unit, then low parts
+constexpr int kGSlots = 8;               // message ring: page slots per worker
 constexpr int kPrefetch = 3;             // pages kept ahead in L2
 constexpr int kOffV = 0;
-constexpr int kOffP = kVSlots * kVHalf;
+constexpr int kOffHi = kVSlots * kVBytes;
+constexpr int kOffLo = kOffHi + kHiUnits * kHiBytes;
 constexpr int kScoreSmem = kSlots * kPageBytes;
-constexpr int kValueSmem = kOffP + kPUnits * kPUnitBytes;
+constexpr int kValueSmem = kOffLo + kLoBufs * kPBytes;
 constexpr int kSmemBytes = (kScoreSmem > kValueSmem ? kScoreSmem : kValueSmem) + 1024;
 constexpr int kMaxItems = 32;            // work items planned per batch
 // TMEM columns (score CTA): latent query [0, 256), rotary query [256, 288),
-// score buffers [384, 448) and [448, 512)
+// score buffers [384, 448) (even pages) and [448, 512) (odd pages)
 constexpr uint32_t kTmemQr = 256;
 constexpr uint32_t kTmemS = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
-// header flag bits of a page message
-constexpr uint32_t kFlagRescale = 1u;    // rows rescaled before this page's value MMA
-constexpr uint32_t kFlagLo = 2u;         // the low bf16 parts of the probabilities follow
+// message flags: the page has low parts (bit 1); bit 4 + q: row quarter q
+// wrote them (the other quarters' low parts are zero)
+constexpr uint32_t kFlagLo = 2u;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-static_assert(kPMsgBytes <= kPUnitBytes, "message unit too small");
-static_assert(kPMsgBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
-static_assert(kPageBytes % 1024 == 0 && kVHalf % 1024 == 0, "SW128 operands need 1 KB alignment");
-static_assert(kOffP % 1024 == 0 && kPUnitBytes % 1024 == 0, "SW128 operands need 1 KB alignment");
-static_assert(8 * 2048 <= kPBytes, "epilogue staging lives in a probability unit");
+static_assert(kPageBytes % 1024 == 0 && kVBytes % 1024 == 0, "SW128 operands need 1 KB alignment");
+static_assert(kOffHi % 1024 == 0 && kHiBytes % 1024 == 0 && kOffLo % 1024 == 0, "SW128 operands need 1 KB alignment");
+static_assert(4 * 4096 <= kPBytes, "epilogue staging: four warps' boxes in a probability area");
 static_assert(kPrefetch < 32, "the prefetch cursor looks at most one block-id chunk ahead");
 
 }  // namespace
 
-size_t tc_msg_bytes_per_worker() { return (size_t)kGSlots * 2 * kPUnitBytes; }
+size_t tc_msg_bytes_per_worker() { return (size_t)kGSlots * kMsgBytes; }
 
 namespace {
 
@@ -120,38 +126,40 @@ struct Item {
 struct SmemCtl {
   // score CTA
   uint64_t slot_full[kSlots], slot_empty[kSlots];
-  uint64_t s_full[2], s_free[2];
+  uint64_t s_full[2], s_free[2];   // score buffer of even / odd pages
   uint64_t q_ready;
   uint64_t q_free;             // the scores of an item are complete: its query may be overwritten
-  uint64_t gfree[kGSlots];     // a message slot may be rewritten (value CTA arrives)
-  uint64_t written[8];         // the softmax warps wrote page g's message ([g % 8], count 4)
+  uint64_t gfree[kGSlots];     // a message slot may be rewritten (the value CTA's copies of it landed)
+  uint64_t written[8];         // a softmax group wrote page g's message ([g % 8], count 4)
   // value CTA
   uint64_t v_full[kVSlots], v_empty[kVSlots];
-  uint64_t p_ready[kGSlots];   // the score CTA wrote a page's message (remote arrive)
-  uint64_t p_recv[kPUnits];    // a unit's bytes arrived in shared memory
-  uint64_t unit_free[kPUnits]; // a unit may be reloaded
-  uint64_t pv_done[kPUnits];   // value MMAs of the page whose first unit sits here completed
-  uint64_t rows_seen[kPUnits]; // all row warps have read the header and factors in a unit
-  uint64_t resc_done, vz_done;
+  uint64_t p_ready[kGSlots];   // the score CTA wrote page g's message (remote arrive)
+  uint64_t msg_full[kHiUnits]; // page g's message copied into unit g % 3 (and a low-part buffer)
+  uint64_t vready[8];          // page g's probabilities are in shared memory, rescale and tail done
+  uint64_t pv_done[8];         // value MMAs of page g completed
   uint64_t o_free;          // the epilogue has read O: the next item may overwrite it
   uint64_t epi_go;          // O of the item is final (value row warps -> other warps)
-  uint64_t epi_done;        // all epilogue warps are done with the staging units
+  uint64_t epi_done;        // all epilogue warps are done with the staging areas
   // both
   uint64_t mma_final;
-  uint32_t pflag_in[kGSlots];  // value CTA: header flags of a page (remote store by the score CTA)
+  uint32_t pflag_in[kGSlots];  // value CTA: flags of a page (remote store by the score CTA)
+  uint32_t uflag[8];           // value CTA: flags of page g at [g % 8], bit 8 its low-part buffer (producer -> row warps, MMA)
   uint32_t tmem_base;
   int abort;
   int never;                // stays 0: abort flag for the final drain waits
   int n_batch, n_total, n_flat;
   int scan[kThreads / 32];
   int item_flat[kMaxItems + 1];   // first page (in the batch's page order) of each item
-  // score CTA: header flags of page g at [g % 8], gathered with atomicOr; a
-  // word is read and reset by the signaler after the page's `written`
-  // barrier and written again eight pages later
+  // score CTA: flags of page g at [g % 8], gathered with atomicOr; a word is
+  // read and reset by the signaler after the page's `written` barrier and
+  // written again eight pages later
   uint32_t pflags[8];
-  uint32_t uflags[kPUnits];    // value CTA: header flags of the page loaded into a unit
+  // score CTA: the reference max of each row shared by the two softmax
+  // groups, tagged with the item it belongs to: (tag << 32) | float bits
+  unsigned long long mref[kRows];
   float lrow[kRows];           // value CTA: row sums of an item (row warps -> epilogue warps)
-  uint32_t epi_unit;        // value CTA: first unit of the item's last page (for the epilogue)
+  uint32_t epi_lo;             // value CTA: low-part buffer of the item's last page (epilogue staging)
+  uint32_t epi_count;          // value CTA: items whose epilogue no longer uses its staging buffers
   Item items[kMaxItems];
 };
 
@@ -280,6 +288,19 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity
   return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, abort, budget));
 }
 
+// wait until a counter in shared memory reaches v (bounded like the barrier waits)
+__device__ __forceinline__ bool wait_count(const volatile uint32_t* c, uint32_t v, volatile int* abort,
+                                           uint64_t budget) {
+  if (*c >= v) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (*c >= v) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > budget) return false;
+    __nanosleep(32);
+  }
+}
+
 __device__ __forceinline__ uint32_t lo_half_f(uint32_t u) { return u << 16; }
 __device__ __forceinline__ uint32_t hi_half_f(uint32_t u) { return u & 0xffff0000u; }
 
@@ -331,21 +352,20 @@ __device__ __forceinline__ void load_query_row(const DecodeArgs& a, const Item& 
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page,
-                 const __grid_constant__ CUtensorMap tm_vhalf, const __grid_constant__ CUtensorMap tm_o,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                  const __grid_constant__ CUtensorMap tm_ws) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ SmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* pslots = smem + kOffP;                  // value CTA: probability units
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();         // 0: score CTA, 1: value CTA
   const int w = (int)cluster_id_x();
   volatile int* abort_flag = &ctl.abort;
   const uint64_t wait_ns = a.wait_ns ? a.wait_ns : kWaitNs;
-  // this worker's message ring: page slot s holds a hi unit and a lo unit
-  unsigned char* gmsg = a.msg + (size_t)w * kGSlots * 2 * kPUnitBytes;
+  // this worker's message ring: page g in slot g % kGSlots
+  unsigned char* gmsg = a.msg + (size_t)w * kGSlots * kMsgBytes;
 
   if (threadIdx.x == 0) {
     ctl.abort = 0;
@@ -367,27 +387,26 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
       mbar_init(&ctl.v_full[i], 1);
       mbar_init(&ctl.v_empty[i], 1);
     }
-    for (int i = 0; i < kPUnits; ++i) {
-      mbar_init(&ctl.p_recv[i], 1);
-      mbar_init(&ctl.unit_free[i], 1);
+    for (int i = 0; i < kHiUnits; ++i) mbar_init(&ctl.msg_full[i], 1);
+    ctl.epi_count = 0;
+    for (int i = 0; i < 8; ++i) {
+      mbar_init(&ctl.written[i], 4);
+      mbar_init(&ctl.vready[i], 4);
       mbar_init(&ctl.pv_done[i], 1);
-      mbar_init(&ctl.rows_seen[i], 4);
+      ctl.pflags[i] = 0;
     }
-    for (int i = 0; i < 8; ++i) ctl.pflags[i] = 0;
+    for (int i = 0; i < kRows; ++i) ctl.mref[i] = 0ull;
     mbar_init(&ctl.q_ready, 8);
     mbar_init(&ctl.q_free, 1);
-    mbar_init(&ctl.resc_done, 4);
-    mbar_init(&ctl.vz_done, 4);
     mbar_init(&ctl.o_free, 8);
     mbar_init(&ctl.epi_go, 4);
     mbar_init(&ctl.epi_done, 8);
-    for (int i = 0; i < 8; ++i) mbar_init(&ctl.written[i], 4);
     mbar_init(&ctl.mma_final, 1);
     fence_mbar_init_cluster();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_page);
-    tma_prefetch_desc(&tm_vhalf);
+    tma_prefetch_desc(&tm_v);
   }
   if (warp == 1) tmem_alloc(&ctl.tmem_base, 512);
   tc_fence_before();
@@ -403,21 +422,17 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
                                   // always run 128 rows, the rest are zero padding)
   const int cap = a.max_blocks * kPage;
 
-  uint32_t g_prod = 0;                 // producer: pages walked (loads of both CTAs)
-  uint32_t g_issue = 0;                // producer: score CTA: 1 + last page loaded; value CTA: halves loaded
-  uint32_t g_page = 0;                 // pages (score MMA and softmax, value MMA and warps)
-  uint32_t g_load = 0;                 // value message loader: pages
-  uint32_t un_l = 0;                   // value message loader: units loaded
+  uint32_t g_prod = 0;                 // producer: pages walked
+  uint32_t g_issue = 0;                // producer: score CTA: 1 + last page loaded; value CTA: pages loaded
+  uint32_t g_page = 0;                 // pages (MMA issuers, softmax, value warps)
   uint32_t g_sig = 0;                  // score signaler: pages signalled
-  uint32_t it_cnt = 0;                 // items (MMA issuers, value warps)
-  uint32_t n_resc = 0, n_vz = 0;
-  // probability-unit counters: they run on across planning batches, like the
-  // mbarrier phases they index
-  uint32_t un = 0;                     // value MMA: units consumed
-  // value row warps: units seen, and per unit slot the parity of the next
-  // phase of its page barriers (pv_done, rows_seen advance only when the slot
-  // holds a page's first unit)
-  uint32_t un_v = 0, pvpar = 0, prev_slot = 0, prev_par = 0;
+  uint32_t it_cnt = 0;                 // items (MMA issuers, softmax, value warps)
+  // value producer: messages copied, low-part pages copied, items walked;
+  // per probability unit and low-part buffer the item (+1) whose epilogue
+  // stages in it (0: none), and per low-part buffer its last page
+  uint32_t g_msg = 0, n_lo = 0, p_items = 0;
+  uint32_t hi_epi[kHiUnits] = {0u, 0u, 0u};
+  uint32_t lo_epi[kLoBufs] = {0u, 0u}, lo_occ[kLoBufs] = {0xffffffffu, 0xffffffffu};
 
   for (int offset = 0;; offset += kMaxItems) {
     plan_batch(a, w, offset, &ctl);
@@ -428,9 +443,11 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
       // ============================================================ producer
       // The whole warp walks the batch's pages in order; lane k holds the
       // block ids of pages 32c + k of the current chunk c and of the next one
-      // (loaded a chunk ahead), lane 0 issues the copies.
+      // (loaded a chunk ahead), lane 0 issues the copies: one per page.
       const int total = ctl.n_flat;
-      const uint64_t pol = policy_evict_first();
+      // the score CTA's page copies stay in L2 for the value CTA's copy of the
+      // same latents, which is their last use
+      const uint64_t pol = rank == 0 ? policy_evict_last() : policy_evict_first();
       int cur = lane < total ? block_of(a, &ctl, n_items, lane) : -1;
       int nxt = 32 + lane < total ? block_of(a, &ctl, n_items, 32 + lane) : -1;
       if (rank == 0) {
@@ -439,8 +456,10 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
           if (lane == 0 && bp >= 0 && bp < a.num_blocks) tma_prefetch_l2_4d(&tm_page, 0, 0, 0, bp * 8);
         }
       }
+      int ip = 0;                          // item of page f
       for (int f = 0; f < total; ++f) {
         if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        while (ip + 1 < n_items && ctl.item_flat[ip + 1] <= f) ++ip;
         if ((f & 31) == 0 && f > 0) {
           cur = nxt;
           nxt = f + 32 + lane < total ? block_of(a, &ctl, n_items, f + 32 + lane) : -1;
@@ -465,22 +484,62 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
               g_issue = g_prod + 1;
             }
           } else {
-            for (int nh = 0; nh < 2; ++nh) {
-              const uint32_t u = 2 * g_prod + nh, vs = u % kVSlots;
-              if (u >= (uint32_t)kVSlots &&
-                  !mbar_wait(&ctl.v_empty[vs], ((u / kVSlots) - 1) & 1, abort_flag, wait_ns)) {
-                fail(&ctl, a.err);
-                break;
-              }
-              mbar_arrive_expect_tx(&ctl.v_full[vs], kVHalf);
-              tma_load_4d(smem + kOffV + vs * kVHalf, &tm_vhalf, &ctl.v_full[vs], 0, 0, 4 * nh, y, pol);
+            const uint32_t g = g_prod, vs = g % kVSlots;
+            bool ok2 = g < (uint32_t)kVSlots ||
+                       mbar_wait(&ctl.v_empty[vs], ((g / kVSlots) - 1) & 1, abort_flag, wait_ns);
+            if (ok2) {
+              mbar_arrive_expect_tx(&ctl.v_full[vs], kVBytes);
+              tma_load_4d(smem + kOffV + vs * kVBytes, &tm_v, &ctl.v_full[vs], 0, 0, 0, y, pol);
               ++g_issue;
+            }
+            // page g's message: probabilities and row info into unit g % 3,
+            // low parts (if any) into the next low-part buffer.  The unit was
+            // last read by page g - 3's value MMAs; a unit or buffer that
+            // held an item's last page is the staging area of its epilogue.
+            const uint32_t gs = g % kGSlots, u = g % kHiUnits;
+            const uint32_t K = p_items + (uint32_t)ip;
+            const bool last_in_item = f + 1 == ctl.item_flat[ip + 1];
+            if (ok2) ok2 = mbar_wait_cluster(&ctl.p_ready[gs], (g / kGSlots) & 1, abort_flag, wait_ns);
+            if (ok2 && g >= (uint32_t)kHiUnits)
+              ok2 = mbar_wait(&ctl.pv_done[(g - kHiUnits) & 7], ((g - kHiUnits) >> 3) & 1, abort_flag, wait_ns);
+            if (ok2 && hi_epi[u]) ok2 = wait_count(&ctl.epi_count, hi_epi[u], abort_flag, wait_ns);
+            const uint32_t fl = *reinterpret_cast<volatile uint32_t*>(&ctl.pflag_in[gs]);
+            const bool lo = (fl & kFlagLo) != 0;
+            const uint32_t lb = n_lo % kLoBufs;
+            if (ok2 && lo) {
+              // the buffer's last page: pages up to g - 3 are known to be done;
+              // a more recent one is waited for here (the pv_done ring is
+              // indexed by page, so an old page must not be waited for by parity)
+              const uint32_t occ = lo_occ[lb];
+              if (occ != 0xffffffffu && occ + kHiUnits > g)
+                ok2 = mbar_wait(&ctl.pv_done[occ & 7], (occ >> 3) & 1, abort_flag, wait_ns);
+              if (ok2 && lo_epi[lb]) ok2 = wait_count(&ctl.epi_count, lo_epi[lb], abort_flag, wait_ns);
+            }
+            if (!ok2) {
+              fail(&ctl, a.err);
+            } else {
+              ctl.uflag[g & 7] = fl | (lb << 8);
+              // the score CTA's writes of the message, acquired above, before
+              // the bulk copies read them
+              fence_proxy_async_global();
+              const unsigned char* src = gmsg + (size_t)gs * kMsgBytes;
+              mbar_arrive_expect_tx(&ctl.msg_full[u], kHiBytes + (lo ? kPBytes : 0));
+              bulk_load_g2s(smem + kOffHi + u * kHiBytes, src, kHiBytes, &ctl.msg_full[u]);
+              if (lo) bulk_load_g2s(smem + kOffLo + lb * kPBytes, src + kHiBytes, kPBytes, &ctl.msg_full[u]);
+              hi_epi[u] = last_in_item ? K + 1 : 0u;
+              if (lo) {
+                lo_occ[lb] = g;
+                lo_epi[lb] = last_in_item ? K + 1 : 0u;
+                ++n_lo;
+              }
+              ++g_msg;
             }
           }
         }
         ++g_prod;
         __syncwarp();
       }
+      p_items += (uint32_t)n_items;
     } else if (warp == 1) {
       // ============================================================ MMA issuer
       if (lane == 0) {
@@ -501,7 +560,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
               // apart); chunk c starts 1 KB further, a K-step of 16 dims 32 B
               const uint64_t b0 = sdesc_sw128(smem_u32(smem + sl * kPageBytes), 16, 9216);
               const uint32_t d = tmem + kTmemS + 64 * sb;
-#pragma unroll
+#pragma unroll 1
               for (int c = 0; c < 9; ++c)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
@@ -517,59 +576,37 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
           g_page = g;
         } else {
           const uint32_t idPV = idesc_bf16_f32(128, 256, 0, 1);
-          const uint32_t peer_gfree = mapa(smem_u32(&ctl.gfree[0]), 0);   // + 8 * slot
           for (int ii = 0; ii < n_items && !*abort_flag; ++ii) {
             const Item it = ctl.items[ii];
-            const int L = a.seqlens[it.b];
-            const int Pb = pages_of(L, a.T_q, cap);
             // the previous item's epilogue must have read O before it is overwritten
             bool ok = it_cnt == 0 || mbar_wait(&ctl.o_free, (it_cnt - 1) & 1, abort_flag, wait_ns);
             for (int i = 0; ok && i < it.j1 - it.j0; ++i) {
-              const uint32_t g = g_page + i, slot = un % kPUnits;
-              const int j = it.j0 + i;
-              ok = mbar_wait(&ctl.p_recv[slot], (un / kPUnits) & 1, abort_flag, wait_ns);
+              const uint32_t g = g_page + i, vs = g % kVSlots;
+              ok = mbar_wait(&ctl.vready[g & 7], (g >> 3) & 1, abort_flag, wait_ns);
+              if (ok) ok = mbar_wait(&ctl.v_full[vs], (g / kVSlots) & 1, abort_flag, wait_ns);
               if (!ok) break;
-              const uint8_t* ps = pslots + slot * kPUnitBytes;
-              const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(&ctl.uflags[slot]);
+              tc_fence_after();
+              const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(&ctl.uflag[g & 7]);
               const bool lo = (flags & kFlagLo) != 0;
-              const uint8_t* pl = pslots + ((un + 1) % kPUnits) * kPUnitBytes;   // low parts' unit
-              if (lo) ok = mbar_wait(&ctl.p_recv[(un + 1) % kPUnits], ((un + 1) / kPUnits) & 1, abort_flag, wait_ns);
-              if (!ok) break;
-              // the page's message slot in global memory has been read: the
-              // score CTA may write it again
-              mbar_arrive_remote(peer_gfree + 8 * (g % kGSlots));
-              if ((flags & kFlagRescale) && i > 0) {          // rows rescaled by the value warps
-                ok = mbar_wait(&ctl.resc_done, n_resc & 1, abort_flag, wait_ns);
-                ++n_resc;
-              }
-              if (ok && j == Pb - 1 && (L & (kPage - 1)) != 0) {   // tail rows zeroed
-                ok = mbar_wait(&ctl.vz_done, n_vz & 1, abort_flag, wait_ns);
-                ++n_vz;
-              }
-              for (int nh = 0; ok && nh < 2; ++nh) {
-                const uint32_t u = 2 * g + nh, vs = u % kVSlots;
-                ok = mbar_wait(&ctl.v_full[vs], (u / kVSlots) & 1, abort_flag, wait_ns);
-                if (!ok) break;
-                tc_fence_after();
-                // B = V (MN-major SW128): 64-dim chunks 1 KB apart along N,
-                // 8-token groups 4 KB apart along K; a K-step is 16 tokens
-                const uint64_t bv = sdesc_sw128(smem_u32(smem + kOffV + vs * kVHalf), 1024, 4096);
-                const uint64_t ah = sdesc_sw128(smem_u32(ps), 16, 1024);
+              // B = V (MN-major SW128): 64-dim chunks 1 KB apart along N,
+              // 8-token groups 8 KB apart along K; a K-step is 16 tokens
+              const uint64_t bv = sdesc_sw128(smem_u32(smem + kOffV + vs * kVBytes), 1024, 8192);
+              const uint64_t ah = sdesc_sw128(smem_u32(smem + kOffHi + (g % kHiUnits) * kHiBytes), 16, 1024);
+              const uint64_t al = sdesc_sw128(smem_u32(smem + kOffLo + ((flags >> 8) & 1u) * kPBytes), 16, 1024);
+#pragma unroll
+              for (int nh = 0; nh < 2; ++nh) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)   // 64 tokens, K-step 16
-                  mma_ss(tmem + nh * 256, ah + (uint64_t)(2 * kk), bv + (uint64_t)(512 * kk), idPV,
+                  mma_ss(tmem + nh * 256, ah + (uint64_t)(2 * kk), bv + (uint64_t)(1024 * kk + 256 * nh), idPV,
                          (i > 0 || kk > 0) ? 1u : 0u);
                 if (lo) {
-                  const uint64_t al = sdesc_sw128(smem_u32(pl), 16, 1024);
 #pragma unroll
                   for (int kk = 0; kk < 4; ++kk)   // the same V rows, A = low parts
-                    mma_ss(tmem + nh * 256, al + (uint64_t)(2 * kk), bv + (uint64_t)(512 * kk), idPV, 1u);
+                    mma_ss(tmem + nh * 256, al + (uint64_t)(2 * kk), bv + (uint64_t)(1024 * kk + 256 * nh), idPV, 1u);
                 }
-                mma_commit(&ctl.v_empty[vs]);
               }
-              if (!ok) break;
-              mma_commit(&ctl.pv_done[slot]);
-              un += lo ? 2 : 1;
+              mma_commit(&ctl.v_empty[vs]);
+              mma_commit(&ctl.pv_done[g & 7]);
             }
             if (!ok) { fail(&ctl, a.err); break; }
             g_page += it.j1 - it.j0;
@@ -578,13 +615,15 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
         }
       }
       __syncwarp();
-    } else if (rank == 0 && warp <= 5) {
+    } else if (rank == 0 && warp <= 9) {
       // ============================================================ softmax (score CTA)
-      // warp w owns TMEM lane quarter w & 3: rows 32 (w & 3) .. + 31, one row
-      // per thread over all 64 tokens of a page, so a row's running max and
-      // sum live in one thread and the four warps need no barrier among
-      // themselves; each arrives on the page's `written` barrier once its
-      // rows of the message are out
+      // Two groups of four warps: warps 2-5 take the even pages, warps 6-9
+      // the odd ones.  Warp w owns TMEM lane quarter w & 3 (rows 32 (w & 3)
+      // .. + 31), one row per thread over all 64 tokens of a page.  The
+      // groups share each row's reference max through `mref` (tagged with the
+      // item); a page's message carries the reference its probabilities are
+      // relative to, and the value CTA rescales when consecutive pages differ.
+      const int grp = warp >= 6 ? 1 : 0;
       const int q4 = warp & 3;
       const int r = 32 * q4 + lane;
       const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
@@ -598,23 +637,29 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
         // padding rows (r >= rows_g) see no token at all
         const int lim = r >= rows_g ? -1 : a.causal ? (L - a.T_q + t) : (L - 1);
         const int n = it.j1 - it.j0;
-        load_query_row(a, it, rows, tmem, lane_off, r, 0, &ctl.q_ready);
+        const uint32_t tag = it_cnt + 1;
+        // the previous item's scores, which read the query, are complete
+        // (one phase of q_free per item; a group is never more than one item
+        // ahead, because the scores of an item wait for its query)
+        if (it_cnt > 0 && !warp_wait(&ctl.q_free, (it_cnt - 1) & 1, abort_flag, wait_ns)) { fail(&ctl, a.err); break; }
+        load_query_row(a, it, rows, tmem, lane_off, r, grp, &ctl.q_ready);
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int k = 0; k < n; ++k) {
-          const uint32_t g = g_page + k, sb = g & 1, gs = g % kGSlots;
+          const uint32_t g = g_page + k, gs = g % kGSlots;
+          if ((int)(g & 1) != grp) continue;
           const int j = it.j0 + k;
           const bool last_page = k + 1 == n;
           const int bk = __ldg(a.block_table + (size_t)it.b * a.max_blocks + j);
           const bool page_ok = bk >= 0 && bk < a.num_blocks;
-          if (!warp_wait(&ctl.s_full[sb], (g >> 1) & 1, abort_flag, wait_ns)) { ok = false; break; }
+          if (!warp_wait(&ctl.s_full[grp], (g >> 1) & 1, abort_flag, wait_ns)) { ok = false; break; }
           tc_fence_after();
           float x[64];
-          tmem_ld64(tmem + lane_off + kTmemS + 64 * sb, x);
+          tmem_ld64(tmem + lane_off + kTmemS + 64 * grp, x);
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl.s_free[sb]);     // score buffer reusable
+          if (lane == 0) mbar_arrive(&ctl.s_free[grp]);     // score buffer reusable
           // mask (tokens past the visible range, a bad block id, padding rows)
           const int tok0 = j * kPage;
           if (!page_ok || tok0 + 63 > L - a.T_q || r >= rows_g) {
@@ -626,77 +671,74 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
 #pragma unroll
           for (int q = 1; q < 64; ++q) mx = fmaxf(mx, x[q]);
           const float m_page = mx * sl2;
-          const float m_new = fmaxf(m_run, m_page);
-          const bool need = m_new > m_run + kRescaleThreshold;
-          float alpha = 1.f;
-          if (need) {
-            alpha = ex2(m_run - m_new);     // 0 when m_run = -inf
+          // reference: the larger of this group's and the shared one; it moves
+          // only when the page max exceeds it by more than 2^8
+          const unsigned long long e = ctl.mref[r];
+          const float m_peer = (uint32_t)(e >> 32) == tag ? __uint_as_float((uint32_t)e) : -INFINITY;
+          const float m_cur = fmaxf(m_run, m_peer);
+          const float m_new = m_page > m_cur + kRescaleThreshold ? m_page : m_cur;
+          if (m_new != m_run) {
+            l_run = m_run == -INFINITY ? 0.f : l_run * ex2(m_run - m_new);
             m_run = m_new;
-            l_run *= alpha;
           }
-          // Precision of the bf16 probabilities: a page whose largest
-          // probability is not small against the row's sum so far also sends
-          // the low bf16 parts (p - bf16(p)).  The item's last page always
-          // sends them: its two units then give the value CTA's epilogue its
-          // staging space.
-          // (Every page's low parts are written, so that the flag may come
-          // from any of the four warps.)
+          if (m_run > m_peer) ctl.mref[r] = ((unsigned long long)tag << 32) | __float_as_uint(m_run);
+          // Precision of the bf16 probabilities: when a page's largest
+          // probability is not small against this group's sum for the row so
+          // far, the warp also sends the low bf16 parts (p - bf16(p)) of its
+          // rows.  The item's last page always sends them: its buffers then
+          // give the value CTA's epilogue its staging space.
           const bool lo = __any_sync(0xffffffffu, ex2(m_page - m_run) >= l_run) || last_page;
           // the page's message slot must have been read by the value CTA
           if (g >= (uint32_t)kGSlots &&
               !warp_wait_cluster(&ctl.gfree[gs], ((g / kGSlots) - 1) & 1, abort_flag, wait_ns)) { ok = false; break; }
-          unsigned char* msg = gmsg + (size_t)gs * 2 * kPUnitBytes;
+          unsigned char* msg = gmsg + (size_t)gs * kMsgBytes;
           {
-            // probabilities rounded to bf16, and the residuals rounded again
-            // (the low parts).  Rows are written in the layout the value
-            // CTA's MMA reads (K-major SW128: 16-byte chunk c of row r at
-            // c ^ (r & 7)).  The running sum here only guides the choice of
-            // the low parts; the value CTA sums what its MMAs use.
-            float psum = 0.f;
-            const float neg_m = -m_run;
+            // probabilities rounded to bf16 (and the residuals rounded again),
+            // rows in the layout the value CTA's MMA reads (K-major SW128:
+            // 16-byte chunk c of row r at c ^ (r & 7))
+            const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+            float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               uint32_t pk[4], pl[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float x0 = x[8 * c + 2 * e], x1 = x[8 * c + 2 * e + 1];
-                const float p0 = x0 == -INFINITY ? 0.f : ex2(fmaf(x0, sl2, neg_m));
-                const float p1 = x1 == -INFINITY ? 0.f : ex2(fmaf(x1, sl2, neg_m));
-                pk[e] = pack_bf16x2(p0, p1);
-                const float h0 = __uint_as_float(lo_half_f(pk[e])), h1 = __uint_as_float(hi_half_f(pk[e]));
-                psum += p0 + p1;
-                pl[e] = pack_bf16x2(p0 - h0, p1 - h1);
+              for (int e2 = 0; e2 < 4; ++e2) {
+                const float p0 = ex2(fmaf(x[8 * c + 2 * e2], sl2, neg_m));
+                const float p1 = ex2(fmaf(x[8 * c + 2 * e2 + 1], sl2, neg_m));
+                pk[e2] = pack_bf16x2(p0, p1);
+                // the row sum counts the rounded values the value MMA multiplies
+                const float h0 = __uint_as_float(lo_half_f(pk[e2])), h1 = __uint_as_float(hi_half_f(pk[e2]));
+                ps0 += h0;
+                ps1 += h1;
+                if (lo) {
+                  pl[e2] = pack_bf16x2(p0 - h0, p1 - h1);
+                  ps0 += __uint_as_float(lo_half_f(pl[e2]));
+                  ps1 += __uint_as_float(hi_half_f(pl[e2]));
+                }
               }
               const int off = r * 128 + ((c ^ (r & 7)) << 4);
               *reinterpret_cast<uint4*>(msg + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              *reinterpret_cast<uint4*>(msg + kPUnitBytes + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+              if (lo) *reinterpret_cast<uint4*>(msg + kHiBytes + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
             }
-            l_run += psum;
+            // row info: the reference max and the sum of this page's
+            // (rounded) probabilities
+            *reinterpret_cast<float2*>(msg + kPBytes + r * 8) = make_float2(m_run, ps0 + ps1);
+            l_run += ps0 + ps1;
           }
-          // per-row (alpha, m): the rescale factor that applies before this
-          // page's value MMA, and the reference max the page's
-          // probabilities are relative to (base 2, scaled)
-          *reinterpret_cast<float2*>(msg + kPBytes + 16 + r * 8) = make_float2(alpha, m_run);
-          fence_proxy_async_global();      // the value CTA reads the message with a bulk copy
-          // flags of the page (gathered from the four warps), then this
-          // warp's rows are out
-          const bool resc = __any_sync(0xffffffffu, need) && k > 0;
-          if (lane == 0) {
-            const uint32_t fl = (lo ? kFlagLo : 0u) | (resc ? kFlagRescale : 0u);
-            if (fl) atomicOr(&ctl.pflags[g & 7], fl);
-          }
+          if (lane == 0 && lo) atomicOr(&ctl.pflags[g & 7], kFlagLo | (16u << q4));
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl.written[g & 7]);
         }
         if (!ok) { fail(&ctl, a.err); break; }
         g_page += n;
+        ++it_cnt;
       }
     } else if (rank == 0 && warp == 10) {
       // ============================================================ signaler (score CTA)
-      // once the four softmax warps have written page g's message: its flags
-      // into the value CTA's shared memory, then an arrival at cluster scope
-      // there, which releases every write of the message (they happen before
-      // it through the `written` barrier)
+      // once a softmax group has written page g's message: its flags into
+      // the value CTA's shared memory, then an arrival at cluster scope there,
+      // which releases every write of the message (they happen before it
+      // through the `written` barrier)
       if (lane == 0) {
         const uint32_t peer_pready = mapa(smem_u32(&ctl.p_ready[0]), 1);   // + 8 * slot
         const uint32_t peer_pflag = mapa(smem_u32(&ctl.pflag_in[0]), 1);   // + 4 * slot
@@ -715,58 +757,12 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
         }
       }
       __syncwarp();
-    } else if (rank == 0) {
-      // score CTA warps 6-9: the second half of each item's query rows
-      const int q4 = warp & 3;
-      const int r = 32 * q4 + lane;
-      const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-      for (int ii = 0; ii < n_items; ++ii) {
-        if (__any_sync(0xffffffffu, *abort_flag)) break;
-        const Item it = ctl.items[ii];
-        // the previous item's scores, which read the query, are complete
-        // (one phase of q_free per item; these warps are never more than one
-        // item ahead, because the scores of an item wait for its query)
-        if (it_cnt > 0 && !warp_wait(&ctl.q_free, (it_cnt - 1) & 1, abort_flag, wait_ns)) { fail(&ctl, a.err); break; }
-        load_query_row(a, it, rows, tmem, lane_off, r, 1, &ctl.q_ready);
-        ++it_cnt;
-      }
-    } else if (warp == 10) {
-      // ============================================================ value CTA: message loader
-      // page g's message: one unit, or two when its flags say that the low
-      // parts follow; each goes to the next shared-memory unit once the value
-      // warps have freed it
-      if (lane == 0) {
-        const int total = ctl.n_flat;
-        for (int f = 0; f < total && !*abort_flag; ++f) {
-          const uint32_t g = g_load, gs = g % kGSlots;
-          if (!mbar_wait_cluster(&ctl.p_ready[gs], (g / kGSlots) & 1, abort_flag, wait_ns)) {
-            fail(&ctl, a.err);
-            break;
-          }
-          fence_proxy_async_global();
-          const uint32_t fl = *reinterpret_cast<volatile uint32_t*>(&ctl.pflag_in[gs]);
-          const unsigned char* msg = gmsg + (size_t)gs * 2 * kPUnitBytes;
-          bool ok = true;
-          for (uint32_t e = 0; e < ((fl & kFlagLo) ? 2u : 1u); ++e) {
-            const uint32_t su = un_l % kPUnits;
-            if (un_l >= (uint32_t)kPUnits &&
-                !mbar_wait(&ctl.unit_free[su], ((un_l / kPUnits) - 1) & 1, abort_flag, wait_ns)) {
-              ok = false;
-              break;
-            }
-            ctl.uflags[su] = fl;   // read by the value warps after the unit's bytes arrive
-            mbar_arrive_expect_tx(&ctl.p_recv[su], kPMsgBytes);
-            bulk_load_g2s(pslots + su * kPUnitBytes, msg + e * kPUnitBytes, kPMsgBytes, &ctl.p_recv[su]);
-            ++un_l;
-          }
-          if (!ok) { fail(&ctl, a.err); break; }
-          ++g_load;
-        }
-      }
-      __syncwarp();
-    } else {
+    } else if (rank == 1 && warp <= 9) {
       // ============================================================ value CTA warps
-      // warps 2-5 ("row warps"): page bookkeeping, row rescales, tail zeroing;
+      // warps 2-5 ("row warps", one row per thread): once a page's message
+      // is in shared memory, zero the low parts of the row quarters that sent
+      // none, rescale O rows when the reference max changes, zero the V rows
+      // of a last page past the sequence end, keep the row sums;
       // warps 2-9: the epilogue, warp w writing rows 32 (w & 3) .. + 31 and
       // output columns [256 * (w >= 6), + 256)
       const int q4 = warp & 3;
@@ -775,7 +771,8 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
       const int r = 32 * q4 + lane;
       const int tq = threadIdx.x - 64;             // 0..127 (row warps)
       const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-      float l_row = 0.f;                           // row warps: row r's running sum
+      const uint32_t peer_gfree = mapa(smem_u32(&ctl.gfree[0]), 0);   // + 8 * slot
+      float l_row = 0.f, m_prev = -INFINITY;
       for (int ii = 0; ii < n_items; ++ii) {
         if (__any_sync(0xffffffffu, *abort_flag)) break;
         const Item it = ctl.items[ii];
@@ -785,72 +782,38 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
         bool ok = true;
         if (row_warp) {
           for (int i = 0; i < n; ++i) {
-            const uint32_t g = g_page + i, slot = un_v % kPUnits;
+            const uint32_t g = g_page + i;
             const int j = it.j0 + i;
-            uint8_t* ps = pslots + slot * kPUnitBytes;
-            if (!warp_wait(&ctl.p_recv[slot], (un_v / kPUnits) & 1, abort_flag, wait_ns)) { ok = false; break; }
-            const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(&ctl.uflags[slot]);
-            const bool lo = (flags & kFlagLo) != 0;
-            const uint32_t par = (pvpar >> slot) & 1;
-            const float* info = reinterpret_cast<const float*>(ps + kPBytes + 16);
-            if (lo && !warp_wait(&ctl.p_recv[(un_v + 1) % kPUnits], ((un_v + 1) / kPUnits) & 1, abort_flag, wait_ns)) {
-              ok = false;
-              break;
-            }
-            {
-              // the row sum of exactly what the value MMAs use: the bf16
-              // probabilities of this row (and their low parts)
-              const float2 am = reinterpret_cast<const float2*>(info)[r];
-              float srow = 0.f;
-              for (uint32_t e = 0; e < (lo ? 2u : 1u); ++e) {
-                const uint4* prow = reinterpret_cast<const uint4*>(pslots + ((un_v + e) % kPUnits) * kPUnitBytes + r * 128);
+            const uint32_t u = g % kHiUnits;
+            if (!(ok = warp_wait(&ctl.msg_full[u], (g / kHiUnits) & 1, abort_flag, wait_ns))) break;
+            const uint32_t fl = *reinterpret_cast<const volatile uint32_t*>(&ctl.uflag[g & 7]);
+            const uint32_t lb = (fl >> 8) & 1u;
+            const float2 info = *reinterpret_cast<const float2*>(smem + kOffHi + u * kHiBytes + kPBytes + r * 8);
+            if ((fl & kFlagLo) && !(fl & (16u << q4))) {
+              // this row quarter sent no low parts: its rows of the buffer are zero
+              uint4* lz = reinterpret_cast<uint4*>(smem + kOffLo + lb * kPBytes + q4 * 4096);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                  const uint4 v = prow[c];
-                  srow += __uint_as_float(lo_half_f(v.x)) + __uint_as_float(hi_half_f(v.x)) +
-                          __uint_as_float(lo_half_f(v.y)) + __uint_as_float(hi_half_f(v.y)) +
-                          __uint_as_float(lo_half_f(v.z)) + __uint_as_float(hi_half_f(v.z)) +
-                          __uint_as_float(lo_half_f(v.w)) + __uint_as_float(hi_half_f(v.w));
-                }
-              }
-              l_row = (i == 0 ? 0.f : l_row * am.x) + srow;
-              if (i == n - 1) {
-                // the item's last page: lse (natural log), the merge record,
-                // and the row sum for the epilogue warps
-                ctl.lrow[r] = l_row;
-                const int rb = kRows * it.g;
-                if (r < min(kRows, rows - rb)) {
-                  const float lse = l_row > 0.f ? (am.y + __log2f(l_row)) * kLn2 : -INFINITY;
-                  if (it.flags & 1) { if (a.lse) a.lse[(size_t)it.b * rows + rb + r] = lse; }
-                  else a.ws_lse[(size_t)(it.vb + w) * a.SR + r] = lse;
-                  if (r == 0 && it.j0 == 0) a.meta[it.vb] = make_int2(it.w_first, it.w_last);
-                }
-              }
+              for (int c = 0; c < 8; ++c) lz[32 * c + lane] = make_uint4(0u, 0u, 0u, 0u);
+              fence_proxy_async_smem();    // the value MMA reads these bytes
             }
-            if (j == Pb - 1 && (L & (kPage - 1)) != 0) {
-              // last page: zero the V rows past the sequence end (they may hold NaN)
-              const int nv = L & (kPage - 1);
-              const int per_half = (kPage - nv) * 4 * 8;   // 16-byte pieces per half page
-              for (int nh = 0; nh < 2 && ok; ++nh) {
-                const uint32_t u = 2 * g + nh, vs = u % kVSlots;
-                if (!warp_wait(&ctl.v_full[vs], (u / kVSlots) & 1, abort_flag, wait_ns)) { ok = false; break; }
-                uint4* vp = reinterpret_cast<uint4*>(smem + kOffV + vs * kVHalf);
-                for (int q = tq; q < per_half; q += kRows) {
-                  const int tk = nv + q / 32, rem = q & 31;      // token, (chunk, piece)
-                  const int cc = rem >> 3, pc = rem & 7;
-                  vp[((tk >> 3) * 4096 + cc * 1024 + (tk & 7) * 128) / 16 + pc] = make_uint4(0, 0, 0, 0);
-                }
-              }
-              if (!ok) break;
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&ctl.vz_done);
+            __syncwarp();
+            // the copies of the message slot have landed: the score CTA may reuse it
+            if (q4 == 0 && lane == 0) mbar_arrive_remote_relaxed(peer_gfree + 8 * (g % kGSlots));
+            const float m_j = info.x, srow = info.y;
+            // rescale factor of this row: O and l hold pages < j relative to
+            // m_prev; this page's probabilities are relative to m_j
+            float alpha = 1.f;
+            if (i == 0) {
+              l_row = 0.f;
+              m_prev = m_j;
+            } else if (m_j != -INFINITY && m_j != m_prev) {
+              alpha = m_prev == -INFINITY ? 0.f : ex2(m_prev - m_j);
+              m_prev = m_j;
             }
-            if ((flags & kFlagRescale) && i > 0) {
-              // rescale O rows before this page's value MMA: O holds pages < j
-              if (!warp_wait(&ctl.pv_done[prev_slot], prev_par, abort_flag, wait_ns)) { ok = false; break; }
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+              // O rows rescaled before this page's value MMA: O holds pages < j
+              if (!(ok = warp_wait(&ctl.pv_done[(g - 1) & 7], ((g - 1) >> 3) & 1, abort_flag, wait_ns))) break;
               tc_fence_after();
-              const float alpha = info[2 * r];
 #pragma unroll 1
               for (int c = 0; c < 8; ++c) {
                 float o[64];
@@ -867,47 +830,56 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
               }
               tmem_st_wait();
               tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&ctl.resc_done);
             }
-            // header and factors read by this warp (one barrier per unit slot: a
-            // warp cannot reach the slot's next page before this unit is released)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.rows_seen[slot]);
-            // this page's value MMA done
-            if (!warp_wait(&ctl.pv_done[slot], par, abort_flag, wait_ns)) { ok = false; break; }
-            if (i < n - 1) {
-              // the page's units may be reloaded once every row warp is past its header
-              if (threadIdx.x == 64) {
-                if (mbar_wait(&ctl.rows_seen[slot], par, abort_flag, wait_ns)) {
-                  for (uint32_t e = 0; e < (lo ? 2u : 1u); ++e) mbar_arrive(&ctl.unit_free[(un_v + e) % kPUnits]);
-                } else {
-                  fail(&ctl, a.err);
-                }
+            l_row = l_row * alpha + srow;
+            if (j == Pb - 1 && (L & (kPage - 1)) != 0) {
+              // last page: zero the V rows past the sequence end (they may hold NaN)
+              const uint32_t vs = g % kVSlots;
+              if (!(ok = warp_wait(&ctl.v_full[vs], (g / kVSlots) & 1, abort_flag, wait_ns))) break;
+              const int nv = L & (kPage - 1);
+              const int pieces = (kPage - nv) * 8 * 8;      // 16-byte pieces: tokens x chunks x 8
+              uint4* vp = reinterpret_cast<uint4*>(smem + kOffV + vs * kVBytes);
+              for (int q = tq; q < pieces; q += kRows) {
+                const int tk = nv + q / 64, rem = q & 63;     // token, (chunk, piece)
+                const int cc = rem >> 3, pc = rem & 7;
+                vp[((tk >> 3) * 8192 + cc * 1024 + (tk & 7) * 128) / 16 + pc] = make_uint4(0, 0, 0, 0);
               }
-              __syncwarp();
-            } else {
-              // O is final; the last page's two units (it always carries low
-              // parts) become the epilogue staging and are handed back after it
-              if (threadIdx.x == 64) ctl.epi_unit = lo ? un_v : 0xffffffffu;
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&ctl.epi_go);
+              fence_proxy_async_smem();
             }
-            prev_slot = slot;
-            prev_par = par;
-            pvpar ^= 1u << slot;
-            un_v += lo ? 2 : 1;
+            if (i == n - 1) {
+              // the item's last page: lse (natural log), the merge record, and
+              // the row sum for the epilogue warps
+              ctl.lrow[r] = l_row;
+              const int rb = kRows * it.g;
+              if (r < min(kRows, rows - rb)) {
+                const float lse = l_row > 0.f ? (m_prev + __log2f(l_row)) * kLn2 : -INFINITY;
+                if (it.flags & 1) { if (a.lse) a.lse[(size_t)it.b * rows + rb + r] = lse; }
+                else a.ws_lse[(size_t)(it.vb + w) * a.SR + r] = lse;
+                if (r == 0 && it.j0 == 0) a.meta[it.vb] = make_int2(it.w_first, it.w_last);
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.vready[g & 7]);
+            if (i == n - 1) {
+              // O is final once the last page's value MMAs are done; the
+              // epilogue stages in this page's buffers
+              if (!(ok = warp_wait(&ctl.pv_done[g & 7], (g >> 3) & 1, abort_flag, wait_ns))) break;
+              if (lane == 0) {
+                if (q4 == 2) ctl.epi_lo = lb;
+                mbar_arrive(&ctl.epi_go);
+              }
+            }
           }
         }
         if (ok && !warp_wait(&ctl.epi_go, it_cnt & 1, abort_flag, wait_ns)) ok = false;
         if (!ok) { fail(&ctl, a.err); break; }
-        // ---- epilogue: normalise and write the item's 128 x 512 output, each
-        // warp staging 32 rows x 16 columns at a time for full-sector writes
+        // ---- epilogue: normalise and write the item's 128 x 512 output, staged
+        // in the last page's probability unit and low-part buffer (the last
+        // page always has low parts), each warp 32 rows x 16 columns at a time
         tc_fence_after();
-        const uint32_t eu = ctl.epi_unit;
-        if (eu == 0xffffffffu) { fail(&ctl, a.err); break; }   // cannot happen: the last page sends low parts
-        uint8_t* ps_last = pslots + (eu % kPUnits) * kPUnitBytes;
-        uint8_t* ps_lo = pslots + ((eu + 1) % kPUnits) * kPUnitBytes;
+        const uint32_t gl = g_page + n - 1;
+        uint8_t* ps_last = smem + kOffHi + (gl % kHiUnits) * kHiBytes;
+        uint8_t* ps_lo = smem + kOffLo + ctl.epi_lo * kPBytes;
         const float l_fin = ctl.lrow[r];
         const float inv = l_fin > 0.f ? 1.f / l_fin : 0.f;
         const bool whole = it.flags & 1;
@@ -916,15 +888,12 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
         float* out_base = (whole ? a.o + ((size_t)it.b * rows + rb) * a.d_c
                                  : a.ws_o + (size_t)(it.vb + w) * a.SR * a.d_c) + 256 * ch;
         if (grp_rows > 0) out_base += (size_t)(32 * q4) * a.d_c;
-        // every thread must have read l before the staging writes below
-        __syncwarp();
+        const int wi = warp - 2;
+        uint8_t* box = wi < 4 ? ps_last + wi * 4096 : ps_lo + (wi - 4) * 4096;   // this warp's 4 KB
         if (grp_rows == 32) {
-          // whole 32-row group: 32 x 32 fp32 boxes staged (SW128) in the
-          // units' probability areas (not their factors) and written by TMA
+          // whole 32-row group: 32 x 32 fp32 boxes staged (SW128) and written by TMA
           const CUtensorMap* tmo = whole ? &tm_o : &tm_ws;
           const int row0 = (whole ? it.b * rows + rb : (it.vb + w) * a.SR) + 32 * q4;
-          const int wi = warp - 2;
-          uint8_t* box = wi < 4 ? ps_last + wi * 4096 : ps_lo + (wi - 4) * 4096;
 #pragma unroll 1
           for (int c = 0; c < 8; ++c) {
             float o[32];
@@ -943,13 +912,10 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
               bulk_commit();
             }
           }
-          if (lane == 0) bulk_wait_read0();         // staging free before the units are handed back
+          if (lane == 0) bulk_wait_read0();         // staging free before it is reused
           __syncwarp();
         }
-        // a warp's own 4 KB of the two units (the same region its TMA boxes
-        // would use, so a partial group never overlaps another warp's box)
-        float4* stg = reinterpret_cast<float4*>((warp - 2) < 4 ? ps_last + (warp - 2) * 4096
-                                                                : ps_lo + (warp - 6) * 4096);   // 32 rows x 4 float4
+        float4* stg = reinterpret_cast<float4*>(box);   // 32 rows x 4 float4
 #pragma unroll 1
         for (int c = 0; c < (grp_rows > 0 && grp_rows < 32 ? 4 : 0); ++c) {
           float o[64];
@@ -979,15 +945,10 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
           mbar_arrive(&ctl.o_free);      // O may be overwritten now
           mbar_arrive(&ctl.epi_done);
         }
-        if (threadIdx.x == 64) {
-          // hand the staging units back once every epilogue warp is done with them
-          if (mbar_wait(&ctl.epi_done, it_cnt & 1, abort_flag, wait_ns)) {
-            for (uint32_t e = 0; e < 2; ++e) mbar_arrive(&ctl.unit_free[(eu + e) % kPUnits]);
-          } else {
-            fail(&ctl, a.err);
-          }
-        }
-        __syncwarp();
+        // the staging areas are reused by later pages: wait until every
+        // epilogue warp is done with them, then let the producer copy into them
+        if (!warp_wait(&ctl.epi_done, it_cnt & 1, abort_flag, wait_ns)) { fail(&ctl, a.err); break; }
+        if (warp == 2 && lane == 0) *reinterpret_cast<volatile uint32_t*>(&ctl.epi_count) = it_cnt + 1;
         g_page += n;
         ++it_cnt;
       }
@@ -1016,19 +977,16 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
           atomicOr(a.err, kErrTimeout);
       }
     } else {
-      const uint32_t nu = g_issue;
-      for (uint32_t k = 0; k < (uint32_t)kVSlots && k < nu; ++k) {
-        const uint32_t u = nu - 1 - k;
-        if (!mbar_wait(&ctl.v_full[u % kVSlots], (u / kVSlots) & 1, &ctl.never, wait_ns))
+      for (uint32_t k = 0; k < (uint32_t)kVSlots && k < g_issue; ++k) {
+        const uint32_t g = g_issue - 1 - k;
+        if (!mbar_wait(&ctl.v_full[g % kVSlots], (g / kVSlots) & 1, &ctl.never, wait_ns))
           atomicOr(a.err, kErrTimeout);
       }
-    }
-  }
-  if (rank == 1 && warp == 10 && lane == 0) {
-    for (uint32_t k = 0; k < (uint32_t)kPUnits && k < un_l; ++k) {
-      const uint32_t u = un_l - 1 - k;
-      if (!mbar_wait(&ctl.p_recv[u % kPUnits], (u / kPUnits) & 1, &ctl.never, wait_ns))
-        atomicOr(a.err, kErrTimeout);
+      for (uint32_t k = 0; k < (uint32_t)kHiUnits && k < g_msg; ++k) {
+        const uint32_t g = g_msg - 1 - k;
+        if (!mbar_wait(&ctl.msg_full[g % kHiUnits], (g / kHiUnits) & 1, &ctl.never, wait_ns))
+          atomicOr(a.err, kErrTimeout);
+      }
     }
   }
   tc_fence_before();
@@ -1153,10 +1111,10 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = set_smem_attr(dev);
   if (e != cudaSuccess) return e;
-  CUtensorMap tm_page, tm_vhalf, tm_o, tm_ws;
+  CUtensorMap tm_page, tm_v, tm_o, tm_ws;
   e = make_page_map(&tm_page, a.cache, a.num_blocks, 9);
   if (e != cudaSuccess) return e;
-  e = make_page_map(&tm_vhalf, a.cache, a.num_blocks, 4);
+  e = make_page_map(&tm_v, a.cache, a.num_blocks, 8);   // the 512 latent dims of a page
   if (e != cudaSuccess) return e;
   // outputs and split parts: [rows, 512] fp32, written in 32 x 32 boxes
   const uint64_t rows = (uint64_t)a.T_q * a.H;
@@ -1174,7 +1132,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   attr.val.clusterDim.x = 2; attr.val.clusterDim.y = 1; attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, a, tm_page, tm_vhalf, tm_o, tm_ws);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, a, tm_page, tm_v, tm_o, tm_ws);
 }
 
 }  // namespace mla
