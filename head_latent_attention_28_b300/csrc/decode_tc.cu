@@ -22,13 +22,17 @@
 //    [64-dim chunk][8 tokens][64 dims] with 128-byte swizzle, so each
 //    (group, chunk) is one 1 KB swizzle atom and an MMA operand over the
 //    page's 64 tokens is a uniform stride of 9 KB.  Scores S = Q . C^T
-//    (M = 128 rows, N = 64 tokens, K = 576: 36 MMAs issued from a rolled
-//    chunk loop, which keeps the issuing code small and resident in the
-//    instruction cache next to the softmax code) go into one of two
-//    tensor-memory buffers; the whole query is the A operand in tensor
-//    memory.  Two groups of four softmax warps take the even and the odd
-//    pages (one row per thread, all 64 tokens), run a base-2 online softmax
-//    with a lazy running max shared by the groups (the output is rescaled
+//    (M = 128 rows, K = 576) are computed for the pages of an item in pairs
+//    into two adjacent tensor-memory buffers: a pair in adjacent ring slots
+//    is one operand of 128 tokens (36 MMAs with N = 128, about 0.65 of the
+//    time of two N = 64 chains on this part), any other pair two N = 64
+//    chains sharing each A step, an odd last page one N = 64 chain.  The
+//    MMAs are issued from a rolled chunk loop, which keeps the issuing code
+//    small and resident in the instruction cache next to the softmax code.
+//    The whole query is the A operand in tensor memory.  Two groups of four
+//    softmax warps take the first and the second page of each pair (one
+//    row per thread, all 64 tokens), run a base-2 online softmax
+//    with a lazy running max passed from page to page (the output is rescaled
 //    only when a row max grows by more than 2^8; exact after the final
 //    division) and round the probabilities to bf16.  Each page's
 //    probabilities and per-row info (reference max, sum of the rounded
@@ -94,7 +98,7 @@ constexpr int kValueSmem = kOffLo + kLoBufs * kPBytes;
 constexpr int kSmemBytes = (kScoreSmem > kValueSmem ? kScoreSmem : kValueSmem) + 1024;
 constexpr int kMaxItems = 32;            // work items planned per batch
 // TMEM columns (score CTA): latent query [0, 256), rotary query [256, 288),
-// score buffers [384, 448) (even pages) and [448, 512) (odd pages)
+// score buffers [384, 448) (first page of a pair) and [448, 512) (second page)
 constexpr uint32_t kTmemQr = 256;
 constexpr uint32_t kTmemS = 384;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -126,7 +130,7 @@ struct Item {
 struct SmemCtl {
   // score CTA
   uint64_t slot_full[kSlots], slot_empty[kSlots];
-  uint64_t s_full[2], s_free[2];   // score buffer of even / odd pages
+  uint64_t s_full[2], s_free[2];   // score buffer of the first / second page of a pair
   uint64_t q_ready;
   uint64_t q_free;             // the scores of an item are complete: its query may be overwritten
   uint64_t gfree[kGSlots];     // a message slot may be rewritten (the value CTA's copies of it landed)
@@ -154,8 +158,8 @@ struct SmemCtl {
   // read and reset by the signaler after the page's `written` barrier and
   // written again eight pages later
   uint32_t pflags[8];
-  // score CTA: the reference max of each row shared by the two softmax
-  // groups, tagged with the item it belongs to: (tag << 32) | float bits
+  // score CTA: the reference max of each row for the latest page, passed
+  // between the two softmax groups: ((page index + 1) << 32) | float bits
   unsigned long long mref[kRows];
   float lrow[kRows];           // value CTA: row sums of an item (row warps -> epilogue warps)
   uint32_t epi_lo;             // value CTA: low-part buffer of the item's last page (epilogue staging)
@@ -286,6 +290,21 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort,
                                                   uint64_t budget) {
   return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, abort, budget));
+}
+
+// wait until the tag (high 32 bits) of a shared-memory word is `tag`; the
+// word is returned in *out (bounded like the barrier waits)
+__device__ __forceinline__ bool wait_tag(const volatile unsigned long long* p, uint32_t tag,
+                                         unsigned long long* out, volatile int* abort, uint64_t budget) {
+  unsigned long long e = *p;
+  if ((uint32_t)(e >> 32) == tag) { *out = e; return true; }
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    e = *p;
+    if ((uint32_t)(e >> 32) == tag) { *out = e; return true; }
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > budget) return false;
+  }
 }
 
 // wait until a counter in shared memory reaches v (bounded like the barrier waits)
@@ -426,6 +445,8 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
   uint32_t g_issue = 0;                // producer: score CTA: 1 + last page loaded; value CTA: pages loaded
   uint32_t g_page = 0;                 // pages (MMA issuers, softmax, value warps)
   uint32_t g_sig = 0;                  // score signaler: pages signalled
+  uint32_t s_use[2] = {0u, 0u};        // score MMA: times each score buffer was written
+  uint32_t s_seen = 0;                 // softmax group: pages of this group processed
   uint32_t it_cnt = 0;                 // items (MMA issuers, softmax, value warps)
   // value producer: messages copied, low-part pages copied, items walked;
   // per probability unit and low-part buffer the item (+1) whose epilogue
@@ -545,29 +566,65 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
       if (lane == 0) {
         if (rank == 0) {
           const uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);
+          const uint32_t idS2 = idesc_bf16_f32(128, 128, 0, 0);
           uint32_t g = g_page;
           for (int ii = 0; ii < n_items && !*abort_flag; ++ii) {
             const Item it = ctl.items[ii];
             const int n = it.j1 - it.j0;
             bool ok = mbar_wait(&ctl.q_ready, it_cnt & 1, abort_flag, wait_ns);
-            for (int k = 0; ok && k < n; ++k, ++g) {
-              const uint32_t sb = g & 1, sl = g % kSlots;
-              if (g >= 2) ok = mbar_wait(&ctl.s_free[sb], ((g >> 1) - 1) & 1, abort_flag, wait_ns);
-              if (ok) ok = mbar_wait(&ctl.slot_full[sl], (g / kSlots) & 1, abort_flag, wait_ns);
+            // The item's pages in pairs (the first of a pair into score
+            // buffer 0, the second into buffer 1; an odd last page alone).
+            // A pair in adjacent ring slots is ONE operand of 128 tokens (the
+            // second slot continues the first's 9 KB stride): 36 MMAs with
+            // N = 128 instead of 72 with N = 64.
+            for (int k = 0; ok && k < n; k += 2) {
+              const bool pair = k + 1 < n;
+              const uint32_t sl0 = g % kSlots, sl1 = (g + 1) % kSlots;
+              if (s_use[0] > 0) ok = mbar_wait(&ctl.s_free[0], (s_use[0] - 1) & 1, abort_flag, wait_ns);
+              if (ok && pair && s_use[1] > 0) ok = mbar_wait(&ctl.s_free[1], (s_use[1] - 1) & 1, abort_flag, wait_ns);
+              if (ok) ok = mbar_wait(&ctl.slot_full[sl0], (g / kSlots) & 1, abort_flag, wait_ns);
+              if (ok && pair) ok = mbar_wait(&ctl.slot_full[sl1], ((g + 1) / kSlots) & 1, abort_flag, wait_ns);
               if (!ok) break;
               tc_fence_after();
-              // B = the page's tokens (K-major SW128, 8-token groups 9 KB
+              // B = a page's tokens (K-major SW128, 8-token groups 9 KB
               // apart); chunk c starts 1 KB further, a K-step of 16 dims 32 B
-              const uint64_t b0 = sdesc_sw128(smem_u32(smem + sl * kPageBytes), 16, 9216);
-              const uint32_t d = tmem + kTmemS + 64 * sb;
+              const uint64_t b0 = sdesc_sw128(smem_u32(smem + sl0 * kPageBytes), 16, 9216);
+              const uint64_t b1 = sdesc_sw128(smem_u32(smem + sl1 * kPageBytes), 16, 9216);
+              const uint32_t d = tmem + kTmemS;
+              if (pair && sl1 == sl0 + 1) {
 #pragma unroll 1
-              for (int c = 0; c < 9; ++c)
+                for (int c = 0; c < 9; ++c)
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  mma_ts(d, tmem + (uint32_t)(8 * (4 * c + kk)), b0 + (uint64_t)(64 * c + 2 * kk), idS,
-                         (c | kk) ? 1u : 0u);
-              mma_commit(&ctl.slot_empty[sl]);
-              mma_commit(&ctl.s_full[sb]);
+                  for (int kk = 0; kk < 4; ++kk)
+                    mma_ts(d, tmem + (uint32_t)(8 * (4 * c + kk)), b0 + (uint64_t)(64 * c + 2 * kk), idS2,
+                           (c | kk) ? 1u : 0u);
+              } else if (pair) {
+#pragma unroll 1
+                for (int c = 0; c < 9; ++c)
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t at = tmem + (uint32_t)(8 * (4 * c + kk));
+                    const uint32_t acc = (c | kk) ? 1u : 0u;
+                    mma_ts(d, at, b0 + (uint64_t)(64 * c + 2 * kk), idS, acc);
+                    mma_ts(d + 64, at, b1 + (uint64_t)(64 * c + 2 * kk), idS, acc);
+                  }
+              } else {
+#pragma unroll 1
+                for (int c = 0; c < 9; ++c)
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk)
+                    mma_ts(d, tmem + (uint32_t)(8 * (4 * c + kk)), b0 + (uint64_t)(64 * c + 2 * kk), idS,
+                           (c | kk) ? 1u : 0u);
+              }
+              mma_commit(&ctl.slot_empty[sl0]);
+              mma_commit(&ctl.s_full[0]);
+              ++s_use[0];
+              if (pair) {
+                mma_commit(&ctl.slot_empty[sl1]);
+                mma_commit(&ctl.s_full[1]);
+                ++s_use[1];
+              }
+              g += pair ? 2 : 1;
             }
             if (!ok) { fail(&ctl, a.err); break; }
             mma_commit(&ctl.q_free);
@@ -617,12 +674,14 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
       __syncwarp();
     } else if (rank == 0 && warp <= 9) {
       // ============================================================ softmax (score CTA)
-      // Two groups of four warps: warps 2-5 take the even pages, warps 6-9
-      // the odd ones.  Warp w owns TMEM lane quarter w & 3 (rows 32 (w & 3)
-      // .. + 31), one row per thread over all 64 tokens of a page.  The
-      // groups share each row's reference max through `mref` (tagged with the
-      // item); a page's message carries the reference its probabilities are
-      // relative to, and the value CTA rescales when consecutive pages differ.
+      // Two groups of four warps: warps 2-5 take the first page of each pair
+      // of an item's pages (and an odd last page), warps 6-9 the second.
+      // Warp w owns TMEM lane quarter w & 3 (rows 32 (w & 3) .. + 31), one
+      // row per thread over all 64 tokens of a page.  Each page's reference
+      // max follows from the previous page's (passed between the groups
+      // through `mref`); a page's message carries the reference its
+      // probabilities are relative to, and the value CTA rescales when
+      // consecutive pages differ.
       const int grp = warp >= 6 ? 1 : 0;
       const int q4 = warp & 3;
       const int r = 32 * q4 + lane;
@@ -637,7 +696,6 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
         // padding rows (r >= rows_g) see no token at all
         const int lim = r >= rows_g ? -1 : a.causal ? (L - a.T_q + t) : (L - 1);
         const int n = it.j1 - it.j0;
-        const uint32_t tag = it_cnt + 1;
         // the previous item's scores, which read the query, are complete
         // (one phase of q_free per item; a group is never more than one item
         // ahead, because the scores of an item wait for its query)
@@ -647,12 +705,13 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
         bool ok = true;
         for (int k = 0; k < n; ++k) {
           const uint32_t g = g_page + k, gs = g % kGSlots;
-          if ((int)(g & 1) != grp) continue;
+          if ((k & 1) != grp) continue;   // group 0 the first page of each pair, group 1 the second
           const int j = it.j0 + k;
           const bool last_page = k + 1 == n;
           const int bk = __ldg(a.block_table + (size_t)it.b * a.max_blocks + j);
           const bool page_ok = bk >= 0 && bk < a.num_blocks;
-          if (!warp_wait(&ctl.s_full[grp], (g >> 1) & 1, abort_flag, wait_ns)) { ok = false; break; }
+          if (!warp_wait(&ctl.s_full[grp], s_seen & 1, abort_flag, wait_ns)) { ok = false; break; }
+          ++s_seen;
           tc_fence_after();
           float x[64];
           tmem_ld64(tmem + lane_off + kTmemS + 64 * grp, x);
@@ -671,17 +730,24 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
 #pragma unroll
           for (int q = 1; q < 64; ++q) mx = fmaxf(mx, x[q]);
           const float m_page = mx * sl2;
-          // reference: the larger of this group's and the shared one; it moves
-          // only when the page max exceeds it by more than 2^8
-          const unsigned long long e = ctl.mref[r];
-          const float m_peer = (uint32_t)(e >> 32) == tag ? __uint_as_float((uint32_t)e) : -INFINITY;
-          const float m_cur = fmaxf(m_run, m_peer);
-          const float m_new = m_page > m_cur + kRescaleThreshold ? m_page : m_cur;
+          // The page's reference max: the previous page's (sent by the other
+          // group, which takes the item's other pages) unless this page's max
+          // exceeds it by more than 2^8.  So the references of an item's pages
+          // never decrease and the value CTA only ever scales O down.  The
+          // references go through `mref`, tagged with page index + 1.
+          float m_prev_ref = -INFINITY;
+          volatile unsigned long long* mr = &ctl.mref[r];
+          if (k > 0) {
+            unsigned long long e = 0;
+            if (!__all_sync(0xffffffffu, wait_tag(mr, g, &e, abort_flag, wait_ns))) { ok = false; break; }
+            m_prev_ref = __uint_as_float((uint32_t)e);
+          }
+          const float m_new = m_page > m_prev_ref + kRescaleThreshold ? m_page : m_prev_ref;
+          *mr = ((unsigned long long)(g + 1) << 32) | __float_as_uint(m_new);
           if (m_new != m_run) {
             l_run = m_run == -INFINITY ? 0.f : l_run * ex2(m_run - m_new);
             m_run = m_new;
           }
-          if (m_run > m_peer) ctl.mref[r] = ((unsigned long long)tag << 32) | __float_as_uint(m_run);
           // Precision of the bf16 probabilities: when a page's largest
           // probability is not small against this group's sum for the row so
           // far, the warp also sends the low bf16 parts (p - bf16(p)) of its
