@@ -15,7 +15,8 @@ from ._lib import (  # noqa: F401
     LIB_PATH, MLA_BF16, MLA_ERR_BAD_INDEX, MLA_ERR_BAD_RECORD, MLA_ERR_CUDA, MLA_ERR_INVALID_ARG,
     MLA_ERR_TIMEOUT, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE, MLA_F32, MLA_OK, PAGE_SIZE,
     SIGNATURES, MLAError, alloc_step_workspace, alloc_workspace, lib, load_library,
-    mla_absorb_output, mla_absorb_query, mla_cache_append, mla_check_status,
+    mla_absorb_output, mla_absorb_output_merged, mla_absorb_output_merged_workspace_size,
+    mla_absorb_query, mla_cache_append, mla_check_status, mla_merge_output_weights,
     mla_decode_item_cost, mla_decode_num_workers, mla_decode_paged, mla_decode_paged_noalloc,
     mla_decode_row_groups, mla_decode_split_plan, mla_decode_step, mla_decode_workspace_size,
     mla_prefill_attention, mla_prefill_kv, mla_prefill_kv_rows, mla_prefill_use_rebuild,

@@ -43,6 +43,9 @@ SIGNATURES = {
     "mla_decode_combine": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                 _P, _SZ, _P, _P, _P]),
     "mla_absorb_output": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "mla_merge_output_weights": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "mla_absorb_output_merged_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "mla_absorb_output_merged": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P, _P]),
     "mla_status_string": (ctypes.c_char_p, [_I]),
     "mla_last_cuda_error": (ctypes.c_char_p, []),
     "mla_check_status": (_I, [_P]),
@@ -262,6 +265,47 @@ def mla_absorb_output(o_lat, w_uv, w_o, *, out=None, stream=None):
         _dtype_code(w_uv), N, H, HD // H, d_c, d, _dev(out, "out", torch.float32),
         _stream(stream))
     _check(st, "mla_absorb_output")
+    return out
+
+
+def mla_merge_output_weights(w_uv, w_o, H, *, out=None, stream=None):
+    """W_m[j, h*d_c + c] = sum_v w_o[j, h*d_h + v] w_uv[h*d_h + v, c]  -> [d, H*d_c] bf16."""
+    HD, d_c = w_uv.shape
+    d, HD2 = w_o.shape
+    if HD2 != HD or HD % H:
+        raise ValueError("shape mismatch")
+    if w_uv.dtype != w_o.dtype:
+        raise TypeError("w_uv and w_o must share a dtype")
+    if out is None:
+        out = torch.empty((d, H * d_c), device=w_o.device, dtype=torch.bfloat16)
+    st = lib().mla_merge_output_weights(_dev(w_uv, "w_uv"), _dev(w_o, "w_o"), _dtype_code(w_uv), H,
+                                        HD // H, d_c, d, _dev(out, "w_merged", torch.bfloat16),
+                                        _stream(stream))
+    _check(st, "mla_merge_output_weights")
+    return out
+
+
+def mla_absorb_output_merged_workspace_size(N, H, d_c, d):
+    return int(lib().mla_absorb_output_merged_workspace_size(N, H, d_c, d))
+
+
+def mla_absorb_output_merged(o_lat, w_merged, *, workspace=None, out=None, stream=None):
+    """out[n, j] = sum_{h,c} w_merged[j, h*d_c + c] o_lat[n, h, c]  -> [N, d] float32."""
+    N, H, d_c = o_lat.shape
+    d, K = w_merged.shape
+    if K != H * d_c:
+        raise ValueError("shape mismatch")
+    need = mla_absorb_output_merged_workspace_size(N, H, d_c, d) if N > 0 else 0
+    if workspace is None and N > 0:
+        workspace = torch.empty(need, device=o_lat.device, dtype=torch.uint8)
+    if out is None:
+        out = torch.empty((N, d), device=o_lat.device, dtype=torch.float32)
+    st = lib().mla_absorb_output_merged(
+        _dev(o_lat, "o_lat", torch.float32), _dev(w_merged, "w_merged"), _dtype_code(w_merged), N, H, d_c, d,
+        _dev(workspace, "workspace") if workspace is not None else None,
+        workspace.numel() * workspace.element_size() if workspace is not None else 0,
+        _dev(out, "out", torch.float32), _stream(stream))
+    _check(st, "mla_absorb_output_merged")
     return out
 
 

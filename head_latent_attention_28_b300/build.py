@@ -20,7 +20,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmla.so")
-SOURCES = ["mla_api.cu", "decode_generic.cu", "decode_tc.cu", "append_absorb.cu", "prefill_tc.cu"]
+SOURCES = ["mla_api.cu", "decode_generic.cu", "decode_tc.cu", "append_absorb.cu", "prefill_tc.cu",
+           "out_proj_tc.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))] + \
           [os.path.join(ROOT, "include", "mla.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

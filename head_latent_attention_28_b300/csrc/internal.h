@@ -82,6 +82,34 @@ struct AbsorbOArgs {
 };
 cudaError_t launch_absorb_output(const AbsorbOArgs& a, cudaStream_t s);
 
+// out_proj_tc.cu (output projections on the tensor cores; bf16 weights)
+struct MergeWArgs {
+  const void* w_uv; const void* w_o;   // [H * d_h, d_c], [d, H * d_h]
+  int H, d_h, d_c, d;
+  void* w_merged;                      // [d, H * d_c] (output)
+  unsigned* err;
+};
+cudaError_t launch_merge_output_weights(const MergeWArgs& a, cudaStream_t s);
+// split of the merged output's K = H * d_c across the grid, and its workspace:
+// the bf16 copy of o_lat at a_offset, fp32 partial sums [splits][N][d] at part_offset
+struct MergedSplit {
+  int splits, k_split;
+  size_t a_offset, part_offset, workspace_bytes;
+};
+MergedSplit merged_output_split(int N, int H, int d_c, int d, int num_sms);
+struct MergedOArgs {
+  const float* o_lat; const void* w_merged;   // [N, H, d_c], [d, H * d_c]
+  int N, H, d_c, d;
+  void* workspace; MergedSplit split;
+  float* out;                                 // [N, d]
+  unsigned* err;
+};
+cudaError_t launch_absorb_output_merged(const MergedOArgs& a, cudaStream_t s);
+// the unmerged pair of projections (mla_absorb_output) on the tensor cores:
+// bf16 weights, d_c % 64 == 0, d_h % 8 == 0, d % 4 == 0, 16-byte aligned
+bool absorb_output_tc_ok(const AbsorbOArgs& a);
+cudaError_t launch_absorb_output_tc(const AbsorbOArgs& a, unsigned* err, int num_sms, cudaStream_t s);
+
 // prefill_tc.cu (materialised per-head keys and values; bf16, d_c = 512,
 // d_h = 128, d_r = 64)
 bool prefill_supported(int dtype, int d_c, int d_r, int d_h);

@@ -217,7 +217,60 @@ int mla_absorb_output(const float* o_lat, const void* w_uv, const void* w_o, int
   if (N == 0) return MLA_OK;
   if (!o_lat || !w_uv || !w_o || !out) return MLA_ERR_INVALID_ARG;
   mla::AbsorbOArgs a{o_lat, w_uv, w_o, dtype, N, H, d_h, d_c, d, out};
-  cudaError_t e = mla::launch_absorb_output(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (mla::absorb_output_tc_ok(a)) {
+    unsigned* err = nullptr;
+    int sms = 0;
+    e = device_info(&err, &sms);
+    if (e != cudaSuccess) return note_cuda(e);
+    e = mla::launch_absorb_output_tc(a, err, sms, static_cast<cudaStream_t>(stream));
+  } else {
+    e = mla::launch_absorb_output(a, static_cast<cudaStream_t>(stream));
+  }
+  return e == cudaSuccess ? MLA_OK : note_cuda(e);
+}
+
+namespace {
+bool merged_dims_ok(int H, int d_c, int d) {
+  return H >= 1 && d_c >= 8 && d_c % 8 == 0 && d >= 4 && d % 4 == 0 && (long long)H * d_c <= (1LL << 30) &&
+         d <= (1 << 24);
+}
+}  // namespace
+
+int mla_merge_output_weights(const void* w_uv, const void* w_o, int dtype, int H, int d_h, int d_c, int d,
+                             void* w_merged, void* stream) {
+  if (!merged_dims_ok(H, d_c, d) || d_h < 1 || !dtype_ok(dtype) || (long long)H * d_h > (1LL << 30))
+    return MLA_ERR_INVALID_ARG;
+  if (!w_uv || !w_o || !w_merged || !aligned16(w_uv) || !aligned16(w_o) || !aligned16(w_merged)) return MLA_ERR_INVALID_ARG;
+  if (dtype != MLA_BF16 || d_h % 64 != 0 || H > 65535) return MLA_ERR_UNSUPPORTED;
+  mla::MergeWArgs a{w_uv, w_o, H, d_h, d_c, d, w_merged, nullptr};
+  cudaError_t e = device_info(&a.err, nullptr);
+  if (e != cudaSuccess) return note_cuda(e);
+  e = mla::launch_merge_output_weights(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : note_cuda(e);
+}
+
+size_t mla_absorb_output_merged_workspace_size(int N, int H, int d_c, int d) {
+  if (N < 1 || !merged_dims_ok(H, d_c, d)) return 0;
+  int sms = 0;
+  if (device_info(nullptr, &sms) != cudaSuccess) return 0;
+  return mla::merged_output_split(N, H, d_c, d, sms).workspace_bytes;
+}
+
+int mla_absorb_output_merged(const float* o_lat, const void* w_merged, int dtype, int N, int H, int d_c, int d,
+                             void* workspace, size_t workspace_bytes, float* out, void* stream) {
+  if (N < 0 || !merged_dims_ok(H, d_c, d) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
+  if (N == 0) return MLA_OK;
+  if (!o_lat || !w_merged || !out || !aligned16(o_lat) || !aligned16(w_merged) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+  if (dtype != MLA_BF16 || (long long)(N + 127) / 128 > 65535) return MLA_ERR_UNSUPPORTED;
+  mla::MergedOArgs a{o_lat, w_merged, N, H, d_c, d, workspace, {}, out, nullptr};
+  int sms = 0;
+  cudaError_t e = device_info(&a.err, &sms);
+  if (e != cudaSuccess) return note_cuda(e);
+  a.split = mla::merged_output_split(N, H, d_c, d, sms);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < a.split.workspace_bytes)
+    return MLA_ERR_WORKSPACE;
+  e = mla::launch_absorb_output_merged(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : note_cuda(e);
 }
 

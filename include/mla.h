@@ -275,10 +275,61 @@ int mla_decode_step(const void* q_nope, const void* q_rope, const void* w_uk, in
  *
  *   o_lat [N, H, d_c] float;  w_uv [H*d_h, d_c] dtype;  w_o [d, H*d_h] dtype
  *   out   [N, d] float (output)
- * Host errors: NULL pointers, non-positive dims, H*d_h > 32768.
+ * bf16 weights with d_c % 64 == 0, d_h % 8 == 0, d % 4 == 0 and 16-byte
+ * aligned pointers run on the tensor cores: o_lat and o enter as bf16 value
+ * plus bf16 remainder (about fp32 accuracy), K of the second product is split
+ * across the grid and the partial sums are added in a fixed order; the call
+ * allocates and frees a scratch buffer in stream order on `stream`.  Other
+ * shapes and fp32 weights run on CUDA cores.
+ * Host errors: NULL pointers, non-positive dims, H*d_h > 32768.  Device
+ * errors: MLA_ERR_TIMEOUT (tensor-core path).
  */
 int mla_absorb_output(const float* o_lat, const void* w_uv, const void* w_o, int dtype,
                       int N, int H, int d_h, int d_c, int d, float* out, void* stream);
+
+/*
+ * mla_merge_output_weights -- fold W^UV into W^O: one d x d_c matrix per head
+ * ("How DeepSeek Rewrote the Transformer", the absorbed inference path: the
+ * value up-projection can be merged into the output projection).
+ *
+ *   w_merged[j, h*d_c + c] = sum_v w_o[j, h*d_h + v] * w_uv[h*d_h + v, c]
+ *
+ *   w_uv [H*d_h, d_c] bf16;  w_o [d, H*d_h] bf16
+ *   w_merged [d, H*d_c] bf16 (output; fp32 sums rounded once)
+ * A one-time weight transform: it allocates and frees a scratch copy of w_uv
+ * (H*d_h*d_c*2 bytes) in stream order on `stream`.
+ * Host errors: MLA_ERR_INVALID_ARG (non-positive dims, d_c % 8 or d % 4 not
+ * zero, NULL or not 16-byte aligned pointers); MLA_ERR_UNSUPPORTED for
+ * dtype != MLA_BF16 or d_h % 64 != 0.  Device errors: MLA_ERR_TIMEOUT (a
+ * bounded wait gave up; w_merged then holds no result).  Asynchronous.
+ */
+int mla_merge_output_weights(const void* w_uv, const void* w_o, int dtype, int H, int d_h, int d_c,
+                             int d, void* w_merged, void* stream);
+
+/*
+ * mla_absorb_output_merged -- the output projection with merged weights:
+ *
+ *   out[n, j] = sum_{h, c} w_merged[j, h*d_c + c] * o_lat[n, h, c]
+ *
+ * equal (up to rounding) to mla_absorb_output with the weights merged by
+ * mla_merge_output_weights.  o_lat is rounded to bf16 (like the weights)
+ * and the products are summed in fp32 on the tensor cores, split along
+ * H*d_c; the splits are added in a fixed order, so the result is
+ * deterministic.  It reads d*H*d_c weights against H*d_h*(d_c + d) unmerged:
+ * more whenever d_h < d_c.
+ *
+ *   o_lat [N, H, d_c] float;  w_merged [d, H*d_c] bf16;  out [N, d] float
+ *   workspace: >= mla_absorb_output_merged_workspace_size(N, H, d_c, d)
+ *              bytes, 256-byte aligned (a bf16 copy of o_lat and the fp32
+ *              partial sums)
+ * Host errors: MLA_ERR_INVALID_ARG (bad sizes, NULL or unaligned pointers),
+ * MLA_ERR_UNSUPPORTED (dtype != MLA_BF16), MLA_ERR_WORKSPACE.  Device
+ * errors: MLA_ERR_TIMEOUT.  Asynchronous on `stream`.
+ */
+size_t mla_absorb_output_merged_workspace_size(int N, int H, int d_c, int d);   /* 0: invalid */
+int mla_absorb_output_merged(const float* o_lat, const void* w_merged, int dtype, int N, int H,
+                             int d_c, int d, void* workspace, size_t workspace_bytes, float* out,
+                             void* stream);
 
 /*
  * mla_decode_split_plan -- HOST helper: which split workers mla_decode_paged

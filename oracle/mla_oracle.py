@@ -29,6 +29,7 @@ __all__ = [
     "full_model_absorbed", "full_model_rope_on_reconstructed_keys",
     "mha_cache_numbers", "gqa_cache_numbers", "mla_cache_numbers",
     "mla_equivalent_gqa_groups", "bf16_to_f64", "rebuild_kv", "prefill_attention",
+    "merge_output_weights", "absorb_output_merged",
 ]
 
 
@@ -153,6 +154,29 @@ def absorb_output(o_lat, W_uv, W_o):
     W = np.asarray(W_uv, dtype=np.float64).reshape(H, -1, d_c)   # [H, d_h, d_c]
     o = np.stack([o_lat[:, hh, :] @ W[hh].T for hh in range(H)], axis=1)    # [n, H, d_h]
     return o.reshape(n, -1) @ np.asarray(W_o, dtype=np.float64).T
+
+
+# --------------------------------------------------------------------------
+# W^UV folded into W^O ("How DeepSeek Rewrote the Transformer", the absorbed
+# inference path: the value up-projection merges into the output projection)
+# --------------------------------------------------------------------------
+
+def merge_output_weights(W_uv, W_o, H):
+    """One d x d_c matrix per head: M_h = W^O_h W^UV_h, where W^O_h is the
+    column block of W^O that multiplies head h's values.  Returned side by
+    side, [d, H * d_c]."""
+    W_uv = np.asarray(W_uv, dtype=np.float64)
+    W_o = np.asarray(W_o, dtype=np.float64)
+    d_h = W_uv.shape[0] // H
+    blocks = [W_o[:, hh * d_h:(hh + 1) * d_h] @ W_uv[hh * d_h:(hh + 1) * d_h] for hh in range(H)]
+    return np.concatenate(blocks, axis=1)
+
+
+def absorb_output_merged(o_lat, W_m):
+    """u = sum_h M_h o_lat,h   ([n, d]); W_m = [M_1 ... M_H]."""
+    o_lat = np.asarray(o_lat, dtype=np.float64)
+    n, H, d_c = o_lat.shape
+    return o_lat.reshape(n, H * d_c) @ np.asarray(W_m, dtype=np.float64).T
 
 
 # --------------------------------------------------------------------------

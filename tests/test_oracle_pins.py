@@ -339,6 +339,43 @@ def test_absorb_output_against_explicit_values():
                                rtol=0, atol=1e-12)
 
 
+def test_merged_output_equals_the_two_projections():
+    """Associativity: W^O [W^UV_h o_h]_h == sum_h (W^O_h W^UV_h) o_h.  The
+    merged form multiplies in the other order, so a transposed block or a
+    wrong head offset on either side breaks the equality."""
+    rng = np.random.default_rng(33)
+    H, d_h, d_c, d, n = 5, 3, 7, 11, 4
+    W_uv = rng.standard_normal((H * d_h, d_c))
+    W_o = rng.standard_normal((d, H * d_h))
+    o_lat = rng.standard_normal((n, H, d_c))
+    W_m = orc.merge_output_weights(W_uv, W_o, H)
+    assert W_m.shape == (d, H * d_c)
+    np.testing.assert_allclose(orc.absorb_output_merged(o_lat, W_m), orc.absorb_output(o_lat, W_uv, W_o),
+                               rtol=0, atol=1e-12)
+
+
+def test_merged_weights_special_cases():
+    """W^UV_h = [I 0] (the first d_h latents) makes M_h the column block
+    W^O_h padded with zeros; a W^O that selects one value coordinate of one
+    head makes a row of M equal a row of W^UV."""
+    rng = np.random.default_rng(34)
+    H, d_h, d_c, d = 3, 2, 5, 4
+    W_uv = np.zeros((H * d_h, d_c))
+    for hh in range(H):
+        W_uv[hh * d_h:(hh + 1) * d_h, :d_h] = np.eye(d_h)
+    W_o = rng.standard_normal((d, H * d_h))
+    W_m = orc.merge_output_weights(W_uv, W_o, H)
+    for hh in range(H):
+        np.testing.assert_array_equal(W_m[:, hh * d_c:hh * d_c + d_h], W_o[:, hh * d_h:(hh + 1) * d_h])
+        np.testing.assert_array_equal(W_m[:, hh * d_c + d_h:(hh + 1) * d_c], 0.0)
+    W_uv = rng.standard_normal((H * d_h, d_c))
+    W_o = np.zeros((d, H * d_h))
+    W_o[2, 1 * d_h + 1] = 1.0                      # output 2 = value coordinate 1 of head 1
+    W_m = orc.merge_output_weights(W_uv, W_o, H)
+    np.testing.assert_array_equal(W_m[2, d_c:2 * d_c], W_uv[1 * d_h + 1])
+    assert np.count_nonzero(W_m[[0, 1, 3]]) == 0 and np.count_nonzero(W_m[2, :d_c]) == 0
+
+
 # --------------------------------------------------------------------------
 # bfloat16 decoding: fixed bit patterns from the format's definition (1 sign,
 # 8 exponent bits with bias 127, 7 fraction bits), and torch's own decoding
