@@ -584,11 +584,90 @@ def run_mla(args, spec):
                 extra[name] = decode_subrecord(mi.DECODE_WORKLOADS[name], dev, args, peaks, peak_src)
         for name, pspec in sorted(mi.PREFILL_WORKLOADS.items()):
             extra[name] = prefill_subrecord(pspec, dev, args, peaks, peak_src)
+        for name, ospec in sorted(mi.OUT_PROJ_WORKLOADS.items()):
+            extra[name] = out_proj_subrecord(ospec, dev, args, peaks, peak_src)
         line["configs"] = extra
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+# --------------------------------------------------------------------------
+# output projections: W^UV then W^O, or the two merged into one matrix
+# --------------------------------------------------------------------------
+
+def out_proj_subrecord(spec, dev, args, peaks, peak_src):
+    """Both forms of the output projection at decode size, each timed alone
+    (back-to-back calls); HBM-bound at this N, so each gets the HBM roofline
+    over its own algorithmic bytes (its weights, o_lat in, out back)."""
+    import torch
+    import head_latent_attention_28_b300 as mla
+    inp = mi.make_out_proj_inputs(spec)
+    N, H, d_h, d_c, d = spec.N, spec.H, spec.d_h, spec.d_c, spec.d
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+    w_uv, w_o = up(inp.w_uv_bits), up(inp.w_o_bits)
+    o_lat = torch.from_numpy(inp.o_lat).to(dev)
+    out = torch.empty((N, d), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    w_m = mla.mla_merge_output_weights(w_uv, w_o, H)
+    torch.cuda.synchronize(dev)
+    merge_ms = 1e3 * (time.perf_counter() - t0)
+    ws = torch.empty(mla.mla_absorb_output_merged_workspace_size(N, H, d_c, d), device=dev, dtype=torch.uint8)
+
+    def unmerged(i):
+        mla.mla_absorb_output(o_lat, w_uv, w_o, out=out, stream=stream)
+
+    def merged(i):
+        mla.mla_absorb_output_merged(o_lat, w_m, workspace=ws, out=out, stream=stream)
+    for _ in range(args.warmup):
+        unmerged(0)
+        merged(0)
+    K = max(min(args.steps, 50), 10)
+    un_ms = device_time_ms(unmerged, K, stream, dev)
+    mg_ms = device_time_ms(merged, K, stream, dev)
+    if mla.mla_check_status(stream) != mla.MLA_OK:
+        raise SystemExit("out_proj: device error")
+    act = N * H * d_c * 4 + N * d * 4
+    b_un = (H * d_h * d_c + d * H * d_h) * 2 + act
+    b_mg = d * H * d_c * 2 + act
+
+    def roof(bytes_, ms, kernel):
+        gbs = bytes_ / (ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": kernel, "kernel_ms": ms,
+                "algorithmic_bytes": bytes_, "peak_source": peak_src + " (burst; calls timed alone)",
+                "kernel_time": "one event pair around back-to-back calls, divided by their number"}
+    rec = {"unmerged_us": 1e3 * un_ms, "merged_us": 1e3 * mg_ms, "merge_weights_ms": merge_ms, "steps": K,
+           "value": b_un / (un_ms / 1e3) / 1e9, "unit": "GB/s",
+           "adopted": "unmerged (mla_absorb_output): it reads H*d_h*(d_c + d) weights against d*H*d_c merged",
+           "roofline": roof(b_un, un_ms, "out_proj_tc.cu (gemm_tn_kernel, unmerged: per-head W^UV, split-K W^O)"),
+           "merged": {"value": b_mg / (mg_ms / 1e3) / 1e9, "unit": "GB/s",
+                      "roofline": roof(b_mg, mg_ms, "out_proj_tc.cu (gemm_tn_kernel, split-K merged weights)")},
+           "config": {"workload": spec.name, "rows": N, "heads": H, "d_h": d_h, "d_c": d_c, "d": d,
+                      "weight_dtype": "bf16", "l2": "the weights of each call exceed L2",
+                      "parallelism": "replicas"}}
+    if not args.no_cpu_baseline:
+        import oracle as orc
+        w_uv64 = mi.bf16_bits_to_f32(inp.w_uv_bits).reshape(inp.w_uv_bits.shape)
+        w_o64 = mi.bf16_bits_to_f32(inp.w_o_bits).reshape(inp.w_o_bits.shape)
+        t0, n = time.perf_counter(), 0
+        while n < N and (n == 0 or time.perf_counter() - t0 < args.cpu_budget / 4):
+            orc.absorb_output(inp.o_lat[n:n + 1], w_uv64, w_o64)
+            n += 1
+        sec = time.perf_counter() - t0
+        # the whole batch at the sample's rate: N rows take N / n times as long
+        rec["cpu_baseline"] = {"value": b_un / (sec * N / n) / 1e9, "unit": "GB/s",
+                               "cores": blas_threads(), "kind": "oracle",
+                               "sample": f"fp64 numpy absorb_output of {n} of the {N} rows, {sec:.1f} s, "
+                                         f"scaled to the batch"}
+    del w_uv, w_o, w_m, ws, o_lat, out
+    torch.cuda.empty_cache()
+    return rec
 
 
 # --------------------------------------------------------------------------

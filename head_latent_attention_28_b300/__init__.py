@@ -20,6 +20,6 @@ from ._lib import (  # noqa: F401
     mla_decode_item_cost, mla_decode_num_workers, mla_decode_paged, mla_decode_paged_noalloc,
     mla_decode_row_groups, mla_decode_split_plan, mla_decode_step, mla_decode_workspace_size,
     mla_prefill_attention, mla_prefill_kv, mla_prefill_kv_rows, mla_prefill_use_rebuild,
-    mla_status_string, mla_test_set_wait_fault)
+    mla_status_string, mla_test_force_splits, mla_test_set_wait_fault)
 
 lib()  # load now: no silent fallback path exists

@@ -50,6 +50,7 @@ SIGNATURES = {
     "mla_last_cuda_error": (ctypes.c_char_p, []),
     "mla_check_status": (_I, [_P]),
     "mla_test_set_wait_fault": (_I, [_I, ctypes.c_uint]),
+    "mla_test_force_splits": (_I, [_I]),
     "mla_version": (_I, []),
     "mla_decode_split_plan": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "mla_decode_item_cost": (_I, [_I, _I, _I, _I, _I]),
@@ -466,6 +467,12 @@ def mla_test_set_wait_fault(skip_load: int, wait_us: int = 1000) -> None:
     `skip_load` of split worker 0 with bounded waits of `wait_us` (0 turns
     the hook off); see include/mla.h."""
     _check(lib().mla_test_set_wait_fault(int(skip_load), int(wait_us)), "mla_test_set_wait_fault")
+
+
+def mla_test_force_splits(num_workers: int) -> None:
+    """Test knob: cap the decode split workers at num_workers (0: default);
+    see include/mla.h."""
+    _check(lib().mla_test_force_splits(int(num_workers)), "mla_test_force_splits")
 
 
 def mla_status_string(status: int) -> str:

@@ -24,6 +24,8 @@ thread_local char g_last_cuda[256] = "";
 
 // test hook of mla_test_set_wait_fault (zero: off)
 std::atomic<int> g_test_skip_load{0};
+// test knob of mla_test_force_splits (zero: off)
+std::atomic<int> g_test_force_workers{0};
 std::atomic<unsigned long long> g_test_wait_ns{0};
 
 // Scratch of mla_decode_paged_noalloc: the split workspace (merge metadata,
@@ -97,8 +99,9 @@ bool decode_dims_ok(int B, int T_q, int H, int d_c, int d_r) {
 
 int decode_workers(int dtype, int B, int T_q, int H, int d_c, int d_r, int sms) {
   (void)B;
-  return mla::tc_supported(dtype, H, T_q, d_c, d_r) ? mla::tc_workers(sms)
-                                                     : mla::generic_workers(sms);
+  const int W = mla::tc_supported(dtype, H, T_q, d_c, d_r) ? mla::tc_workers(sms) : mla::generic_workers(sms);
+  const int f = g_test_force_workers.load(std::memory_order_relaxed);
+  return f > 0 && f < W ? f : W;
 }
 
 // the split partition's item cost for the kernel a shape selects (the
@@ -158,6 +161,12 @@ int mla_check_status(void* stream) {
   if (v & mla::kErrTimeout) return MLA_ERR_TIMEOUT;
   if (v & mla::kErrBadIndex) return MLA_ERR_BAD_INDEX;
   if (v & mla::kErrBadRecord) return MLA_ERR_BAD_RECORD;
+  return MLA_OK;
+}
+
+int mla_test_force_splits(int num_workers) {
+  if (num_workers < 0) return MLA_ERR_INVALID_ARG;
+  g_test_force_workers.store(num_workers, std::memory_order_relaxed);
   return MLA_OK;
 }
 

@@ -508,6 +508,18 @@ int mla_check_status(void* stream);
  */
 int mla_test_set_wait_fault(int skip_load, unsigned wait_us);
 
+/*
+ * mla_test_force_splits -- TEST KNOB (process-wide): cap the split workers
+ * of mla_decode_paged (and of mla_decode_workspace_size and
+ * mla_decode_num_workers, which must see the same value) at num_workers, so
+ * that tests can run the same batch with 1, 2, ... splits and compare.  The
+ * cost-weighted partition then cuts the pages into at most that many ranges
+ * (fewer when the batch is small).  0 restores the default; values above the
+ * device's worker count have no effect.  Returns MLA_OK, or
+ * MLA_ERR_INVALID_ARG for a negative value.  Not for concurrent use.
+ */
+int mla_test_force_splits(int num_workers);
+
 /* Library ABI version (major * 100 + minor). */
 int mla_version(void);
 

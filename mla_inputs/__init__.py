@@ -342,3 +342,46 @@ def make_prefill_inputs(spec: PrefillSpec, with_kv: bool = False) -> PrefillInpu
             kr[b, L:] = 0
         inp.k_nope_bits, inp.v_bits, inp.k_rope_bits = k, v, kr
     return inp
+
+
+# --------------------------------------------------------------------------
+# output projection inputs (the attended latent and the value / output weights)
+# --------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class OutProjSpec:
+    """W^UV then W^O (or the two merged) applied to N attended latents."""
+    name: str
+    seed: int
+    N: int
+    H: int = 128
+    d_h: int = 128
+    d_c: int = 512
+    d: int = 5120
+
+
+# one decode step of the ragged serving batch (128 sequences x 1 token) at
+# the pages' model width d = 5120
+OUT_PROJ = OutProjSpec("out_proj_n128_h128_d5120", seed=9, N=128)
+OUT_PROJ_WORKLOADS = {OUT_PROJ.name: OUT_PROJ}
+
+
+@dataclasses.dataclass
+class OutProjInputs:
+    spec: OutProjSpec
+    o_lat: np.ndarray           # float32 [N, H, d_c]
+    w_uv_bits: np.ndarray       # uint16 [H * d_h, d_c]
+    w_o_bits: np.ndarray        # uint16 [d, H * d_h]
+
+
+def make_out_proj_inputs(spec: OutProjSpec) -> OutProjInputs:
+    """From default_rng(seed): o_lat ~ N(0, 1) float32; W^UV ~ N(0, 1/d_c) and
+    W^O ~ N(0, 1/(H d_h)) rounded once to bfloat16, in that order (unit-size
+    numbers through both projections)."""
+    rng = np.random.default_rng(spec.seed)
+    o_lat = rng.standard_normal((spec.N, spec.H, spec.d_c), dtype=np.float32)
+    w_uv = rng.standard_normal((spec.H * spec.d_h, spec.d_c), dtype=np.float32) * np.float32(1.0 / math.sqrt(spec.d_c))
+    w_o = rng.standard_normal((spec.d, spec.H * spec.d_h), dtype=np.float32) * np.float32(
+        1.0 / math.sqrt(spec.H * spec.d_h))
+    return OutProjInputs(spec, o_lat, f32_to_bf16_bits(w_uv).reshape(w_uv.shape),
+                         f32_to_bf16_bits(w_o).reshape(w_o.shape))

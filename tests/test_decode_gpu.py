@@ -243,12 +243,27 @@ def test_workspace_too_small_is_rejected():
 FULL = [mi.V2_DECODE, mi.RAGGED_SERVING, mi.LONG_CONTEXT, mi.FEW_HEAD_MTP]
 
 
-def sample_sequences(inp, n):
+def straddling_sequences(inp):
+    """Sequences whose pages the decode's split plan gives to more than one
+    worker (their results go through the log-sum-exp merge)."""
+    s = inp.spec
+    W = mla.mla_decode_num_workers(s.B, s.T_q, s.H, s.d_c, s.d_r, mla.MLA_BF16)
+    C = mla.mla_decode_item_cost(s.T_q, s.H, s.d_c, s.d_r, mla.MLA_BF16)
+    fw, lw, _ = mla.mla_decode_split_plan(inp.seqlens, s.T_q, inp.block_table.shape[1], W, C)
+    return [b for b in range(s.B) if fw[b] != lw[b]]
+
+
+def sample_sequences(inp, n, prefer=()):
+    """Both ends, the longest and shortest, up to n // 2 of `prefer`, then
+    seeded random picks, n in all (at least 4)."""
     L = inp.seqlens
     picks = {0, len(L) - 1, int(np.argmax(L)), int(np.argmin(L))}
     rng = np.random.default_rng(inp.spec.seed + 1000)
-    picks |= set(rng.choice(len(L), size=min(n, len(L)), replace=False).tolist())
-    return sorted(picks)[: max(n, 4)]
+    prefer = list(prefer)
+    if prefer:
+        picks |= set(rng.choice(prefer, size=min(n // 2, len(prefer)), replace=False).tolist())
+    rest = [b for b in rng.permutation(len(L)).tolist() if b not in picks]
+    return sorted(picks | set(rest[: max(0, max(n, 4) - len(picks))]))
 
 
 @pytest.mark.parametrize("spec", FULL, ids=[s.name for s in FULL])
@@ -256,8 +271,11 @@ def test_full_size_workload_sampled(spec):
     inp = mi.make_decode_inputs(spec)
     o, lse = run_decode(inp)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
-    n = 2 if spec.B <= 4 else 6
-    batch = sample_sequences(inp, n)
+    # the ragged batch: about 24 sequences, half of them split across workers
+    n = 2 if spec.B <= 4 else 24 if spec is mi.RAGGED_SERVING else 6
+    batch = sample_sequences(inp, n, straddling_sequences(inp) if spec is mi.RAGGED_SERVING else ())
+    if spec is mi.RAGGED_SERVING:
+        assert len(batch) >= 24 and len(set(batch) & set(straddling_sequences(inp))) >= 8
     want_o, want_l = oracle_all(inp, batch=batch)
     for b in batch:
         assert_decode_close(o[b], want_o[b], what=f"{spec.name} seq {b}")
@@ -289,3 +307,38 @@ def test_random_shapes_match_oracle(spec):
     want_o, want_lse = oracle_all(inp)
     assert_decode_close(o, want_o, what=spec.name)
     np.testing.assert_allclose(lse, want_lse, rtol=0, atol=2e-2)
+
+
+# --------------------------------------------------------------------------
+# split invariance: the same batch with 1, 2, 7 and 74 split workers
+# --------------------------------------------------------------------------
+
+SPLIT_SPEC = mi.DecodeSpec("forced_splits", seed=77, B=3, H=128, seqlens=(5000, 300, 12000))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 74])
+def test_forced_splits_match_oracle(splits):
+    """Every split count gives the oracle's result at the decode tolerance;
+    one worker holds everything at 1 split, the long sequences straddle
+    workers at 7 and 74."""
+    s = SPLIT_SPEC
+    inp = mi.make_decode_inputs(s)
+    natural = mla.mla_decode_num_workers(s.B, s.T_q, s.H, s.d_c, s.d_r, mla.MLA_BF16)
+    try:
+        mla.mla_test_force_splits(splits)
+        W = mla.mla_decode_num_workers(s.B, s.T_q, s.H, s.d_c, s.d_r, mla.MLA_BF16)
+        assert W == min(splits, natural)
+        o, lse = run_decode(inp)
+        C = mla.mla_decode_item_cost(s.T_q, s.H, s.d_c, s.d_r, mla.MLA_BF16)
+        fw, lw, _ = mla.mla_decode_split_plan(inp.seqlens, s.T_q, inp.block_table.shape[1], W, C)
+    finally:
+        mla.mla_test_force_splits(0)
+    assert mla.mla_decode_num_workers(s.B, s.T_q, s.H, s.d_c, s.d_r, mla.MLA_BF16) == natural
+    if splits == 1:
+        assert list(fw) == [0, 0, 0] and list(lw) == [0, 0, 0]
+    if splits >= 7:
+        assert lw[2] > fw[2] and lw[0] > fw[0]
+    want_o, want_l = oracle_all(inp)
+    for b in range(s.B):
+        assert_decode_close(o[b], want_o[b], what=f"{splits} splits, seq {b}")
+        np.testing.assert_allclose(lse[b], want_l[b], rtol=0, atol=2e-2)
