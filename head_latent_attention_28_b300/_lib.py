@@ -63,6 +63,8 @@ SIGNATURES = {
     "mla_prefill_kv_rows": (_I, [_I]),
     "mla_prefill_use_rebuild": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "mla_prefill_kv": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P]),
+    "mla_prefill_kv_chunk": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P, _P,
+                                  _P]),
     "mla_prefill_attention": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F,
                                    _P, _P, _P]),
 }
@@ -402,10 +404,13 @@ def mla_prefill_use_rebuild(T_q, L, H, d_c=512, d_r=64, d_h=128, dtype=torch.bfl
     return int(lib().mla_prefill_use_rebuild(T_q, L, H, d_c, d_r, d_h, code))
 
 
-def mla_prefill_kv(kv_cache, block_table, seqlens, w_uk, w_uv, *, H, out=None, stream=None):
+def mla_prefill_kv(kv_cache, block_table, seqlens, w_uk, w_uv, *, H, out=None, stream=None, T_new=0):
     """Rebuild k_nope = W^UK_h c_s, v = W^UV_h c_s ([B, H, R, d_h] bf16) and copy
-    k_rope = R_s k^R_s ([B, R, d_r]) for every cached row.  Returns
-    (k_nope, v, k_rope)."""
+    k_rope = R_s k^R_s ([B, R, d_r]) for every cached row, or with T_new > 0
+    only for the last T_new rows of each sequence into the caller's buffers
+    `out` (mla_prefill_kv_chunk).  Returns (k_nope, v, k_rope)."""
+    if T_new and out is None:
+        raise ValueError("a chunk's rebuild writes into the buffers of the earlier chunks: pass out=")
     num_blocks, page, D = kv_cache.shape
     B, max_blocks = block_table.shape
     HD, d_c = w_uk.shape
@@ -419,13 +424,13 @@ def mla_prefill_kv(kv_cache, block_table, seqlens, w_uk, w_uv, *, H, out=None, s
                torch.empty((B, H, R, d_h), device=dev, dtype=kv_cache.dtype),
                torch.empty((B, R, d_r), device=dev, dtype=kv_cache.dtype))
     k_nope, v, k_rope = out
-    st = lib().mla_prefill_kv(
+    st = lib().mla_prefill_kv_chunk(
         _dev(kv_cache, "kv_cache"), _dtype_code(kv_cache), _dev(block_table, "block_table", torch.int32),
         _dev(seqlens, "seqlens", torch.int32), B, d_c, d_r, page, max_blocks, num_blocks,
-        _dev(w_uk, "w_uk", kv_cache.dtype), _dev(w_uv, "w_uv", kv_cache.dtype), H, d_h,
+        _dev(w_uk, "w_uk", kv_cache.dtype), _dev(w_uv, "w_uv", kv_cache.dtype), H, d_h, int(T_new),
         _dev(k_nope, "k_nope", kv_cache.dtype), _dev(v, "v", kv_cache.dtype),
         _dev(k_rope, "k_rope", kv_cache.dtype), _stream(stream))
-    _check(st, "mla_prefill_kv")
+    _check(st, "mla_prefill_kv_chunk" if T_new else "mla_prefill_kv")
     return k_nope, v, k_rope
 
 

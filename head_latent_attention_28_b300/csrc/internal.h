@@ -123,6 +123,7 @@ struct PrefillKvArgs {
   void* k_nope; void* v;                // [B, H, R, d_h] (head-major)
   void* k_rope;                         // [B, R, d_r]
   unsigned* err;
+  int T_new = 0;                        // > 0: only rows [L - T_new, L) (and zeros past L) are written
 };
 cudaError_t launch_prefill_kv(const PrefillKvArgs& a, cudaStream_t s);
 struct PrefillAttnArgs {

@@ -551,6 +551,15 @@ int mla_prefill_kv(const void* kv_cache, int dtype, const int32_t* block_table,
                    const int32_t* seqlens, int B, int d_c, int d_r, int page_size,
                    int max_blocks_per_seq, int num_blocks, const void* w_uk, const void* w_uv,
                    int H, int d_h, void* k_nope, void* v, void* k_rope, void* stream) {
+  return mla_prefill_kv_chunk(kv_cache, dtype, block_table, seqlens, B, d_c, d_r, page_size, max_blocks_per_seq,
+                              num_blocks, w_uk, w_uv, H, d_h, 0, k_nope, v, k_rope, stream);
+}
+
+int mla_prefill_kv_chunk(const void* kv_cache, int dtype, const int32_t* block_table,
+                         const int32_t* seqlens, int B, int d_c, int d_r, int page_size,
+                         int max_blocks_per_seq, int num_blocks, const void* w_uk, const void* w_uv,
+                         int H, int d_h, int T_new, void* k_nope, void* v, void* k_rope, void* stream) {
+  if (T_new < 0) return MLA_ERR_INVALID_ARG;
   if (B < 0 || H < 1 || d_h < 1 || d_c < 1 || d_r < 0 || !dtype_ok(dtype) ||
       page_size != MLA_PAGE_SIZE || max_blocks_per_seq < 1 || max_blocks_per_seq > (1 << 24) ||
       num_blocks < 1)
@@ -566,7 +575,7 @@ int mla_prefill_kv(const void* kv_cache, int dtype, const int32_t* block_table,
       (long long)num_blocks * MLA_PAGE_SIZE >= (1LL << 31) || (long long)B * R >= (1LL << 31))
     return MLA_ERR_UNSUPPORTED;
   mla::PrefillKvArgs a{kv_cache, block_table, seqlens, B, max_blocks_per_seq, num_blocks, d_c, d_r,
-                       w_uk, w_uv, H, d_h, R, k_nope, v, k_rope, nullptr};
+                       w_uk, w_uv, H, d_h, R, k_nope, v, k_rope, nullptr, T_new};
   cudaError_t e = device_info(&a.err, nullptr);
   if (e != cudaSuccess) return note_cuda(e);
   e = mla::launch_prefill_kv(a, static_cast<cudaStream_t>(stream));

@@ -20,7 +20,10 @@
 //    epilogue of one head overlaps the MMAs of the next).  Four warps convert
 //    to bf16 and write k_nope[b, h, s, :] and v[b, h, s, :]; rows past the
 //    sequence end inside its last tile are written as zeros.  The first head
-//    group also copies the rotated rotary key R_s k^R_s of each row.
+//    group also copies the rotated rotary key R_s k^R_s of each row.  For a
+//    chunk of a chunked prefill only the chunk's rows [L - T_new, L) are
+//    written (tiles below them exit at once); earlier rows stay as the
+//    earlier chunks wrote them.
 //  * prefill_attn_kernel: one CTA per (128-token query tile, head, sequence),
 //    heavy (late) tiles first.  Scores over d_h + d^R_h = 192 dims
 //    (M = 128 queries, N = 128 keys) go into one of two TMEM buffers.  Two
@@ -101,6 +104,10 @@ prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_
   }
   const int r0 = tile * 128;
   if (r0 >= L) return;   // the whole CTA: no row of this sequence here
+  // a chunk's rebuild writes only the new rows [L - T_new, L) (earlier rows
+  // are the caller's from earlier chunks)
+  const int row_lo = a.T_new > 0 ? max(0, L - a.T_new) : 0;
+  if (r0 + 128 <= row_lo) return;
   const int pages = (L + kPage - 1) / kPage;
 
   if (threadIdx.x == 0) {
@@ -200,8 +207,9 @@ prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const int row = r0 + r;
     const bool real = row < L;
+    const bool mine = row >= row_lo;   // rows of earlier chunks are left as they are
     const size_t orow = (size_t)b * a.R + row;
-    if (blockIdx.z == 0) {
+    if (blockIdx.z == 0 && mine) {
       // R_s k^R_s, unchanged from the cache row (zeros past the sequence end)
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.k_rope) + orow * a.d_r);
       int blk = -1;
@@ -237,7 +245,7 @@ prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_
           if (real)
             w = make_uint4(pack_bf16x2(x[8 * i], x[8 * i + 1]), pack_bf16x2(x[8 * i + 2], x[8 * i + 3]),
                            pack_bf16x2(x[8 * i + 4], x[8 * i + 5]), pack_bf16x2(x[8 * i + 6], x[8 * i + 7]));
-          dst[i] = w;
+          if (mine) dst[i] = w;
         }
       }
       tc_fence_before();

@@ -455,6 +455,23 @@ int mla_prefill_kv(const void* kv_cache, int dtype, const int32_t* block_table,
                    int H, int d_h, void* k_nope, void* v, void* k_rope, void* stream);
 
 /*
+ * mla_prefill_kv_chunk -- the same rebuild for one chunk of a chunked
+ * prefill ("Attention, Part 2: MQA, GQA and MLA" and "The MLA equations",
+ * T > 1 new tokens after earlier ones): only the chunk's rows
+ * s in [seqlens[b] - T_new, seqlens[b]) are rebuilt into the caller's
+ * buffers, plus the zero rows past seqlens[b] up to the next multiple of 128;
+ * earlier rows keep what the earlier chunks' calls wrote.  T_new = 0 rebuilds
+ * every row (mla_prefill_kv).  The buffers must have been written for the
+ * earlier rows (by mla_prefill_kv or earlier chunks) and hold zeros or later
+ * rows' data past them.  Errors as mla_prefill_kv, and MLA_ERR_INVALID_ARG for
+ * T_new < 0.
+ */
+int mla_prefill_kv_chunk(const void* kv_cache, int dtype, const int32_t* block_table,
+                         const int32_t* seqlens, int B, int d_c, int d_r, int page_size,
+                         int max_blocks_per_seq, int num_blocks, const void* w_uk, const void* w_uv,
+                         int H, int d_h, int T_new, void* k_nope, void* v, void* k_rope, void* stream);
+
+/*
  * mla_prefill_attention -- causal softmax attention of T_q new tokens per
  * sequence over the rebuilt keys and values.  Query t of sequence b sits at
  * position seqlens[b] - T_q + t (seqlens counts every cached row, the new

@@ -181,3 +181,72 @@ def test_prefill_full_size_sampled():
                                              pos, want_k, want_v, want_kr, spec.softmax_scale, spec.rope_base)
     assert_decode_close(o[0, queries].double().cpu().numpy(), want_o, what="full-size sampled queries")
     np.testing.assert_allclose(lse[0, queries].double().cpu().numpy(), want_lse, rtol=0, atol=2e-2)
+
+
+def test_prefill_lazy_rescale_after_a_jump():
+    """Keys 200-259 scaled by 16: every row's score maximum jumps by far more
+    than 2^8 (8 log2 units) after the first 128-key tile, so the kernel must
+    rescale its output accumulator in tensor memory mid-sequence (the lazy
+    O-rescale).  The jump is checked on the oracle's scores first."""
+    spec = mi.PrefillSpec("pf_lazy_rescale", seed=65, B=1, H=8, T_q=64, seqlens=(512,))
+    inp = mi.make_prefill_inputs(spec, with_kv=True)
+    kn = f64(inp.k_nope_bits)                                   # [B, H, R, d_h]
+    kn[:, :, 200:260, :] *= 16.0
+    inp.k_nope_bits = mi.f32_to_bf16_bits(kn.astype(np.float32)).reshape(kn.shape)
+    pos = positions(inp, 0)
+    qn = f64(inp.q_nope_bits[0])                                # [T, H, d_h]
+    qr = orc.rope(f64(inp.q_rope_bits[0]).transpose(1, 0, 2), pos, spec.rope_base).transpose(1, 0, 2)
+    k = f64(inp.k_nope_bits[0]).transpose(1, 0, 2)              # [R, H, d_h]
+    kr = f64(inp.k_rope_bits[0])                                # [R, d_r]
+    s = spec.softmax_scale * (np.einsum("thd,shd->ths", qn, k) + np.einsum("thd,sd->ths", qr, kr))
+    jump = (s[:, :, 128:int(pos[-1]) + 1].max(axis=2) - s[:, :, :128].max(axis=2)) / np.log(2.0)
+    assert jump.min() > 8.0, jump.min()
+    dev = upload(inp)
+    kd, vd, krd = (bits_to_device(x) for x in (inp.k_nope_bits, inp.v_bits, inp.k_rope_bits))
+    o, lse = mla.mla_prefill_attention(dev["qn"], dev["qr"], kd, vd, krd, dev["sl"],
+                                       max_blocks_per_seq=inp.cache.max_blocks,
+                                       softmax_scale=spec.softmax_scale, rope_base=spec.rope_base)
+    assert mla.mla_check_status() == mla.MLA_OK
+    want_o, want_lse = orc.prefill_attention(qn, f64(inp.q_rope_bits[0]), pos, k,
+                                             f64(inp.v_bits[0]).transpose(1, 0, 2), kr,
+                                             spec.softmax_scale, spec.rope_base)
+    assert_decode_close(o.double().cpu().numpy()[0], want_o, what="lazy rescale")
+    np.testing.assert_allclose(lse.double().cpu().numpy()[0], want_lse, rtol=0, atol=2e-2)
+
+
+
+def test_chunked_prefill_two_chunks_rebuilds_only_new_rows():
+    """Two chunks per sequence: the first rebuilds rows [0, L1) in full, the
+    second (mla_prefill_kv_chunk) only its T_new rows into the same buffers.
+    The buffers then equal one full rebuild at L2 bit for bit, rows of the
+    first chunk untouched by the second call (checked by planting a marker
+    where it must not write), and the second chunk's attention matches the
+    oracle chain."""
+    spec = mi.PrefillSpec("pf_two_chunks", seed=66, B=2, H=12, T_q=130, seqlens=(430, 200))
+    inp = mi.make_prefill_inputs(spec)
+    dev = upload(inp)
+    sl2 = dev["sl"]
+    sl1 = sl2 - spec.T_q                                     # 300 and 70 rows before the chunk
+    k, v, kr = mla.mla_prefill_kv(dev["pool"], dev["bt"], sl1, dev["wuk"], dev["wuv"], H=spec.H)
+    # a marker in rows of the first chunk: the chunk's call must leave it
+    k[:, :, 5, :] = 7.0
+    mla.mla_prefill_kv(dev["pool"], dev["bt"], sl2, dev["wuk"], dev["wuv"], H=spec.H, out=(k, v, kr),
+                       T_new=spec.T_q)
+    assert mla.mla_check_status() == mla.MLA_OK
+    assert torch.all(k[:, :, 5, :] == 7.0)
+    k[:, :, 5, :] = mla.mla_prefill_kv(dev["pool"], dev["bt"], sl1, dev["wuk"], dev["wuv"], H=spec.H)[0][:, :, 5, :]
+    kf, vf, krf = mla.mla_prefill_kv(dev["pool"], dev["bt"], sl2, dev["wuk"], dev["wuv"], H=spec.H)
+    assert mla.mla_check_status() == mla.MLA_OK
+    for b in range(spec.B):          # rows the calls write: up to L2 rounded up to 128
+        n = (int(inp.cache.seqlens[b]) + 127) // 128 * 128
+        assert torch.equal(k[b, :, :n], kf[b, :, :n]) and torch.equal(v[b, :, :n], vf[b, :, :n])
+        assert torch.equal(kr[b, :n], krf[b, :n])
+    o, lse = mla.mla_prefill_attention(dev["qn"], dev["qr"], k, v, kr, sl2,
+                                       max_blocks_per_seq=inp.cache.max_blocks,
+                                       softmax_scale=spec.softmax_scale, rope_base=spec.rope_base)
+    assert mla.mla_check_status() == mla.MLA_OK
+    o, lse = o.double().cpu().numpy(), lse.double().cpu().numpy()
+    for b in range(spec.B):
+        want_o, want_lse = oracle_chain(inp, b)
+        assert_decode_close(o[b], want_o, what=f"second chunk b={b}")
+        np.testing.assert_allclose(lse[b], want_lse, rtol=0, atol=2e-2)
