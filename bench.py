@@ -356,10 +356,12 @@ def device_time_ms(fn, K, stream, dev):
 
 def host_enqueue_us(fn, K, dev):
     """Host-clock time of one call (argument checks, marshalling, launches),
-    with the device busy so that no call waits for it."""
+    with the device busy so that no call waits for it: few enough calls that
+    their launches fit the launch queue (a full queue makes the host wait for
+    the device, which is not host work)."""
     import torch
     torch.cuda.synchronize(dev)
-    torch.cuda._sleep(20_000_000)
+    torch.cuda._sleep(40_000_000)
     t0 = time.perf_counter()
     for i in range(K):
         fn(i)
@@ -416,7 +418,7 @@ class DecodeBench:
         from back-to-back launches of that kernel alone."""
         main_ms = device_time_ms(lambda i: self.step(i, "partial"), K, self.stream, self.dev)
         comb_ms = device_time_ms(lambda i: self.step(i, "combine"), K, self.stream, self.dev)
-        host_us = host_enqueue_us(self.step, min(K, 200), self.dev)
+        host_us = host_enqueue_us(self.step, min(K, 40), self.dev)
         self.check("kernel timing")
         return main_ms, comb_ms, host_us
 
@@ -950,7 +952,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["mla", "reference"], default="mla")
     ap.add_argument("--workload", default=mi.RAGGED_SERVING.name,
-                    choices=sorted(mi.DECODE_WORKLOADS) + sorted(mi.PREFILL_WORKLOADS))
+                    choices=sorted(mi.DECODE_WORKLOADS) + sorted(mi.PREFILL_WORKLOADS) +
+                    sorted(mi.OUT_PROJ_WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
@@ -958,6 +961,16 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload in mi.OUT_PROJ_WORKLOADS:
+        # the output projections alone (one JSON record, one GPU)
+        import torch
+        peaks, peak_src = load_peaks()
+        rec = out_proj_subrecord(mi.OUT_PROJ_WORKLOADS[args.workload], torch.device("cuda", 0), args, peaks, peak_src)
+        if args.impl == "reference":
+            rec = {"impl": "reference", "metric": "output projection GB/s", "unit": "GB/s",
+                   "value": rec.get("cpu_baseline", {}).get("value"), "config": rec["config"]}
+        print(json.dumps(rec), flush=True)
+        return 0
     if args.workload in mi.PREFILL_WORKLOADS:
         pspec = mi.PREFILL_WORKLOADS[args.workload]
         return run_prefill_reference(args, pspec) if args.impl == "reference" else run_prefill(args, pspec)

@@ -208,8 +208,11 @@ def mla_decode_paged(q_lat, kv_cache, block_table, seqlens, *, d_c, softmax_scal
         o_lat = torch.empty((B, T_q, H, d_c), device=dev, dtype=torch.float32)
     if lse is None and want_lse:
         lse = torch.empty((B, T_q, H), device=dev, dtype=torch.float32)
-    fn = {"both": lib().mla_decode_paged, "partial": lib().mla_decode_paged_partial,
-          "combine": lib().mla_decode_combine}[stage]
+    L = lib()
+    fn = (L.mla_decode_paged if stage == "both" else L.mla_decode_paged_partial if stage == "partial"
+          else L.mla_decode_combine if stage == "combine" else None)
+    if fn is None:
+        raise ValueError(f"unknown stage {stage!r}")
     st = fn(
         _dev(q_lat, "q_lat"), _dev(kv_cache, "kv_cache"), _dtype_code(q_lat),
         _dev(block_table, "block_table", torch.int32), _dev(seqlens, "seqlens", torch.int32),

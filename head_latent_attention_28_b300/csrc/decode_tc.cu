@@ -1114,6 +1114,40 @@ cudaError_t make_page_map(CUtensorMap* m, const void* pool, long long num_blocks
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Tensor maps of recent calls, per host thread: a decode step usually passes
+// the same cache, output and workspace as the step before, and encoding the
+// four maps is a noticeable part of a call's host time.
+struct MapCacheEntry {
+  uint64_t key[5];
+  CUtensorMap map;
+  bool used;
+};
+constexpr int kMapCache = 8;
+thread_local MapCacheEntry t_maps[kMapCache];
+thread_local int t_map_next = 0;
+
+template <typename F>
+cudaError_t cached_map(CUtensorMap* m, uint64_t k0, uint64_t k1, uint64_t k2, uint64_t k3, uint64_t k4, F encode) {
+  const uint64_t key[5] = {k0, k1, k2, k3, k4};
+  for (int i = 0; i < kMapCache; ++i) {
+    const MapCacheEntry& c = t_maps[i];
+    if (c.used && c.key[0] == key[0] && c.key[1] == key[1] && c.key[2] == key[2] && c.key[3] == key[3] &&
+        c.key[4] == key[4]) {
+      *m = c.map;
+      return cudaSuccess;
+    }
+  }
+  const cudaError_t e = encode(m);
+  if (e == cudaSuccess) {
+    MapCacheEntry& c = t_maps[t_map_next];
+    t_map_next = (t_map_next + 1) % kMapCache;
+    for (int i = 0; i < 5; ++i) c.key[i] = key[i];
+    c.map = *m;
+    c.used = true;
+  }
+  return e;
+}
+
 constexpr int kMaxDev = 64;
 std::atomic<int> g_max_clusters[kMaxDev];
 std::atomic<bool> g_attr_set[kMaxDev];
@@ -1178,15 +1212,21 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   e = set_smem_attr(dev);
   if (e != cudaSuccess) return e;
   CUtensorMap tm_page, tm_v, tm_o, tm_ws;
-  e = make_page_map(&tm_page, a.cache, a.num_blocks, 9);
+  const uint64_t cache_p = reinterpret_cast<uintptr_t>(a.cache);
+  e = cached_map(&tm_page, 1, cache_p, (uint64_t)a.num_blocks, 9, 0,
+                 [&](CUtensorMap* m) { return make_page_map(m, a.cache, a.num_blocks, 9); });
   if (e != cudaSuccess) return e;
-  e = make_page_map(&tm_v, a.cache, a.num_blocks, 8);   // the 512 latent dims of a page
+  e = cached_map(&tm_v, 1, cache_p, (uint64_t)a.num_blocks, 8, 0,   // the 512 latent dims of a page
+                 [&](CUtensorMap* m) { return make_page_map(m, a.cache, a.num_blocks, 8); });
   if (e != cudaSuccess) return e;
   // outputs and split parts: [rows, 512] fp32, written in 32 x 32 boxes
   const uint64_t rows = (uint64_t)a.T_q * a.H;
-  e = make_map(&tm_o, a.o, (uint64_t)a.d_c, (uint64_t)a.B * rows, 32, 32, true);
+  const uint64_t o_rows = (uint64_t)a.B * rows, ws_rows = ((uint64_t)a.B * a.G + a.W) * a.SR;
+  e = cached_map(&tm_o, 2, reinterpret_cast<uintptr_t>(a.o), (uint64_t)a.d_c, o_rows, 0,
+                 [&](CUtensorMap* m) { return make_map(m, a.o, (uint64_t)a.d_c, o_rows, 32, 32, true); });
   if (e != cudaSuccess) return e;
-  e = make_map(&tm_ws, a.ws_o, (uint64_t)a.d_c, ((uint64_t)a.B * a.G + a.W) * a.SR, 32, 32, true);
+  e = cached_map(&tm_ws, 2, reinterpret_cast<uintptr_t>(a.ws_o), (uint64_t)a.d_c, ws_rows, 0,
+                 [&](CUtensorMap* m) { return make_map(m, a.ws_o, (uint64_t)a.d_c, ws_rows, 32, 32, true); });
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * a.W);
