@@ -227,7 +227,7 @@ def mla_decode_paged(q_lat, kv_cache, block_table, seqlens, *, d_c, softmax_scal
 
 def mla_decode_paged_noalloc(q_lat, kv_cache, block_table, seqlens, *, d_c, softmax_scale,
                              causal=False, o_lat=None, lse=None, want_lse=True, stream=None):
-    """mla_decode_paged with the library's own 32 MiB device scratch instead of a
+    """mla_decode_paged with the library's own 64 MiB device scratch instead of a
     caller workspace (raises MLAError(MLA_ERR_WORKSPACE) for larger shapes), for
     callers that cannot get device memory at the call (no allocator of their
     own, or all free memory already given to the cache pool).  Calls that
