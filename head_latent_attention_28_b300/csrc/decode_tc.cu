@@ -37,15 +37,18 @@
 //    division) and round the probabilities to bf16.  Each page's
 //    probabilities and per-row info (reference max, sum of the rounded
 //    probabilities) are written from registers into this worker's message
-//    ring in global memory (L2), already in the swizzled layout the value
-//    CTA's MMA reads; a heavy page (a probability not small against its
+//    ring in global memory (L2), already in the layout the value CTA's MMA
+//    reads: chunk-major (16-byte chunk c of row r at c * 2048 + r * 16, the
+//    K-major operand layout without swizzle), so each store instruction of a
+//    warp writes 512 contiguous bytes; a heavy page (a probability not small against its
 //    row's running sum) also sends the low bf16 parts.  A signaler warp sends
 //    the page's flags to the value CTA with one remote store and an mbarrier
 //    arrive (release at cluster scope).
 //  * CTA 1, the value CTA, keeps the 128 x 512 fp32 output in tensor memory.
-//    Its producer loads the 512 latent dims of the same pages (one 64 KB box
-//    per page, an L2 hit: the score CTA's copy marks them evict-last) into a
-//    ring of two, and copies each page's message with one or two bulk copies
+//    Its producer loads the 512 latent dims of the same pages (two 32 KB
+//    boxes per page, in flight together: one copy alone streams slowly; an L2
+//    hit: the score CTA's copy marks them evict-last) into a ring of two, and
+//    copies each page's message with one or two bulk copies
 //    into a ring of three probability units and two low-part buffers.  The
 //    MMA warp accumulates O += P . V (A = P from shared memory, B = V
 //    MN-major, N = 256).  Four row warps zero the low parts of row quarters
@@ -511,6 +514,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
             if (ok2) {
               mbar_arrive_expect_tx(&ctl.v_full[vs], kVBytes);
               tma_load_4d(smem + kOffV + vs * kVBytes, &tm_v, &ctl.v_full[vs], 0, 0, 0, y, pol);
+              tma_load_4d(smem + kOffV + vs * kVBytes + kVBytes / 2, &tm_v, &ctl.v_full[vs], 0, 0, 0, y + 4, pol);
               ++g_issue;
             }
             // page g's message: probabilities and row info into unit g % 3,
@@ -648,18 +652,22 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
               // B = V (MN-major SW128): 64-dim chunks 1 KB apart along N,
               // 8-token groups 8 KB apart along K; a K-step is 16 tokens
               const uint64_t bv = sdesc_sw128(smem_u32(smem + kOffV + vs * kVBytes), 1024, 8192);
-              const uint64_t ah = sdesc_sw128(smem_u32(smem + kOffHi + (g % kHiUnits) * kHiBytes), 16, 1024);
-              const uint64_t al = sdesc_sw128(smem_u32(smem + kOffLo + ((flags >> 8) & 1u) * kPBytes), 16, 1024);
+              // A = P chunk-major: 16-byte chunk c (tokens 8c .. 8c + 7) of row r at
+              // c * 2048 + r * 16, the canonical K-major layout without swizzle
+              // (core matrices 2 KB apart along K, 128 B apart along M); a K-step
+              // of 16 tokens is two chunks, 4 KB
+              const uint64_t ah = sdesc_noswz(smem_u32(smem + kOffHi + (g % kHiUnits) * kHiBytes), 2048, 128);
+              const uint64_t al = sdesc_noswz(smem_u32(smem + kOffLo + ((flags >> 8) & 1u) * kPBytes), 2048, 128);
 #pragma unroll
               for (int nh = 0; nh < 2; ++nh) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)   // 64 tokens, K-step 16
-                  mma_ss(tmem + nh * 256, ah + (uint64_t)(2 * kk), bv + (uint64_t)(1024 * kk + 256 * nh), idPV,
+                  mma_ss(tmem + nh * 256, ah + (uint64_t)(256 * kk), bv + (uint64_t)(1024 * kk + 256 * nh), idPV,
                          (i > 0 || kk > 0) ? 1u : 0u);
                 if (lo) {
 #pragma unroll
                   for (int kk = 0; kk < 4; ++kk)   // the same V rows, A = low parts
-                    mma_ss(tmem + nh * 256, al + (uint64_t)(2 * kk), bv + (uint64_t)(1024 * kk + 256 * nh), idPV, 1u);
+                    mma_ss(tmem + nh * 256, al + (uint64_t)(256 * kk), bv + (uint64_t)(1024 * kk + 256 * nh), idPV, 1u);
                 }
               }
               mma_commit(&ctl.v_empty[vs]);
@@ -760,8 +768,8 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
           unsigned char* msg = gmsg + (size_t)gs * kMsgBytes;
           {
             // probabilities rounded to bf16 (and the residuals rounded again),
-            // rows in the layout the value CTA's MMA reads (K-major SW128:
-            // 16-byte chunk c of row r at c ^ (r & 7))
+            // in the layout the value CTA's MMA reads (K-major, no swizzle,
+            // chunk-major)
             const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
             float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
@@ -782,7 +790,11 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
                   ps1 += __uint_as_float(hi_half_f(pl[e2]));
                 }
               }
-              const int off = r * 128 + ((c ^ (r & 7)) << 4);
+              // chunk-major (chunk c of row r at c * 2048 + r * 16): each store
+              // instruction of the warp writes 512 contiguous bytes.  (Rows of
+              // 128 bytes, one 16-byte piece per lane and instruction, cost the
+              // score SM ~20%: the MMA-issuing thread stalls behind them.)
+              const int off = c * 2048 + r * 16;
               *reinterpret_cast<uint4*>(msg + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
               if (lo) *reinterpret_cast<uint4*>(msg + kHiBytes + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
             }
@@ -857,9 +869,9 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
             const float2 info = *reinterpret_cast<const float2*>(smem + kOffHi + u * kHiBytes + kPBytes + r * 8);
             if ((fl & kFlagLo) && !(fl & (16u << q4))) {
               // this row quarter sent no low parts: its rows of the buffer are zero
-              uint4* lz = reinterpret_cast<uint4*>(smem + kOffLo + lb * kPBytes + q4 * 4096);
+              uint4* lz = reinterpret_cast<uint4*>(smem + kOffLo + lb * kPBytes);   // chunk-major
 #pragma unroll
-              for (int c = 0; c < 8; ++c) lz[32 * c + lane] = make_uint4(0u, 0u, 0u, 0u);
+              for (int c = 0; c < 8; ++c) lz[128 * c + r] = make_uint4(0u, 0u, 0u, 0u);
               fence_proxy_async_smem();    // the value MMA reads these bytes
             }
             __syncwarp();
@@ -1103,10 +1115,11 @@ cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t r
 // 8 tokens of a group, 9 chunks, num_blocks * 8 groups).  A box of `chunks`
 // chunks starting at chunk c0 and 8 groups is one page (or its latent
 // half), laid out [group][chunk][token][dim] in shared memory.
-cudaError_t make_page_map(CUtensorMap* m, const void* pool, long long num_blocks, uint32_t chunks) {
+cudaError_t make_page_map(CUtensorMap* m, const void* pool, long long num_blocks, uint32_t chunks,
+                          uint32_t groups = 8) {
   cuuint64_t dims[4] = {64, 8, 9, (cuuint64_t)num_blocks * 8};
   cuuint64_t strides[3] = {576 * 2, 64 * 2, 8 * 576 * 2};
-  cuuint32_t box[4] = {64, 8, chunks, 8};
+  cuuint32_t box[4] = {64, 8, chunks, groups};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims, strides,
                         box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1216,8 +1229,8 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   e = cached_map(&tm_page, 1, cache_p, (uint64_t)a.num_blocks, 9, 0,
                  [&](CUtensorMap* m) { return make_page_map(m, a.cache, a.num_blocks, 9); });
   if (e != cudaSuccess) return e;
-  e = cached_map(&tm_v, 1, cache_p, (uint64_t)a.num_blocks, 8, 0,   // the 512 latent dims of a page
-                 [&](CUtensorMap* m) { return make_page_map(m, a.cache, a.num_blocks, 8); });
+  e = cached_map(&tm_v, 1, cache_p, (uint64_t)a.num_blocks, 8, 4,   // the 512 latent dims of half a page
+                 [&](CUtensorMap* m) { return make_page_map(m, a.cache, a.num_blocks, 8, 4); });
   if (e != cudaSuccess) return e;
   // outputs and split parts: [rows, 512] fp32, written in 32 x 32 boxes
   const uint64_t rows = (uint64_t)a.T_q * a.H;

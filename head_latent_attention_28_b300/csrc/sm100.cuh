@@ -357,6 +357,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
   return d;
 }
 
+// Shared-memory matrix descriptor, no swizzle (K-major: core matrices of 8
+// rows x 16 bytes, rows 16 bytes apart).  lbo: bytes between core matrices
+// adjacent along K; sbo: along M/N.
+__device__ __forceinline__ uint64_t sdesc_noswz(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;                 // descriptor version (sm_100)
+  return d;                               // layout type 0: no swizzle
+}
+
 // 32 lanes x 32 bit, 64 consecutive columns per thread
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   uint32_t* r = reinterpret_cast<uint32_t*>(v);
