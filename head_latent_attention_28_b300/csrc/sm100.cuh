@@ -230,6 +230,12 @@ __device__ __forceinline__ void tma_store_2d(const void* desc, const void* src, 
                "r"(smem_u32(src)), "r"(c0), "r"(c1)
                : "memory");
 }
+// 3-D tiled store, as tma_store_2d
+__device__ __forceinline__ void tma_store_3d(const void* desc, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(desc),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* desc, uint64_t* bar, int c0,
                                             int c1, uint64_t cache_hint) {
   asm volatile(

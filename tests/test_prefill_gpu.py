@@ -121,6 +121,44 @@ def test_prefill_chain_matches_oracle(spec):
         np.testing.assert_allclose(lse[b], want_lse, rtol=0, atol=2e-2)
 
 
+def test_prefill_attention_schedules_agree():
+    """The attention kernel is persistent: its CTAs take work items from a
+    counter kept per stream (and zeroed by the kernel for the next launch), or
+    in a fixed order on the per-thread default stream.  256 items over at
+    most one CTA per SM: repeated launches, fresh streams and the fixed order
+    all give the same bits."""
+    from cuda.bindings import runtime as cudart
+    spec = CASES[3]
+    inp = mi.make_prefill_inputs(spec, with_kv=True)
+    dev = upload(inp)
+    kn, vv, kr = (bits_to_device(x) for x in (inp.k_nope_bits, inp.v_bits, inp.k_rope_bits))
+
+    def run(stream=None):
+        o, lse = mla.mla_prefill_attention(dev["qn"], dev["qr"], kn, vv, kr, dev["sl"],
+                                           max_blocks_per_seq=inp.cache.max_blocks,
+                                           softmax_scale=spec.softmax_scale, rope_base=spec.rope_base,
+                                           stream=stream)
+        torch.cuda.synchronize()
+        if stream is not None:
+            cudart.cudaStreamSynchronize(stream)
+        return o, lse
+
+    torch.cuda.synchronize()
+    ref_o, ref_lse = run()
+    outs = [run(), run(2)]                      # 2 = cudaStreamPerThread: the fixed order
+    streams = []
+    for _ in range(3):
+        err, st = cudart.cudaStreamCreate()
+        assert err == cudart.cudaError_t.cudaSuccess
+        streams.append(st)
+        outs += [run(int(st)), run(int(st))]
+    for st in streams:
+        cudart.cudaStreamDestroy(st)
+    assert mla.mla_check_status() == mla.MLA_OK
+    for o, lse in outs:
+        assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+
+
 def test_prefill_bad_length_reports_and_writes_zeros():
     spec = mi.PrefillSpec("pf_bad_len", seed=64, B=2, H=4, T_q=5, seqlens=(5, 300))
     inp = mi.make_prefill_inputs(spec, with_kv=True)
