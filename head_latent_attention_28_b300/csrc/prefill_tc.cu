@@ -25,23 +25,25 @@
 //    written (tiles below them exit at once); earlier rows stay as the
 //    earlier chunks wrote them.
 //  * prefill_attn_kernel: persistent, one CTA per SM, each taking work items
-//    (a 128-token query tile of one head of one sequence; the items of a
-//    head one after another, latest query tile first) from a counter until
-//    none are left.  Scores over d_h + d^R_h = 192 dims (M = 128 queries,
-//    N = 128 keys) go into one of two TMEM buffers.  Two groups of four
-//    softmax warps split every key tile in halves of 64 keys; each half runs
-//    its own base-2 online softmax with a lazy running max (its output is
-//    rescaled only when a row maximum grows by more than 2^8; exact after the
-//    final division), writes its bf16 probabilities over its own scores in
-//    TMEM and accumulates O_h += P_h . V_h in its own TMEM accumulator (P read
-//    from TMEM as the tcgen05.mma A operand).  The halves merge once, at the
-//    end.  Key and value tiles stream through two-stage rings that run on
-//    from one item into the next, so the scores of tile j + 1 run while the
-//    softmax of tile j does, and the next item's first tiles load while the
-//    current one finishes.  The query's rotary half is copied unrotated and
-//    rotated in place (the same fixed-point angle table as the query
-//    absorption).  Outputs leave through a small per-warp buffer so that each
-//    store instruction writes 16 rows x 32 contiguous bytes.
+//    (query tiles 2p and 2p + 1 of one head of one sequence; the items of a
+//    head one after another, latest pair first) from a counter until none
+//    are left.  Both query tiles of an item share every key and value tile,
+//    so each tile brought into shared memory feeds twice the MMA work of one
+//    query tile.  Scores over d_h + d^R_h = 192 dims (M = 128 queries,
+//    N = 128 keys) of query tile x go into TMEM columns 128 x; four softmax
+//    warps per query tile (thread = query row) run a base-2 online softmax
+//    with a lazy running max (the output is rescaled only when a row maximum
+//    grows by more than 2^8; exact after the final division), write bf16
+//    probabilities over the second half of their scores and accumulate
+//    O_x += P_x V in TMEM (P read from TMEM as the tcgen05.mma A operand).
+//    The MMA issuer interleaves the two query tiles (S_0(j+1) runs while
+//    tile 1's softmax of key tile j does).  Key tiles stream through a
+//    two-stage ring and value tiles through one buffer, each with a producer
+//    warp of its own; both run on from one item into the next.  The query's
+//    rotary half is copied unrotated and rotated in place (the same
+//    fixed-point angle table as the query absorption).  Outputs leave through
+//    the value buffer once an item's MMAs are done, so that each store
+//    instruction writes 4 rows x 128 contiguous bytes.
 // Every mbarrier wait is bounded (2 s): on expiry the kernel records
 // MLA_ERR_TIMEOUT, lets its copies and MMAs finish, frees TMEM and returns.
 #include <cuda.h>
@@ -291,16 +293,14 @@ prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_
 // ---------------------------------------------------------------------------
 constexpr int kAtQ = 3 * kBox16;         // query tile: q_nope (2 boxes), rotated q_rope (1 box)
 constexpr int kAtK = 3 * kBox16;         // key tile: k_nope (2 boxes), k_rope (1 box)
-constexpr int kAtV = 2 * kBox16;         // value tile
-constexpr int kAtStages = 2;
-constexpr int kAtOffK = kAtQ;
+constexpr int kAtV = 2 * kBox16;         // value tile (its buffer also stages the outputs)
+constexpr int kAtStages = 2;             // key ring
+constexpr int kAtOffK = 2 * kAtQ;
 constexpr int kAtOffV = kAtOffK + kAtStages * kAtK;
-constexpr int kAtOffE = kAtOffV + kAtStages * kAtV;   // per-warp output transpose buffers
-constexpr int kAtEpi = 1024;             // 32 rows x 8 fp32 per row warp
-constexpr int kAtSmem = kAtOffE + 8 * kAtEpi + 1024;
-constexpr int kAtThreads = 320;          // 10 warps: producer, MMA issuer, 2 x 4 row warps
-// TMEM columns: two score buffers (each half's probabilities overwrite the
-// first 32 columns of its half of the buffer), then the two halves' outputs
+constexpr int kAtSmem = kAtOffV + kAtV + 1024;
+constexpr int kAtThreads = 352;          // 11 warps: key producer, MMA issuer, 2 x 4 row warps, value producer
+// TMEM columns: the scores of query tile X at 128 X (its probabilities
+// overwrite the last 64 columns), its output accumulator at 256 + 128 X
 constexpr uint32_t kTS = 0, kTO = 256;
 constexpr int kAtSlots = 64;             // work counters: one per stream that launches the kernel
 
@@ -308,36 +308,42 @@ constexpr int kAtSlots = 64;             // work counters: one per stream that l
 // finished (the last CTA to finish zeroes both for the next launch)
 __device__ unsigned g_at_work[kAtSlots][2];
 
-// a work item: one 128-token query tile of one head of one sequence.  Items
-// are numbered head by head (so the CTAs running at any time share the keys
-// and values of a few heads in L2), latest query tile first within a head
-// (it sees the most keys).
+// a work item: query tiles 2p and 2p + 1 (the second may not exist) of one
+// head of one sequence.  Items are numbered head by head (so the CTAs running
+// at any time share the keys and values of a few heads in L2), latest pair
+// first within a head (it sees the most keys).
 struct AtItem {
-  int qt, h, b;
+  int p, h, b;
 };
-__device__ __forceinline__ AtItem at_item(int i, int n_qt, int H) {
-  const int hb = i / n_qt;
-  return AtItem{n_qt - 1 - (i - hb * n_qt), hb % H, hb / H};
+__device__ __forceinline__ AtItem at_item(int i, int n_pairs, int H) {
+  const int hb = i / n_pairs;
+  return AtItem{n_pairs - 1 - (i - hb * n_pairs), hb % H, hb / H};
 }
-// key tiles a query tile sees (0 for a sequence of invalid length): keys 0 ..
-// position of the tile's last query
-__device__ __forceinline__ int at_key_tiles(const PrefillAttnArgs& a, const AtItem& it) {
-  const int L = a.seqlens[it.b];
-  if (L < a.T_q || L > a.max_len) return 0;
-  const int last_t = min(it.qt * 128 + 127, a.T_q - 1);
+// key tiles query tile qt sees (0 past the last tile, or for a sequence of
+// invalid length): keys 0 .. position of the tile's last query
+__device__ __forceinline__ int at_key_tiles(const PrefillAttnArgs& a, int b, int qt) {
+  const int L = a.seqlens[b];
+  if (qt * 128 >= a.T_q || L < a.T_q || L > a.max_len) return 0;
+  const int last_t = min(qt * 128 + 127, a.T_q - 1);
   return (L - a.T_q + last_t) / 128 + 1;
 }
 
 // Persistent: each CTA takes work items (from a counter when `slot` >= 0, else
-// items blockIdx.x, blockIdx.x + gridDim.x, ...) until none are left.  The
+// items blockIdx.x, blockIdx.x + gridDim.x, ...) until none are left.  The key
 // producer publishes each item to the other roles through a two-entry ring.
-// Key and value tiles stream through two-stage rings that run on from one item
-// into the next; the next item's query tile is loaded as soon as the last
-// score MMA of the current one has read the old one, and it is rotated by the
-// row warps between the current item's last softmax and its output stores, so
-// that the next item's first score MMAs overlap those stores.  The first value
-// MMAs of an item wait until the row warps have read the previous item's
-// outputs out of TMEM.
+// An item's two query tiles share every key and value tile (half the bytes
+// per score of one tile per CTA).  The MMA issuer runs S_0(0) S_1(0), then per
+// key tile j PV_0(j) S_0(j+1) PV_1(j) S_1(j+1), so that one query tile's
+// scores run while the other's softmax does.  Key tiles stream through a
+// two-stage ring and value tiles through one buffer (shared memory holds no
+// more beside two query tiles), each with a producer warp of its own; both run
+// on from one item into the next.  The next item's query tiles load as soon as
+// the last score MMA of the current one has read the old ones; the row warps
+// rotate them between their last softmax and their output stores, so the next
+// item's first score MMAs overlap those stores.  The outputs leave through the
+// value buffer (free once the item's last value MMAs are done, refilled once
+// every row warp is done with it), so that each store instruction writes
+// 4 rows x 128 bytes.
 __global__ void __launch_bounds__(kAtThreads, 1)
 prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ CUtensorMap tm_k,
@@ -346,10 +352,8 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
   extern __shared__ uint8_t at_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ uint64_t q_full, q_ready, q_free, k_full[kAtStages], k_empty[kAtStages], v_full[kAtStages],
-      v_empty[kAtStages], s_full[2], p_full[2], pv_done[2], grp, o_free, mma_final, item_full[2],
-      item_empty[2];
-  __shared__ float row_m[2][128], row_l[2][128];   // per-half row statistics for the final merge
+  __shared__ uint64_t q_full, q_ready[2], q_free, k_full[kAtStages], k_empty[kAtStages], v_full, v_empty,
+      s_full[2], p_full[2], pv_done[2], o_free[2], item_done, epi_done, mma_final, item_full[2], item_empty[2];
   __shared__ int item_id[2];
   __shared__ uint32_t tbase;
   __shared__ int abort_raw, never_raw;
@@ -358,28 +362,30 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
   volatile int* items = item_id;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_qt = (a.T_q + 127) / 128;
+  const int n_pairs = (n_qt + 1) / 2;
 
   if (threadIdx.x == 0) {
     abort_raw = 0;
     never_raw = 0;
     mbar_init(&q_full, 1);
-    mbar_init(&q_ready, 8);
     mbar_init(&q_free, 1);
     for (int s = 0; s < kAtStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 8);
-      mbar_init(&pv_done[s], 1);
-      mbar_init(&item_full[s], 1);
-      mbar_init(&item_empty[s], 9);   // the MMA issuer and the 8 row warps
+    mbar_init(&v_full, 1);
+    mbar_init(&v_empty, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&q_ready[x], 4);
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 4);
+      mbar_init(&pv_done[x], 1);
+      mbar_init(&o_free[x], 4);
+      mbar_init(&item_full[x], 1);
+      mbar_init(&item_empty[x], 10);   // the MMA issuer, the 8 row warps and the value producer
     }
-    mbar_init(&grp, 8);
-    mbar_init(&o_free, 8);
+    mbar_init(&item_done, 1);
+    mbar_init(&epi_done, 8);
     mbar_init(&mma_final, 1);
     fence_mbar_init_cluster();
   }
@@ -388,10 +394,9 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tbase;
-  uint8_t* sQ = smem;
   uint8_t* sK = smem + kAtOffK;
   uint8_t* sV = smem + kAtOffV;
-  uint32_t n_k = 0, n_v = 0, n_q = 0;          // producer: key, value and query tiles issued
+  uint32_t n_k = 0, n_v = 0, n_q = 0;          // producers: key, value and query loads issued
 
   // item n of this CTA, as published by the producer (-1: no more work)
   const auto fetch = [&](uint32_t n, int* out) -> bool {
@@ -415,11 +420,12 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
         items[n & 1] = i;
         mbar_arrive(&item_full[n & 1]);
         if (i < 0) break;
-        const AtItem it = at_item(i, n_qt, a.H);
-        const int n_kt = at_key_tiles(a, it);
+        const AtItem it = at_item(i, n_pairs, a.H);
+        const int nk0 = at_key_tiles(a, it.b, 2 * it.p), nk1 = at_key_tiles(a, it.b, 2 * it.p + 1);
+        const int n_kt = max(nk0, nk1);
         const int krow0 = (it.b * a.H + it.h) * a.R;   // first row of (sequence, head) in k_nope and v
         const int rrow0 = it.b * a.R;                  // first row of the sequence in k_rope
-        const int n_tok = it.b * a.T_q + it.qt * 128;  // the tile's first query row in q_nope
+        const int tok0 = it.b * a.T_q + 256 * it.p;    // the first query tile's first row in q_nope
         for (int j = 0; ok && j < n_kt; ++j) {
           const uint32_t s = n_k & 1;
           ok = n_k < 2 || mbar_wait(&k_empty[s], ((n_k >> 1) - 1) & 1, abort_flag, kPfWaitNs);
@@ -430,21 +436,19 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
           tma_load_2d(kd + 2 * kBox16, &tm_kr, &k_full[s], 0, rrow0 + 128 * j, pol_kv);
           ++n_k;
           if (j == 0) {
-            // the query tile, once the last score MMA of the previous item has read the old one
+            // the query tiles, once the last score MMA of the previous item has read the old ones
             ok = n_q == 0 || mbar_wait(&q_free, (n_q - 1) & 1, abort_flag, kPfWaitNs);
             if (!ok) break;
-            mbar_arrive_expect_tx(&q_full, 3 * kBox16);
-            tma_load_3d(sQ, &tm_q, &q_full, 0, it.h, n_tok, pol_q);
-            tma_load_3d(sQ + kBox16, &tm_q, &q_full, 64, it.h, n_tok, pol_q);
-            tma_load_3d(sQ + 2 * kBox16, &tm_qr, &q_full, 0, it.h, n_tok, pol_q);   // rotated in place
+            const int nt = nk1 > 0 ? 2 : 1;
+            mbar_arrive_expect_tx(&q_full, nt * kAtQ);
+            for (int x = 0; x < nt; ++x) {
+              uint8_t* qd = smem + x * kAtQ;
+              tma_load_3d(qd, &tm_q, &q_full, 0, it.h, tok0 + 128 * x, pol_q);
+              tma_load_3d(qd + kBox16, &tm_q, &q_full, 64, it.h, tok0 + 128 * x, pol_q);
+              tma_load_3d(qd + 2 * kBox16, &tm_qr, &q_full, 0, it.h, tok0 + 128 * x, pol_q);   // rotated in place
+            }
             ++n_q;
           }
-          const uint32_t sv = n_v & 1;
-          ok = n_v < 2 || mbar_wait(&v_empty[sv], ((n_v >> 1) - 1) & 1, abort_flag, kPfWaitNs);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&v_full[sv], kAtV);
-          tma_load_3d(sV + sv * kAtV, &tm_v, &v_full[sv], 0, krow0 + 128 * j, 0, pol_kv);
-          ++n_v;
         }
       }
       if (!ok) {
@@ -454,65 +458,85 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // MMAs issued by one thread run in issue order: the scores of tile
-      // g + 2 overwrite the buffer that holds the probabilities of tile g only
-      // after the value MMAs of tile g (issued earlier) have read them
+      // MMAs issued by one thread run in issue order: the scores of query
+      // tile x for key tile j + 1 overwrite its probabilities of tile j only
+      // after the value MMAs of tile j (issued earlier) have read them
       const uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);   // Q, K both K-major
       const uint32_t idO = idesc_bf16_f32(128, 128, 0, 1);   // P from TMEM, V MN-major
       bool ok = true;
-      uint32_t g0 = 0, nq = 0;                 // key tiles and query tiles consumed
+      uint32_t g = 0, nq = 0;                  // key tiles and items with key tiles consumed
+      uint32_t cnt0 = 0, cnt1 = 0;             // key tiles each query tile has consumed
       for (uint32_t n = 0; ok; ++n) {
         int i;
         ok = fetch(n, &i);
         if (!ok) break;
         mbar_arrive(&item_empty[n & 1]);
         if (i < 0) break;
-        const int n_kt = at_key_tiles(a, at_item(i, n_qt, a.H));
+        const AtItem it = at_item(i, n_pairs, a.H);
+        const int nk0 = at_key_tiles(a, it.b, 2 * it.p), nk1 = at_key_tiles(a, it.b, 2 * it.p + 1);
+        const int n_kt = max(nk0, nk1);
         if (n_kt == 0) continue;
-        ok = mbar_wait(&q_full, nq & 1, abort_flag, kPfWaitNs) &&
-             mbar_wait(&q_ready, nq & 1, abort_flag, kPfWaitNs);
-        for (int j = 0; ok && j <= n_kt; ++j) {
-          if (j < n_kt) {
-            const uint32_t g = g0 + j, s = g & 1;
-            ok = mbar_wait(&k_full[s], (g >> 1) & 1, abort_flag, kPfWaitNs);
-            if (!ok) break;
-            tc_fence_after();
-            const uint8_t* kd = sK + s * kAtK;
+        ok = mbar_wait(&q_full, nq & 1, abort_flag, kPfWaitNs);
+        // key tile j is seen by query tile x when j < nk_x (nk1 >= nk0 unless
+        // the second tile does not exist)
+        const auto sees = [&](int x, int j) { return j < (x ? nk1 : nk0); };
+        // S_x(j): scores of query tile x against key tile j; the first score
+        // MMA of a key tile waits for it, the last frees its slot
+        const auto score = [&](int x, int j) -> bool {
+          const uint32_t gj = g + j, s = gj & 1;
+          if ((x == 0 || !sees(0, j)) && !mbar_wait(&k_full[s], (gj >> 1) & 1, abort_flag, kPfWaitNs)) return false;
+          if (j == 0 && !mbar_wait(&q_ready[x], nq & 1, abort_flag, kPfWaitNs)) return false;
+          tc_fence_after();
+          const uint8_t* qd = smem + x * kAtQ;
+          const uint8_t* kd = sK + s * kAtK;
 #pragma unroll
-            for (int kk = 0; kk < 12; ++kk) {
-              const uint64_t ad = sdesc_sw128(smem_u32(sQ + (kk >> 2) * kBox16 + (kk & 3) * 32), 16, 1024);
-              const uint64_t bd = sdesc_sw128(smem_u32(kd + (kk >> 2) * kBox16 + (kk & 3) * 32), 16, 1024);
-              mma_ss(tmem + kTS + s * 128, ad, bd, idS, kk > 0 ? 1 : 0);
-            }
+          for (int kk = 0; kk < 12; ++kk) {
+            const uint64_t ad = sdesc_sw128(smem_u32(qd + (kk >> 2) * kBox16 + (kk & 3) * 32), 16, 1024);
+            const uint64_t bd = sdesc_sw128(smem_u32(kd + (kk >> 2) * kBox16 + (kk & 3) * 32), 16, 1024);
+            mma_ss(tmem + kTS + 128 * x, ad, bd, idS, kk > 0 ? 1 : 0);
+          }
+          mma_commit(&s_full[x]);
+          if (x == 1 || !sees(1, j)) {
             mma_commit(&k_empty[s]);
-            mma_commit(&s_full[s]);
             if (j == n_kt - 1) mma_commit(&q_free);
           }
-          if (j >= 1) {
-            const uint32_t g = g0 + j - 1, s = g & 1;
-            ok = mbar_wait(&p_full[s], (g >> 1) & 1, abort_flag, kPfWaitNs) &&
-                 mbar_wait(&v_full[s], (g >> 1) & 1, abort_flag, kPfWaitNs);
-            // the first value MMAs of an item overwrite the outputs: the row
-            // warps must have read the previous item's
-            if (ok && j == 1 && nq > 0) ok = mbar_wait(&o_free, (nq - 1) & 1, abort_flag, kPfWaitNs);
-            if (!ok) break;
-            tc_fence_after();
-            const uint8_t* vd = sV + s * kAtV;
-            // half hf: keys 64 hf .. 64 hf + 63 of the tile, its probabilities in
-            // the first 32 columns of its half of the score buffer, into O_hf
+          return true;
+        };
+        // O_x += P_x(j) V(j); the first value MMA of a tile waits for it, the
+        // last frees the value buffer
+        const auto value = [&](int x, int j) -> bool {
+          const uint32_t gj = g + j;
+          if ((x == 0 || !sees(0, j)) && !mbar_wait(&v_full, gj & 1, abort_flag, kPfWaitNs)) return false;
+          if (!mbar_wait(&p_full[x], ((x ? cnt1 : cnt0) + j) & 1, abort_flag, kPfWaitNs)) return false;
+          // the first value MMAs of an item overwrite the output: the row
+          // warps must have read the previous item's
+          if (j == 0 && nq > 0 && !mbar_wait(&o_free[x], (nq - 1) & 1, abort_flag, kPfWaitNs)) return false;
+          tc_fence_after();
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-              for (int k4 = 0; k4 < 4; ++k4) {   // 16 keys per step
-                const uint64_t bd = sdesc_sw128(smem_u32(vd + (4 * hf + k4) * 2048), kBox16, 1024);
-                mma_ts(tmem + kTO + hf * 128, tmem + kTS + s * 128 + hf * 64 + k4 * 8, bd, idO,
-                       (j > 1 || k4 > 0) ? 1 : 0);
-              }
-            mma_commit(&v_empty[s]);
-            mma_commit(&pv_done[s]);
+          for (int k8 = 0; k8 < 8; ++k8) {   // 16 keys per step
+            const uint64_t bd = sdesc_sw128(smem_u32(sV + k8 * 2048), kBox16, 1024);
+            mma_ts(tmem + kTO + 128 * x, tmem + kTS + 128 * x + 64 + 8 * k8, bd, idO, (j > 0 || k8 > 0) ? 1 : 0);
+          }
+          mma_commit(&pv_done[x]);
+          if (x == 1 || !sees(1, j)) mma_commit(&v_empty);
+          return true;
+        };
+        // issue order S_0(0) S_1(0), then per key tile j: PV_0(j) S_0(j+1)
+        // PV_1(j) S_1(j+1), so that each query tile's scores for the next key
+        // tile run while the other tile's softmax does
+        for (int x = 0; ok && x < 2; ++x)
+          if (sees(x, 0)) ok = score(x, 0);
+        for (int j = 0; ok && j < n_kt; ++j) {
+          for (int x = 0; ok && x < 2; ++x) {
+            if (sees(x, j)) ok = value(x, j);
+            if (ok && sees(x, j + 1)) ok = score(x, j + 1);
           }
         }
-        g0 += n_kt;
+        g += n_kt;
+        if (!ok) break;
+        mma_commit(&item_done);
+        cnt0 += nk0;
+        cnt1 += nk1;
         ++nq;
       }
       if (!ok) {
@@ -520,53 +544,96 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
         atomicOr(a.err, kErrTimeout);
       }
     }
+  } else if (warp == kAtThreads / 32 - 1) {
+    // value tiles have a producer of their own: the single value buffer is
+    // refilled only once both query tiles' value MMAs have read it, and the
+    // key tiles must not wait behind that
+    if (lane == 0) {
+      const uint64_t pol_kv = policy_evict_last();
+      bool ok = true;
+      uint32_t nq = 0;                         // items with key tiles
+      for (uint32_t n = 0; ok; ++n) {
+        int i;
+        ok = fetch(n, &i);
+        if (!ok) break;
+        mbar_arrive(&item_empty[n & 1]);
+        if (i < 0) break;
+        const AtItem it = at_item(i, n_pairs, a.H);
+        const int n_kt = max(at_key_tiles(a, it.b, 2 * it.p), at_key_tiles(a, it.b, 2 * it.p + 1));
+        const int krow0 = (it.b * a.H + it.h) * a.R;
+        for (int j = 0; ok && j < n_kt; ++j) {
+          // free once the value MMAs of the previous tile are done and, for an
+          // item's first tile, once every row warp has stored the previous
+          // item's outputs through it
+          ok = n_v == 0 || mbar_wait(&v_empty, (n_v - 1) & 1, abort_flag, kPfWaitNs);
+          if (ok && j == 0 && nq > 0) ok = mbar_wait(&epi_done, (nq - 1) & 1, abort_flag, kPfWaitNs);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&v_full, kAtV);
+          tma_load_3d(sV, &tm_v, &v_full, 0, krow0 + 128 * j, 0, pol_kv);
+          ++n_v;
+        }
+        if (n_kt > 0) ++nq;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(a.err, kErrTimeout);
+      }
+    }
   } else {
-    // row warps: half hf (warps 2-5: keys 0-63 of every tile, warps 6-9: keys
-    // 64-127) runs its own online softmax over its keys into its own output
-    // accumulator O_hf; thread = query row r (TMEM lane r)
-    const int hf = (warp - 2) >> 2;
+    // row warps: query tile x (warps 2-5: the item's first tile, 6-9: its
+    // second) runs a base-2 online softmax over all 128 keys of every key
+    // tile into its output accumulator O_x; thread = query row r (TMEM lane r)
+    const int x = (warp - 2) >> 2;
     const int q4 = warp & 3;
     const int r = 32 * q4 + lane;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const float sl2 = a.scale * kPfLog2e;
-    uint8_t* ebuf = smem + kAtOffE + (4 * hf + q4) * kAtEpi;
-    uint32_t g0 = 0, nq = 0;                   // key tiles and query tiles consumed
+    uint8_t* qx = smem + x * kAtQ;
+    uint8_t* ebuf = sV + (4 * x + q4) * 4096;   // this warp's 32 rows x 128 bytes while storing
+    uint32_t cnt = 0, nq = 0;                  // key tiles and items with key tiles consumed
     bool ok = true;
 
     // the query's rotary half was copied unrotated into box 2 of the query
     // tile (K-major, 128-byte swizzle: 16-byte chunk c of row r sits at chunk
-    // c ^ (r & 7)); rotate it in place by the query's position, half hf taking
-    // chunks 4 hf .. 4 hf + 3; rows past the sequence become zeros
-    const auto rotate = [&](const AtItem& it, uint32_t q_index) -> bool {
-      if (!warp_ok(mbar_wait(&q_full, q_index & 1, abort_flag, kPfWaitNs), abort_flag, a.err)) return false;
-      const int t = it.qt * 128 + r;
-      const int L = a.seqlens[it.b];
-      const bool real = t < a.T_q;
-      const uint64_t pos = (uint64_t)(int64_t)(L - a.T_q + t);
-      uint8_t* qrow_s = sQ + 2 * kBox16 + r * 128;
+    // c ^ (r & 7)); rotate it in place by the query's position; rows past the
+    // sequence become zeros.  A tile that does not exist only signals.
+    const auto prologue = [&](const AtItem& it, int nkx, uint32_t q_index) -> bool {
+      if (nkx > 0) {
+        if (!warp_ok(mbar_wait(&q_full, q_index & 1, abort_flag, kPfWaitNs), abort_flag, a.err)) return false;
+        const int t = (2 * it.p + x) * 128 + r;
+        const int L = a.seqlens[it.b];
+        const bool real = t < a.T_q;
+        const uint64_t pos = (uint64_t)(int64_t)(L - a.T_q + t);
+        uint8_t* qrow_s = qx + 2 * kBox16 + r * 128;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {   // 16-byte chunk c: rotary pairs 4c .. 4c + 3
+          uint4* sl = reinterpret_cast<uint4*>(qrow_s + ((c ^ (r & 7)) << 4));
+          const uint4 raw = *sl;
+          const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t w[4] = {0u, 0u, 0u, 0u};
+          if (real) {
 #pragma unroll
-      for (int c = 4 * hf; c < 4 * hf + 4; ++c) {   // 16-byte chunk c: rotary pairs 4c .. 4c + 3
-        uint4* sl = reinterpret_cast<uint4*>(qrow_s + ((c ^ (r & 7)) << 4));
-        const uint4 raw = *sl;
-        const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (real) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = 4 * c + e;
-            const float half_turns = (float)(int64_t)(pos * fr.turn[j]) * 0x1p-63f;
-            float sn, cs;
-            sincospif(half_turns, &sn, &cs);
-            const float x1 = __uint_as_float(in[e] << 16), x2 = __uint_as_float(in[e] & 0xffff0000u);
-            w[e] = pack_bf16x2(x1 * cs - x2 * sn, x1 * sn + x2 * cs);
+            for (int e = 0; e < 4; ++e) {
+              const int j = 4 * c + e;
+              const float half_turns = (float)(int64_t)(pos * fr.turn[j]) * 0x1p-63f;
+              float sn, cs;
+              sincospif(half_turns, &sn, &cs);
+              const float x1 = __uint_as_float(in[e] << 16), x2 = __uint_as_float(in[e] & 0xffff0000u);
+              w[e] = pack_bf16x2(x1 * cs - x2 * sn, x1 * sn + x2 * cs);
+            }
           }
+          *sl = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        *sl = make_uint4(w[0], w[1], w[2], w[3]);
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&q_ready);
+      if (lane == 0) mbar_arrive(&q_ready[x]);
       return true;
+    };
+    const auto tiles_of = [&](const AtItem& it, int* nkx) -> int {
+      const int n0 = at_key_tiles(a, it.b, 2 * it.p), n1 = at_key_tiles(a, it.b, 2 * it.p + 1);
+      *nkx = x == 0 ? n0 : n1;
+      return max(n0, n1);
     };
 
     uint32_t n = 0;
@@ -577,194 +644,219 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
       if (lane == 0) mbar_arrive(&item_empty[n & 1]);
     }
     AtItem it{};
-    int n_kt = 0;
+    int n_kt = 0, nkx = 0;
     if (ok && cur >= 0) {
-      it = at_item(cur, n_qt, a.H);
-      n_kt = at_key_tiles(a, it);
-      if (n_kt > 0) ok = rotate(it, nq);
+      it = at_item(cur, n_pairs, a.H);
+      n_kt = tiles_of(it, &nkx);
+      if (n_kt > 0) ok = prologue(it, nkx, nq);
     }
     while (ok && cur >= 0) {
-      const int t = it.qt * 128 + r;
+      const int qt = 2 * it.p + x;
+      const int t = qt * 128 + r;
       const int L = a.seqlens[it.b];
       const size_t qrow = (size_t)it.b * a.T_q + t;
-      float* orow = a.o + (qrow * a.H + it.h) * a.d_h;
       if (n_kt == 0) {
         // a sequence of invalid length: zeros (the error word says why)
-        if (it.qt == 0 && it.h == 0 && lane == 0 && hf == 0 && q4 == 0) atomicOr(a.err, kErrBadIndex);
+        if (it.p == 0 && it.h == 0 && lane == 0 && x == 0 && q4 == 0) atomicOr(a.err, kErrBadIndex);
         if (t < a.T_q) {
-          for (int c = 0; c < 16; ++c)
-            reinterpret_cast<float4*>(orow + 64 * hf)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (hf == 0 && a.lse) a.lse[qrow * a.H + it.h] = 0.f;
+          float* orow = a.o + (qrow * a.H + it.h) * a.d_h;
+          for (int c = 0; c < 32; ++c) reinterpret_cast<float4*>(orow)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (a.lse) a.lse[qrow * a.H + it.h] = 0.f;
         }
-      } else {
-        const int lim = t < a.T_q ? L - a.T_q + t : -1;   // position of the query = its last visible key
-        float m_run = -INFINITY, l_run = 0.f;
-        for (int j = 0; ok && j < n_kt; ++j) {
-          const uint32_t g = g0 + j, s = g & 1;
-          ok = warp_ok(mbar_wait(&s_full[s], (g >> 1) & 1, abort_flag, kPfWaitNs), abort_flag, a.err);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t sbuf = tmem + lane_off + kTS + s * 128 + hf * 64;
-          float x[64];
-          tmem_ld64(sbuf, x);
-          tmem_ld_wait();
-          const int key0 = 128 * j + 64 * hf;
-          if (key0 + 63 > lim) {   // causal mask (and padding rows: every key)
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (key0 + c > lim) x[c] = -INFINITY;
-          }
-          float mq[4] = {x[0], x[1], x[2], x[3]};
-#pragma unroll
-          for (int c = 4; c < 64; c += 4) {
-            mq[0] = fmaxf(mq[0], x[c]);
-            mq[1] = fmaxf(mq[1], x[c + 1]);
-            mq[2] = fmaxf(mq[2], x[c + 2]);
-            mq[3] = fmaxf(mq[3], x[c + 3]);
-          }
-          const float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-          const float m_cand = fmaxf(m_run, mt * sl2);
-          const bool grow = m_cand > m_run + kPfRescale;   // also the first finite maximum
-          float alpha = 1.f;
-          if (grow) {
-            alpha = (m_run == -INFINITY) ? 0.f : ex2f(m_run - m_cand);
-            m_run = m_cand;
-          }
-          // O_hf holds this half's value sums of tiles < j: rescale the rows
-          // whose maximum grew, once the value MMAs of tile j - 1 are complete
-          if (__any_sync(0xffffffffu, grow && l_run > 0.f)) {
-            ok = warp_ok(mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag, kPfWaitNs),
-                         abort_flag, a.err);
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              float o[32];
-              const uint32_t oc = tmem + lane_off + kTO + hf * 128 + 32 * c;
-              tmem_ld32(oc, o);
-              tmem_ld_wait();
-              uint32_t u[32];
-#pragma unroll
-              for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(o[e] * alpha);
-              tmem_st32(oc, u);
-            }
-            tmem_st_wait();
-          }
-          l_run *= alpha;
-          const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-          // probabilities as bf16 pairs over the first 32 columns of this
-          // half's scores (already read into registers)
-          float sq[4] = {0.f, 0.f, 0.f, 0.f};
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float p0 = ex2f(fmaf(x[2 * c], sl2, -mu)), p1 = ex2f(fmaf(x[2 * c + 1], sl2, -mu));
-            sq[c & 3] += p0 + p1;
-            pk[c] = pack_bf16x2(p0, p1);
-          }
-          tmem_st32(sbuf, pk);
-          tmem_st_wait();
-          l_run += (sq[0] + sq[1]) + (sq[2] + sq[3]);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&p_full[s]);
-        }
-        if (!ok) break;
-        const uint32_t g_last = g0 + n_kt - 1;
-        g0 += n_kt;
-        ++nq;
-        // the next item: its query tile is rotated now, so that its first
-        // score MMAs run while this item's outputs are written
         ++n;
-        int nxt;
-        ok = warp_ok(fetch(n, &nxt), abort_flag, a.err);
+        ok = warp_ok(fetch(n, &cur), abort_flag, a.err);
         if (!ok) break;
         __syncwarp();
         if (lane == 0) mbar_arrive(&item_empty[n & 1]);
-        AtItem it2{};
-        int n_kt2 = 0;
-        if (nxt >= 0) {
-          it2 = at_item(nxt, n_qt, a.H);
-          n_kt2 = at_key_tiles(a, it2);
-          if (n_kt2 > 0 && !rotate(it2, nq)) {
-            ok = false;
-            break;
-          }
+        if (cur >= 0) {
+          it = at_item(cur, n_pairs, a.H);
+          n_kt = tiles_of(it, &nkx);
+          if (n_kt > 0) ok = prologue(it, nkx, nq);
         }
-        // epilogue: merge the two halves, o = (O_0 a_0 + O_1 a_1) / (l_0 a_0 + l_1 a_1)
-        // with a_h = 2^(m_h - m), lse = (m + log2 l) ln 2.  Half hf writes
-        // output columns 64 hf .. 64 hf + 63.
-        ok = warp_ok(mbar_wait(&pv_done[g_last & 1], (g_last >> 1) & 1, abort_flag, kPfWaitNs), abort_flag,
-                     a.err);
-        if (!ok) break;
-        row_m[hf][r] = m_run;
-        row_l[hf][r] = l_run;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&grp);
-        ok = warp_ok(mbar_wait(&grp, (nq - 1) & 1, abort_flag, kPfWaitNs), abort_flag, a.err);
-        if (!ok) break;
-        tc_fence_after();
-        const float m0 = row_m[0][r], m1 = row_m[1][r];
-        float m = fmaxf(m0, m1);
-        if (m == -INFINITY) m = 0.f;   // padding rows
-        const float a0 = ex2f(m0 - m), a1 = ex2f(m1 - m);
-        const float l = row_l[0][r] * a0 + row_l[1][r] * a1;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const float f0 = a0 * inv, f1 = a1 * inv;
-        const int row0 = it.qt * 128 + 32 * q4;   // first query of this warp's rows
-        float* obase = a.o + (((size_t)it.b * a.T_q + row0) * a.H + it.h) * a.d_h + 64 * hf;
-        const size_t ostride = (size_t)a.H * a.d_h;
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          float o0[32], o1[32];
-          tmem_ld32(tmem + lane_off + kTO + 64 * hf + 32 * c, o0);
-          tmem_ld32(tmem + lane_off + kTO + 128 + 64 * hf + 32 * c, o1);
-          tmem_ld_wait();
-          if (c == 1) {   // both halves' outputs read: the next item's value MMAs may overwrite them
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&o_free);
-          }
-          // 8 columns at a time through this warp's buffer, so that each
-          // store instruction writes 16 rows x 32 contiguous bytes (one row
-          // per thread would write 32 rows x 16 bytes): row i's two 16-byte
-          // halves sit at i * 32 + 16 (k ^ ((i >> 2) & 1)), conflict-free both ways
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const int e = 8 * q + 4 * k;
-              *reinterpret_cast<float4*>(ebuf + lane * 32 + ((k ^ ((lane >> 2) & 1)) << 4)) =
-                  make_float4(o0[e] * f0 + o1[e] * f1, o0[e + 1] * f0 + o1[e + 1] * f1,
-                              o0[e + 2] * f0 + o1[e + 2] * f1, o0[e + 3] * f0 + o1[e + 3] * f1);
-            }
-            __syncwarp();
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const int i = 16 * h2 + (lane >> 1), k = lane & 1;
-              const float4 v = *reinterpret_cast<const float4*>(ebuf + i * 32 + ((k ^ ((i >> 2) & 1)) << 4));
-              if (row0 + i < a.T_q) *reinterpret_cast<float4*>(obase + i * ostride + 32 * c + 8 * q + 4 * k) = v;
-            }
-            __syncwarp();
-          }
-        }
-        if (hf == 0 && t < a.T_q && a.lse) a.lse[qrow * a.H + it.h] = (m + log2f(l)) * kPfLn2;
-        cur = nxt;
-        it = it2;
-        n_kt = n_kt2;
         continue;
       }
-      // an item without key tiles: on to the next
+      const int lim = t < a.T_q ? L - a.T_q + t : -1;   // position of the query = its last visible key
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; ok && j < nkx; ++j) {
+        const uint32_t g = cnt + j;
+        ok = warp_ok(mbar_wait(&s_full[x], g & 1, abort_flag, kPfWaitNs), abort_flag, a.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sbuf = tmem + lane_off + kTS + 128 * x;
+        const int key0 = 128 * j;
+        const bool masked = key0 + 127 > lim;   // causal mask (and padding rows: every key)
+        // the row maximum over both 64-key halves, keeping the second half;
+        // the first is read again for its probabilities (two halves in
+        // registers at once would not fit beside the rest)
+        float xb[64];
+        float mq[4];
+        {
+          float xa[64];
+          tmem_ld64(sbuf, xa);
+          tmem_ld_wait();
+          if (masked) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (key0 + c > lim) xa[c] = -INFINITY;
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) mq[c] = xa[c];
+#pragma unroll
+          for (int c = 4; c < 64; c += 4) {
+            mq[0] = fmaxf(mq[0], xa[c]);
+            mq[1] = fmaxf(mq[1], xa[c + 1]);
+            mq[2] = fmaxf(mq[2], xa[c + 2]);
+            mq[3] = fmaxf(mq[3], xa[c + 3]);
+          }
+        }
+        tmem_ld64(sbuf + 64, xb);
+        tmem_ld_wait();
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (key0 + 64 + c > lim) xb[c] = -INFINITY;
+        }
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          mq[0] = fmaxf(mq[0], xb[c]);
+          mq[1] = fmaxf(mq[1], xb[c + 1]);
+          mq[2] = fmaxf(mq[2], xb[c + 2]);
+          mq[3] = fmaxf(mq[3], xb[c + 3]);
+        }
+        const float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        const float m_cand = fmaxf(m_run, mt * sl2);
+        const bool grow = m_cand > m_run + kPfRescale;   // also the first finite maximum
+        const bool rescale = __any_sync(0xffffffffu, grow && l_run > 0.f);
+        float alpha = 1.f;
+        if (grow) {
+          alpha = (m_run == -INFINITY) ? 0.f : ex2f(m_run - m_cand);
+          m_run = m_cand;
+        }
+        l_run *= alpha;
+        const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+        // probabilities as bf16 pairs over score columns 64-127: keys 64-127
+        // (from registers) into columns 96-127, then keys 0-63 (read again)
+        // into columns 64-95
+        float sq[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float p0 = ex2f(fmaf(xb[2 * c], sl2, -mu)), p1 = ex2f(fmaf(xb[2 * c + 1], sl2, -mu));
+            sq[c & 3] += p0 + p1;
+            pk[c] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(sbuf + 96, pk);
+        }
+        {
+          float xa[64];
+          tmem_ld64(sbuf, xa);
+          tmem_ld_wait();
+          if (masked) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (key0 + c > lim) xa[c] = -INFINITY;
+          }
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float p0 = ex2f(fmaf(xa[2 * c], sl2, -mu)), p1 = ex2f(fmaf(xa[2 * c + 1], sl2, -mu));
+            sq[c & 3] += p0 + p1;
+            pk[c] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(sbuf + 64, pk);
+        }
+        l_run += (sq[0] + sq[1]) + (sq[2] + sq[3]);
+        // O_x holds the value sums of tiles < j: rescale the rows whose
+        // maximum grew, once the value MMAs of tile j - 1 are complete (the
+        // value MMAs of tile j wait for this warp's signal below)
+        if (rescale) {
+          ok = warp_ok(mbar_wait(&pv_done[x], (g - 1) & 1, abort_flag, kPfWaitNs), abort_flag, a.err);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float o[32];
+            const uint32_t oc = tmem + lane_off + kTO + 128 * x + 32 * c;
+            tmem_ld32(oc, o);
+            tmem_ld_wait();
+            uint32_t u[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(o[e] * alpha);
+            tmem_st32(oc, u);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[x]);
+      }
+      if (!ok) break;
+      cnt += nkx;
+      ++nq;
+      const AtItem done_it = it;
+      const int done_nkx = nkx;
+      // the next item: its query tile is rotated now, so that its first
+      // score MMAs run while this item's outputs are written
       ++n;
       ok = warp_ok(fetch(n, &cur), abort_flag, a.err);
       if (!ok) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(&item_empty[n & 1]);
       if (cur >= 0) {
-        it = at_item(cur, n_qt, a.H);
-        n_kt = at_key_tiles(a, it);
-        if (n_kt > 0) ok = rotate(it, nq);
+        it = at_item(cur, n_pairs, a.H);
+        n_kt = tiles_of(it, &nkx);
+        if (n_kt > 0 && !prologue(it, nkx, nq)) {
+          ok = false;
+          break;
+        }
       }
+      // epilogue, once every MMA of the item is done (the value buffer is
+      // then free): o = O_x / l, lse = (m + log2 l) ln 2
+      ok = warp_ok(mbar_wait(&item_done, (nq - 1) & 1, abort_flag, kPfWaitNs), abort_flag, a.err);
+      if (!ok) break;
+      tc_fence_after();
+      if (done_nkx > 0) {
+        const float m = m_run == -INFINITY ? 0.f : m_run;   // padding rows
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const int row0 = (2 * done_it.p + x) * 128 + 32 * q4;   // first query of this warp's rows
+        float* obase = a.o + (((size_t)done_it.b * a.T_q + row0) * a.H + done_it.h) * a.d_h;
+        const size_t ostride = (size_t)a.H * a.d_h;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float o[32];
+          tmem_ld32(tmem + lane_off + kTO + 128 * x + 32 * c, o);
+          tmem_ld_wait();
+          if (c == 3) {   // the outputs are read: the next item's value MMAs may overwrite them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_free[x]);
+          }
+          // 32 columns through this warp's staging rows: row i's 16-byte
+          // chunk k sits at i * 128 + 16 (k ^ (i & 7)), conflict-free both
+          // ways; each store instruction then writes 4 rows x 128 bytes
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4*>(ebuf + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                make_float4(o[4 * k] * inv, o[4 * k + 1] * inv, o[4 * k + 2] * inv, o[4 * k + 3] * inv);
+          __syncwarp();
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const int i = 4 * i4 + (lane >> 3), k = lane & 7;
+            const float4 v = *reinterpret_cast<const float4*>(ebuf + i * 128 + ((k ^ (i & 7)) << 4));
+            if (row0 + i < a.T_q) *reinterpret_cast<float4*>(obase + i * ostride + 32 * c + 4 * k) = v;
+          }
+          __syncwarp();
+        }
+        if (t < a.T_q && a.lse) a.lse[qrow * a.H + done_it.h] = (m + log2f(l_run)) * kPfLn2;
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&o_free[x]);
+      }
+      // the value buffer may be refilled
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&epi_done);
     }
   }
 
@@ -780,11 +872,9 @@ prefill_attn_kernel(const PrefillAttnArgs a, const __grid_constant__ CUtensorMap
       const uint32_t j = n_k - 1 - k;
       if (!mbar_wait(&k_full[j & 1], (j >> 1) & 1, never, kPfWaitNs)) atomicOr(a.err, kErrTimeout);
     }
-    for (uint32_t k = 0; k < (uint32_t)kAtStages && k < n_v; ++k) {
-      const uint32_t j = n_v - 1 - k;
-      if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, never, kPfWaitNs)) atomicOr(a.err, kErrTimeout);
-    }
   }
+  if (warp == kAtThreads / 32 - 1 && lane == 0 && n_v > 0 && !mbar_wait(&v_full, (n_v - 1) & 1, never, kPfWaitNs))
+    atomicOr(a.err, kErrTimeout);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -930,9 +1020,8 @@ cudaError_t launch_prefill_attn(const PrefillAttnArgs& a, cudaStream_t s) {
   for (int i = 0; i < 2; ++i) {
     // k_nope, v [B, H, R, d_h = 128] as 3-D (64 dims, B * H * R rows, 2 halves
     // of d_h): one box of 64 dims x 128 rows x 2 halves is a whole key tile of
-    // a head (32 KB) in ONE copy, laid out [half][row][64 dims] as the MMA
-    // reads it (every copy instruction costs the SM's copy engine ~0.3 us, so
-    // the tile is not split into two boxes)
+    // a head (32 KB), landing in one copy as [half][row][64 dims], as the MMA
+    // reads it
     cuuint64_t dims[3] = {64, (cuuint64_t)kv_rows * a.H, (cuuint64_t)a.d_h / 64};
     cuuint64_t strides[2] = {(cuuint64_t)a.d_h * 2, 128};
     cuuint32_t box[3] = {64, 128, 2};
@@ -958,7 +1047,7 @@ cudaError_t launch_prefill_attn(const PrefillAttnArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   // one CTA per SM (the rings fill shared memory), each taking work items
   // until none are left
-  const long long n_items = (long long)((a.T_q + 127) / 128) * a.H * a.B;
+  const long long n_items = (long long)((a.T_q + 255) / 256) * a.H * a.B;   // pairs of query tiles
   if (n_items > INT32_MAX) return cudaErrorInvalidValue;
   int sms = 0;
   e = device_sm_count(&sms);

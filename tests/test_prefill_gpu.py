@@ -122,13 +122,14 @@ def test_prefill_chain_matches_oracle(spec):
 
 
 def test_prefill_attention_schedules_agree():
-    """The attention kernel is persistent: its CTAs take work items from a
-    counter kept per stream (and zeroed by the kernel for the next launch), or
-    in a fixed order on the per-thread default stream.  256 items over at
-    most one CTA per SM: repeated launches, fresh streams and the fixed order
-    all give the same bits."""
+    """The attention kernel is persistent: its CTAs take work items (two
+    query tiles of one head) from a counter kept per stream and zeroed by the
+    kernel for the next launch, or in a fixed order on the per-thread default
+    stream.  384 items (the last pair of each head has one tile) over at most
+    one CTA per SM: sampled queries match the oracle, and repeated launches,
+    fresh streams and the fixed order all give the same bits."""
     from cuda.bindings import runtime as cudart
-    spec = CASES[3]
+    spec = mi.PrefillSpec("pf_sched_h64_t640", seed=65, B=2, H=64, T_q=640, seqlens=(640, 900))
     inp = mi.make_prefill_inputs(spec, with_kv=True)
     dev = upload(inp)
     kn, vv, kr = (bits_to_device(x) for x in (inp.k_nope_bits, inp.v_bits, inp.k_rope_bits))
@@ -145,6 +146,15 @@ def test_prefill_attention_schedules_agree():
 
     torch.cuda.synchronize()
     ref_o, ref_lse = run()
+    assert mla.mla_check_status() == mla.MLA_OK
+    queries = np.array([0, 127, 128, 255, 256, 383, 384, 511, 512, 639])
+    for b in range(spec.B):
+        want_o, want_lse = orc.prefill_attention(
+            f64(inp.q_nope_bits[b, queries]), f64(inp.q_rope_bits[b, queries]), positions(inp, b)[queries],
+            f64(inp.k_nope_bits[b]).transpose(1, 0, 2), f64(inp.v_bits[b]).transpose(1, 0, 2),
+            f64(inp.k_rope_bits[b]), spec.softmax_scale, spec.rope_base)
+        assert_decode_close(ref_o[b, queries].double().cpu().numpy(), want_o, what=f"sampled queries b={b}")
+        np.testing.assert_allclose(ref_lse[b, queries].double().cpu().numpy(), want_lse, rtol=0, atol=2e-2)
     outs = [run(), run(2)]                      # 2 = cudaStreamPerThread: the fixed order
     streams = []
     for _ in range(3):
