@@ -162,8 +162,18 @@ def test_prefill_attention_schedules_agree():
         assert err == cudart.cudaError_t.cudaSuccess
         streams.append(st)
         outs += [run(int(st)), run(int(st))]
+    # two launches in flight at once on two streams (two counters in use together)
+    pair = []
+    for st in streams[:2]:
+        pair.append(mla.mla_prefill_attention(dev["qn"], dev["qr"], kn, vv, kr, dev["sl"],
+                                              max_blocks_per_seq=inp.cache.max_blocks,
+                                              softmax_scale=spec.softmax_scale, rope_base=spec.rope_base,
+                                              stream=int(st)))
     for st in streams:
+        cudart.cudaStreamSynchronize(st)
         cudart.cudaStreamDestroy(st)
+    torch.cuda.synchronize()
+    outs += pair
     assert mla.mla_check_status() == mla.MLA_OK
     for o, lse in outs:
         assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
