@@ -487,6 +487,14 @@ int mla_prefill_kv_chunk(const void* kv_cache, int dtype, const int32_t* block_t
  * unaligned pointers), MLA_ERR_UNSUPPORTED.  Device errors (MLA_ERR_BAD_INDEX):
  * seqlens[b] < T_q or > 64 * max_blocks_per_seq (zeros written for b).
  * MLA_ERR_TIMEOUT: a bounded wait gave up.  Asynchronous on `stream`.
+ * Scheduling: one persistent CTA per SM takes (pair of query tiles, head)
+ * items from a work counter in device memory that belongs to `stream` (the
+ * first 64 streams that call it on a device get one each; the kernel leaves
+ * it at zero).  Launches on one stream run in order, so they never share a
+ * counter while running; later streams, and the per-thread default stream,
+ * take items in a fixed order instead.  The result is the same bits either
+ * way.  A CUDA graph that captured this call keeps the capturing stream's
+ * counter: do not run two instances of such a graph at the same time.
  */
 int mla_prefill_attention(const void* q_nope, const void* q_rope, int dtype, const void* k_nope,
                           const void* v, const void* k_rope, const int32_t* seqlens, int B,
