@@ -425,10 +425,10 @@ int mla_prefill_kv_rows(int max_blocks_per_seq);   /* 0 for invalid input; host 
  * mla_prefill_attention) is expected to be faster than the absorbed decode
  * (mla_decode_paged with T_q query tokens), 0 when the absorbed decode is,
  * or when the rebuild path does not support the shape, and -1 for invalid
- * input.  The estimate uses whole-GPU costs measured on B300: about 3.0 us
+ * input.  The estimate uses whole-GPU costs measured on B300: about 2.9 us
  * per group of 128 query rows and 4096 cached rows for the absorbed decode
- * (each group streams the pages once); about 210 us per 4096 rows at 128
- * heads for the rebuild, scaled by rows x heads; and 747 TFLOP/s for the
+ * (each group streams the pages once); about 207 us per 4096 rows at 128
+ * heads for the rebuild, scaled by rows x heads; and 980 TFLOP/s for the
  * attention over rebuilt keys.  At H = 128 it switches near T_q = 80.  Needs
  * no device.
  */
