@@ -18,7 +18,8 @@
 //    (256 x 512) in 64-column chunks; tcgen05.mma with M = 128 rows, N = 256,
 //    K = 512 accumulates both products of a head in TMEM (two buffers, so the
 //    epilogue of one head overlaps the MMAs of the next).  Four warps convert
-//    to bf16 and write k_nope[b, h, s, :] and v[b, h, s, :]; rows past the
+//    to bf16 and write k_nope[b, h, s, :] and v[b, h, s, :] through a small
+//    staging area, 512 contiguous bytes per store instruction; rows past the
 //    sequence end inside its last tile are written as zeros.  The first head
 //    group also copies the rotated rotary key R_s k^R_s of each row.  For a
 //    chunk of a chunked prefill only the chunk's rows [L - T_new, L) are
@@ -93,7 +94,8 @@ constexpr int kKvHeads = 8;              // heads per CTA (the latent tile is re
 constexpr int kKvStages = 2;             // weight chunk ring
 constexpr int kKvA = 8 * kBox16;         // 128 rows x 512 latents
 constexpr int kKvW = 2 * kBox16;         // 64-column chunk of W^UK_h (128 rows) and W^UV_h (128 rows)
-constexpr int kKvSmem = kKvA + kKvStages * kKvW + 1024;
+constexpr int kKvE = 8192;               // per row warp: 32 rows x 256 bytes of output staging
+constexpr int kKvSmem = kKvA + kKvStages * kKvW + 4 * kKvE + 1024;
 
 __global__ void __launch_bounds__(kPfThreads, 1)
 prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_pool,
@@ -237,32 +239,51 @@ prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_
         for (int k = 0; k < 8; ++k) dst[k] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
+    // a head's 32 rows of k_nope (then of v) are 8 KB of contiguous memory:
+    // they go out through this warp's staging rows (row i's 16-byte chunk k at
+    // i * 256 + 16 (k ^ (i & 15)), conflict-free both ways) so that each store
+    // instruction writes 512 contiguous bytes (one row per thread would write
+    // 32 rows x 16 bytes)
+    uint8_t* stage = smem + kKvA + kKvStages * kKvW + q4 * kKvE;
+    const int wrow0 = r0 + 32 * q4;   // this warp's first row
     for (int hh = 0; hh < nh; ++hh) {
       const uint32_t d = hh & 1;
       if (!warp_ok(mbar_wait(&d_full[d], (hh >> 1) & 1, abort_flag, kPfWaitNs), abort_flag, a.err))
         break;
       tc_fence_after();
-      const size_t off = (((size_t)b * a.H + (h0 + hh)) * a.R + row) * a.d_h;
-      __nv_bfloat16* kd = static_cast<__nv_bfloat16*>(a.k_nope) + off;
-      __nv_bfloat16* vd = static_cast<__nv_bfloat16*>(a.v) + off;
+      const size_t off = (((size_t)b * a.H + (h0 + hh)) * a.R + wrow0) * a.d_h;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        float x[32];
-        tmem_ld32(tmem + lane_off + d * 256 + 32 * c, x);
-        tmem_ld_wait();
-        uint4* dst = reinterpret_cast<uint4*>((c < 4 ? kd : vd) + 32 * (c & 3));
+      for (int part = 0; part < 2; ++part) {   // k_nope, then v
+#pragma unroll 1
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float x[32];
+          tmem_ld32(tmem + lane_off + d * 256 + 32 * (4 * part + c4), x);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (real)
-            w = make_uint4(pack_bf16x2(x[8 * i], x[8 * i + 1]), pack_bf16x2(x[8 * i + 2], x[8 * i + 3]),
-                           pack_bf16x2(x[8 * i + 4], x[8 * i + 5]), pack_bf16x2(x[8 * i + 6], x[8 * i + 7]));
-          if (mine) dst[i] = w;
+          for (int i = 0; i < 4; ++i) {
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);
+            if (real)
+              w = make_uint4(pack_bf16x2(x[8 * i], x[8 * i + 1]), pack_bf16x2(x[8 * i + 2], x[8 * i + 3]),
+                             pack_bf16x2(x[8 * i + 4], x[8 * i + 5]), pack_bf16x2(x[8 * i + 6], x[8 * i + 7]));
+            const int k = 4 * c4 + i;
+            *reinterpret_cast<uint4*>(stage + lane * 256 + ((k ^ (lane & 15)) << 4)) = w;
+          }
         }
+        if (part == 1) {   // the head's accumulator is read: the MMAs of head hh + 2 may reuse it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&d_empty[d]);
+        }
+        __syncwarp();
+        uint8_t* gbase = reinterpret_cast<uint8_t*>(part == 0 ? a.k_nope : a.v) + off * 2;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int rr = 2 * i + (lane >> 4), k = lane & 15;
+          const uint4 w = *reinterpret_cast<const uint4*>(stage + rr * 256 + ((k ^ (rr & 15)) << 4));
+          if (wrow0 + rr >= row_lo) *reinterpret_cast<uint4*>(gbase + rr * 256 + k * 16) = w;
+        }
+        __syncwarp();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&d_empty[d]);
     }
   }
 
