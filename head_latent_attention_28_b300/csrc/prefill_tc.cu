@@ -14,13 +14,16 @@
 // Two kernels:
 //  * prefill_kv_kernel: one CTA per (sequence, 128-row tile, group of 8
 //    heads).  TMA brings the tile's two cache pages (latent columns only,
-//    128 x 512, kept for all heads of the group) and streams [W^UK_h ; W^UV_h]
-//    (256 x 512) in 64-column chunks; tcgen05.mma with M = 128 rows, N = 256,
-//    K = 512 accumulates both products of a head in TMEM (two buffers, so the
-//    epilogue of one head overlaps the MMAs of the next).  Four warps convert
-//    to bf16 and write k_nope[b, h, s, :] and v[b, h, s, :] through a small
-//    staging area, 512 contiguous bytes per store instruction; rows past the
-//    sequence end inside its last tile are written as zeros.  The first head
+//    128 x 512); the row warps copy them into TMEM, where they stay as the
+//    MMA's A operand for all heads of the group, and the shared memory they
+//    used becomes output staging.  W^UK_h and W^UV_h (128 x 512 each) stream
+//    in 64-column chunks through a six-unit ring; tcgen05.mma with M = 128
+//    rows, N = 128, K = 512 accumulates k_h and then v_h in two TMEM
+//    accumulators, so the epilogue of one overlaps the MMAs of the other.
+//    Four warps convert to bf16 and write k_nope[b, h, s, :] and
+//    v[b, h, s, :] through the staging area, 512 contiguous bytes per store
+//    instruction; rows past the sequence end inside its last tile are written
+//    as zeros.  The first head
 //    group also copies the rotated rotary key R_s k^R_s of each row.  For a
 //    chunk of a chunked prefill only the chunk's rows [L - T_new, L) are
 //    written (tiles below them exit at once); earlier rows stay as the
@@ -91,11 +94,14 @@ __device__ __forceinline__ bool warp_ok(bool ok, volatile int* abort_flag, unsig
 // K/V rebuild
 // ---------------------------------------------------------------------------
 constexpr int kKvHeads = 8;              // heads per CTA (the latent tile is reused)
-constexpr int kKvStages = 2;             // weight chunk ring
-constexpr int kKvA = 8 * kBox16;         // 128 rows x 512 latents
-constexpr int kKvW = 2 * kBox16;         // 64-column chunk of W^UK_h (128 rows) and W^UV_h (128 rows)
+constexpr int kKvA = 8 * kBox16;         // 128 rows x 512 latents (then the output staging)
+constexpr int kKvUnits = 6;              // weight ring: 64-column chunks of W^UK_h or W^UV_h
+constexpr int kKvW = kBox16;             // one chunk: 128 rows x 64 latents
 constexpr int kKvE = 8192;               // per row warp: 32 rows x 256 bytes of output staging
-constexpr int kKvSmem = kKvA + kKvStages * kKvW + 4 * kKvE + 1024;
+constexpr int kKvSmem = kKvA + kKvUnits * kKvW + 1024;
+// TMEM columns: the K and V accumulators of the current head, then the
+// latent tile as the MMA A operand (a row per lane, bf16 pairs per column)
+constexpr uint32_t kKvAccK = 0, kKvAccV = 128, kKvTA = 256;
 
 __global__ void __launch_bounds__(kPfThreads, 1)
 prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_pool,
@@ -103,7 +109,7 @@ prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_
   extern __shared__ uint8_t kv_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(kv_smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ uint64_t a_full, w_full[kKvStages], w_empty[kKvStages], d_full[2], d_empty[2], mma_final;
+  __shared__ uint64_t a_full, a_ready, w_full[kKvUnits], w_empty[kKvUnits], d_full[2], d_empty[2], mma_final;
   __shared__ uint32_t tbase;
   __shared__ int abort_raw, never_raw;
   volatile int* abort_flag = &abort_raw;
@@ -128,11 +134,12 @@ prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_
     abort_raw = 0;
     never_raw = 0;
     mbar_init(&a_full, 1);
-    for (int s = 0; s < kKvStages; ++s) {
-      mbar_init(&w_full[s], 1);
-      mbar_init(&w_empty[s], 1);
+    mbar_init(&a_ready, 4);
+    for (int u = 0; u < kKvUnits; ++u) {
+      mbar_init(&w_full[u], 1);
+      mbar_init(&w_empty[u], 1);
     }
-    for (int d = 0; d < 2; ++d) {
+    for (int d = 0; d < 2; ++d) {   // d = 0: the K accumulator, 1: the V accumulator
       mbar_init(&d_full[d], 1);
       mbar_init(&d_empty[d], 4);
     }
@@ -166,48 +173,54 @@ prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_
       for (int c = 0; c < 8; ++c)
         for (int p = 0; p < 2; ++p)
           tma_load_2d(sA + c * kBox16 + p * 8192, &tm_pool, &a_full, 64 * c, y[p], pol_a);
+      // per head: the 8 chunks of W^UK_h, then the 8 of W^UV_h
       for (int hh = 0; hh < nh; ++hh) {
         const int wrow = (h0 + hh) * a.d_h;
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t g = n_issued, s = g % kKvStages;
-          if (g >= (uint32_t)kKvStages &&
-              !mbar_wait(&w_empty[s], ((g / kKvStages) - 1) & 1, abort_flag, kPfWaitNs)) {
-            *abort_flag = 1;
-            atomicOr(a.err, kErrTimeout);
-            break;
+        for (int part = 0; part < 2; ++part) {
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t g = n_issued, u = g % kKvUnits;
+            if (g >= (uint32_t)kKvUnits &&
+                !mbar_wait(&w_empty[u], ((g / kKvUnits) - 1) & 1, abort_flag, kPfWaitNs)) {
+              *abort_flag = 1;
+              atomicOr(a.err, kErrTimeout);
+              break;
+            }
+            mbar_arrive_expect_tx(&w_full[u], kKvW);
+            tma_load_2d(sW + u * kKvW, part == 0 ? &tm_wuk : &tm_wuv, &w_full[u], 64 * c, wrow, pol_w);
+            ++n_issued;
           }
-          uint8_t* dst = sW + s * kKvW;
-          mbar_arrive_expect_tx(&w_full[s], kKvW);
-          tma_load_2d(dst, &tm_wuk, &w_full[s], 64 * c, wrow, pol_w);
-          tma_load_2d(dst + kBox16, &tm_wuv, &w_full[s], 64 * c, wrow, pol_w);
-          ++n_issued;
+          if (*abort_flag) break;
         }
         if (*abort_flag) break;
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t id = idesc_bf16_f32(128, 256, 0, 0);   // A and B K-major
-      bool ok = mbar_wait(&a_full, 0, abort_flag, kPfWaitNs);
+      // k_h = W^UK_h c and v_h = W^UV_h c as two M = 128, N = 128, K = 512
+      // products with the latent tile read from TMEM: the epilogue of one
+      // part overlaps the MMAs of the other
+      const uint32_t id = idesc_bf16_f32(128, 128, 0, 0);   // A from TMEM, B K-major
+      bool ok = mbar_wait(&a_ready, 0, abort_flag, kPfWaitNs);
       uint32_t g = 0;
       for (int hh = 0; ok && hh < nh; ++hh) {
-        const uint32_t d = hh & 1;
-        if (hh >= 2) ok = mbar_wait(&d_empty[d], ((hh >> 1) - 1) & 1, abort_flag, kPfWaitNs);
-        for (int c = 0; ok && c < 8; ++c, ++g) {
-          const uint32_t s = g % kKvStages;
-          ok = mbar_wait(&w_full[s], (g / kKvStages) & 1, abort_flag, kPfWaitNs);
-          if (!ok) break;
-          tc_fence_after();
-          const uint8_t* wb = sW + s * kKvW;
+        for (int part = 0; ok && part < 2; ++part) {
+          if (hh >= 1) ok = mbar_wait(&d_empty[part], (hh - 1) & 1, abort_flag, kPfWaitNs);
+          for (int c = 0; ok && c < 8; ++c, ++g) {
+            const uint32_t u = g % kKvUnits;
+            ok = mbar_wait(&w_full[u], (g / kKvUnits) & 1, abort_flag, kPfWaitNs);
+            if (!ok) break;
+            tc_fence_after();
+            const uint8_t* wb = sW + u * kKvW;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint64_t ad = sdesc_sw128(smem_u32(sA + c * kBox16 + q * 32), 16, 1024);
-            const uint64_t bd = sdesc_sw128(smem_u32(wb + q * 32), 16, 1024);
-            mma_ss(tmem + d * 256, ad, bd, id, (c > 0 || q > 0) ? 1 : 0);
+            for (int q = 0; q < 4; ++q) {   // latents 64 c + 16 q .. + 15
+              const uint64_t bd = sdesc_sw128(smem_u32(wb + q * 32), 16, 1024);
+              mma_ts(tmem + (part ? kKvAccV : kKvAccK), tmem + kKvTA + 32 * c + 8 * q, bd, id,
+                     (c > 0 || q > 0) ? 1 : 0);
+            }
+            mma_commit(&w_empty[u]);
           }
-          mma_commit(&w_empty[s]);
+          if (ok) mma_commit(&d_full[part]);
         }
-        if (ok) mma_commit(&d_full[d]);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -223,6 +236,29 @@ prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_
     const bool real = row < L;
     const bool mine = row >= row_lo;   // rows of earlier chunks are left as they are
     const size_t orow = (size_t)b * a.R + row;
+    bool ok = warp_ok(mbar_wait(&a_full, 0, abort_flag, kPfWaitNs), abort_flag, a.err);
+    if (ok) {
+      // the latent row into TMEM columns kKvTA.. (bf16 pairs): chunk c of the
+      // tile (64 latents, 128-byte swizzled rows) into columns 32 c .. 32 c + 31
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[32];
+        const uint8_t* src = sA + c * kBox16 + r * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + ((k ^ (r & 7)) << 4));
+          w[4 * k] = v.x;
+          w[4 * k + 1] = v.y;
+          w[4 * k + 2] = v.z;
+          w[4 * k + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_off + kKvTA + 32 * c, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_ready);
+    }
     if (blockIdx.z == 0 && mine) {
       // R_s k^R_s, unchanged from the cache row (zeros past the sequence end)
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.k_rope) + orow * a.d_r);
@@ -240,24 +276,23 @@ prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_
       }
     }
     // a head's 32 rows of k_nope (then of v) are 8 KB of contiguous memory:
-    // they go out through this warp's staging rows (row i's 16-byte chunk k at
-    // i * 256 + 16 (k ^ (i & 15)), conflict-free both ways) so that each store
-    // instruction writes 512 contiguous bytes (one row per thread would write
-    // 32 rows x 16 bytes)
-    uint8_t* stage = smem + kKvA + kKvStages * kKvW + q4 * kKvE;
+    // they go out through this warp's staging rows in the (now free) latent
+    // buffer (row i's 16-byte chunk k at i * 256 + 16 (k ^ (i & 15)),
+    // conflict-free both ways), so that each store instruction writes 512
+    // contiguous bytes (one row per thread would write 32 rows x 16 bytes)
+    uint8_t* stage = sA + q4 * kKvE;
     const int wrow0 = r0 + 32 * q4;   // this warp's first row
-    for (int hh = 0; hh < nh; ++hh) {
-      const uint32_t d = hh & 1;
-      if (!warp_ok(mbar_wait(&d_full[d], (hh >> 1) & 1, abort_flag, kPfWaitNs), abort_flag, a.err))
-        break;
-      tc_fence_after();
+    for (int hh = 0; ok && hh < nh; ++hh) {
       const size_t off = (((size_t)b * a.H + (h0 + hh)) * a.R + wrow0) * a.d_h;
 #pragma unroll 1
       for (int part = 0; part < 2; ++part) {   // k_nope, then v
+        ok = warp_ok(mbar_wait(&d_full[part], hh & 1, abort_flag, kPfWaitNs), abort_flag, a.err);
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll 1
         for (int c4 = 0; c4 < 4; ++c4) {
           float x[32];
-          tmem_ld32(tmem + lane_off + d * 256 + 32 * (4 * part + c4), x);
+          tmem_ld32(tmem + lane_off + (part ? kKvAccV : kKvAccK) + 32 * c4, x);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -269,12 +304,10 @@ prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_
             *reinterpret_cast<uint4*>(stage + lane * 256 + ((k ^ (lane & 15)) << 4)) = w;
           }
         }
-        if (part == 1) {   // the head's accumulator is read: the MMAs of head hh + 2 may reuse it
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&d_empty[d]);
-        }
+        // the accumulator is read: the next head's MMAs of this part may reuse it
+        tc_fence_before();
         __syncwarp();
+        if (lane == 0) mbar_arrive(&d_empty[part]);
         uint8_t* gbase = reinterpret_cast<uint8_t*>(part == 0 ? a.k_nope : a.v) + off * 2;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -295,9 +328,9 @@ prefill_kv_kernel(const PrefillKvArgs a, const __grid_constant__ CUtensorMap tm_
   }
   if (warp == 0 && lane == 0) {
     if (!mbar_wait(&a_full, 0, never, kPfWaitNs)) atomicOr(a.err, kErrTimeout);
-    for (uint32_t k = 0; k < (uint32_t)kKvStages && k < n_issued; ++k) {
+    for (uint32_t k = 0; k < (uint32_t)kKvUnits && k < n_issued; ++k) {
       const uint32_t g = n_issued - 1 - k;
-      if (!mbar_wait(&w_full[g % kKvStages], (g / kKvStages) & 1, never, kPfWaitNs))
+      if (!mbar_wait(&w_full[g % kKvUnits], (g / kKvUnits) & 1, never, kPfWaitNs))
         atomicOr(a.err, kErrTimeout);
     }
   }
