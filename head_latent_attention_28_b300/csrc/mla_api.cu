@@ -536,14 +536,14 @@ int mla_prefill_use_rebuild(int T_q, int L, int H, int d_c, int d_r, int d_h, in
     return 0;
   // Whole-GPU costs measured on B300 (H = 128): the absorbed decode streams
   // every page once per group of 128 query rows, ~2.9 us per group and 4096
-  // rows (32 x 4096 rows: 91.9 us per step); the rebuild takes ~207 us per
+  // rows (32 x 4096 rows: 91.9 us per step); the rebuild takes ~168 us per
   // 4096 rows at 128 heads; the attention over rebuilt keys runs at ~980
   // TFLOP/s.
   const double rows = (double)H * T_q;
   const double groups = std::ceil(rows / 128.0);
   const double absorbed_us = groups * (double)L * (2.9 / 4096.0);
   const double visible = (double)T_q * (L - T_q) + 0.5 * (double)T_q * (T_q + 1);
-  const double rebuild_us = (double)L * H * (207.0 / (4096.0 * 128.0)) +
+  const double rebuild_us = (double)L * H * (168.0 / (4096.0 * 128.0)) +
                             (double)H * visible * 640.0 / 980.0e6;
   return rebuild_us < absorbed_us ? 1 : 0;
 }

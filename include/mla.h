@@ -427,9 +427,9 @@ int mla_prefill_kv_rows(int max_blocks_per_seq);   /* 0 for invalid input; host 
  * or when the rebuild path does not support the shape, and -1 for invalid
  * input.  The estimate uses whole-GPU costs measured on B300: about 2.9 us
  * per group of 128 query rows and 4096 cached rows for the absorbed decode
- * (each group streams the pages once); about 207 us per 4096 rows at 128
+ * (each group streams the pages once); about 168 us per 4096 rows at 128
  * heads for the rebuild, scaled by rows x heads; and 980 TFLOP/s for the
- * attention over rebuilt keys.  At H = 128 it switches near T_q = 80.  Needs
+ * attention over rebuilt keys.  At H = 128 it switches near T_q = 66.  Needs
  * no device.
  */
 int mla_prefill_use_rebuild(int T_q, int L, int H, int d_c, int d_r, int d_h, int dtype);

@@ -213,10 +213,10 @@ def test_prefill_path_choice():
     # a single new token, or a handful, stay on the absorbed decode; a prompt goes to the rebuild
     assert use(1, 4096, 128) == 0 and use(16, 4096, 128) == 0 and use(64, 131072, 128) == 0
     assert use(4096, 4096, 128) == 1 and use(512, 32768, 128) == 1
-    # at 128 heads the switch sits near 80 new tokens whatever the length
+    # at 128 heads the switch sits near 66 new tokens whatever the length
     for L in (4096, 32768, 131072):
         flips = [T for T in range(1, 200) if use(T, L, 128) == 1]
-        assert flips and 70 <= flips[0] <= 100, (L, flips[:3])
+        assert flips and 55 <= flips[0] <= 80, (L, flips[:3])
         assert all(use(T, L, 128) == 1 for T in range(flips[0], 200))
     # fewer heads form fewer 128-row groups, so the absorbed decode stays longer
     assert use(64, 4096, 16) == 0 and use(1024, 4096, 16) == 1
