@@ -31,6 +31,11 @@ CASES = [
     mi.PrefillSpec("pf_chunk_ragged_h12", seed=61, B=3, H=12, T_q=130, seqlens=(130, 400, 259)),
     # DeepSeek-V2 head count, 256 new tokens after 128 cached ones
     mi.PrefillSpec("pf_h128_t256", seed=63, B=1, H=128, T_q=256, seqlens=(384,)),
+    # one new token after 699 cached rows, one head: a work item whose second
+    # query tile does not exist and whose first holds one real row
+    mi.PrefillSpec("pf_one_token_h1", seed=66, B=1, H=1, T_q=1, seqlens=(700,)),
+    # 129 new tokens: the item's second query tile holds one real row
+    mi.PrefillSpec("pf_t129_h3", seed=67, B=2, H=3, T_q=129, seqlens=(129, 300)),
 ]
 IDS = [c.name for c in CASES]
 
