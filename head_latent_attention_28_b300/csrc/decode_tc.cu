@@ -23,10 +23,10 @@
 //    (group, chunk) is one 1 KB swizzle atom and an MMA operand over the
 //    page's 64 tokens is a uniform stride of 9 KB.  Scores S = Q . C^T
 //    (M = 128 rows, K = 576) are computed for the pages of an item in pairs
-//    into two adjacent tensor-memory buffers: a pair in adjacent ring slots
-//    is one operand of 128 tokens (36 MMAs with N = 128, about 0.65 of the
-//    time of two N = 64 chains on this part), any other pair two N = 64
-//    chains sharing each A step, an odd last page one N = 64 chain.  The
+//    into adjacent tensor-memory buffers.  The ring places every pair in
+//    adjacent slots, (0, 1) or (1, 2) (page_slot), so a pair is always one
+//    operand of 128 tokens: 36 MMAs with N = 128, which on this part take as
+//    long as 36 with N = 64.  An odd last page is one N = 64 chain.  The
 //    MMAs are issued from a rolled chunk loop, which keeps the issuing code
 //    small and resident in the instruction cache next to the softmax code.
 //    The whole query is the A operand in tensor memory.  Two groups of four
@@ -103,7 +103,18 @@ constexpr int kMaxItems = 32;            // work items planned per batch
 // TMEM columns (score CTA): latent query [0, 256), rotary query [256, 288),
 // score buffers [384, 448) (first page of a pair) and [448, 512) (second page)
 constexpr uint32_t kTmemQr = 256;
-constexpr uint32_t kTmemS = 384;
+constexpr uint32_t kTmemS = 384;   // the first page of a unit; the second at +64 or -64
+
+// Ring slot of a page of the score CTA.  An item's pages go in units: a pair
+// (pages k, k + 1 for even k) or an odd last page alone.  A unit's first page
+// goes to slot 0 or 2 (alternating unit by unit), a pair's second page to
+// slot 1: every pair then sits in adjacent slots, (0, 1) or (1, 2), and is ONE
+// MMA operand of 128 tokens.  On this part an M = 128, K = 16 MMA takes as
+// long at N = 64 as at N = 128, so a pair scored as two N = 64 chains costs
+// twice as much per page.
+__device__ __forceinline__ uint32_t page_slot(uint32_t unit, int second) {
+  return second ? 1u : ((unit & 1u) ? 2u : 0u);
+}
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -447,6 +458,13 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
   uint32_t g_prod = 0;                 // producer: pages walked
   uint32_t g_issue = 0;                // producer: score CTA: 1 + last page loaded; value CTA: pages loaded
   uint32_t g_page = 0;                 // pages (MMA issuers, softmax, value warps)
+  uint32_t g_unit = 0;                 // score CTA: page units (producer, MMA issuer, softmax)
+  // score CTA: pages put in (producer) or taken from (MMA issuer) each ring
+  // slot, 21 bits per slot (a worker walks far fewer than 2^21 pages);
+  // producer: slots whose last page was copied (bits)
+  uint64_t slot_uses = 0;
+  uint32_t slot_loaded = 0;
+  const auto uses_of = [&](uint32_t sl) { return (uint32_t)(slot_uses >> (21 * sl)) & 0x1fffffu; };
   uint32_t g_sig = 0;                  // score signaler: pages signalled
   uint32_t s_use[2] = {0u, 0u};        // score MMA: times each score buffer was written
   uint32_t s_seen = 0;                 // softmax group: pages of this group processed
@@ -498,15 +516,20 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
           if (rank == 0) {
             if (!ok) atomicOr(a.err, kErrBadIndex);
             if (pf < total && bpf >= 0 && bpf < a.num_blocks) tma_prefetch_l2_4d(&tm_page, 0, 0, 0, bpf * 8);
-            const uint32_t sl = g_prod % kSlots;
-            if (g_prod >= (uint32_t)kSlots &&
-                !mbar_wait(&ctl.slot_empty[sl], ((g_prod / kSlots) - 1) & 1, abort_flag, wait_ns)) {
+            const int kp = f - ctl.item_flat[ip];   // page of its item
+            const uint32_t sl = page_slot((kp & 1) ? g_unit - 1 : g_unit, kp & 1);
+            if (!(kp & 1)) ++g_unit;
+            slot_loaded &= ~(1u << sl);
+            if (uses_of(sl) > 0 &&
+                !mbar_wait(&ctl.slot_empty[sl], (uses_of(sl) - 1) & 1, abort_flag, wait_ns)) {
               fail(&ctl, a.err);
             } else if (!(a.skip_load > 0 && w == 0 && g_prod + 1 == (uint32_t)a.skip_load)) {
               mbar_arrive_expect_tx(&ctl.slot_full[sl], kPageBytes);
               tma_load_4d(smem + sl * kPageBytes, &tm_page, &ctl.slot_full[sl], 0, 0, 0, y, pol);
               g_issue = g_prod + 1;
+              slot_loaded |= 1u << sl;
             }
+            slot_uses += 1ull << (21 * sl);
           } else {
             const uint32_t g = g_prod, vs = g % kVSlots;
             bool ok2 = g < (uint32_t)kVSlots ||
@@ -576,57 +599,43 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
             const Item it = ctl.items[ii];
             const int n = it.j1 - it.j0;
             bool ok = mbar_wait(&ctl.q_ready, it_cnt & 1, abort_flag, wait_ns);
-            // The item's pages in pairs (the first of a pair into score
-            // buffer 0, the second into buffer 1; an odd last page alone).
-            // A pair in adjacent ring slots is ONE operand of 128 tokens (the
-            // second slot continues the first's 9 KB stride): 36 MMAs with
-            // N = 128 instead of 72 with N = 64.
+            // The item's pages in units (page_slot): a pair in slots (0, 1)
+            // or (1, 2), scored as ONE operand of 128 tokens (the upper slot
+            // continues the lower one's 9 KB stride), or an odd last page
+            // alone.  The first page's scores always land at kTmemS; a pair in
+            // (1, 2) holds its second page in the lower slot, so the operand
+            // starts there and the scores start 64 columns lower.
             for (int k = 0; ok && k < n; k += 2) {
               const bool pair = k + 1 < n;
-              const uint32_t sl0 = g % kSlots, sl1 = (g + 1) % kSlots;
+              const uint32_t sx = page_slot(g_unit, 0);
+              ++g_unit;
               if (s_use[0] > 0) ok = mbar_wait(&ctl.s_free[0], (s_use[0] - 1) & 1, abort_flag, wait_ns);
               if (ok && pair && s_use[1] > 0) ok = mbar_wait(&ctl.s_free[1], (s_use[1] - 1) & 1, abort_flag, wait_ns);
-              if (ok) ok = mbar_wait(&ctl.slot_full[sl0], (g / kSlots) & 1, abort_flag, wait_ns);
-              if (ok && pair) ok = mbar_wait(&ctl.slot_full[sl1], ((g + 1) / kSlots) & 1, abort_flag, wait_ns);
+              if (ok) ok = mbar_wait(&ctl.slot_full[sx], uses_of(sx) & 1, abort_flag, wait_ns);
+              if (ok && pair) ok = mbar_wait(&ctl.slot_full[1], uses_of(1) & 1, abort_flag, wait_ns);
               if (!ok) break;
               tc_fence_after();
               // B = a page's tokens (K-major SW128, 8-token groups 9 KB
               // apart); chunk c starts 1 KB further, a K-step of 16 dims 32 B
-              const uint64_t b0 = sdesc_sw128(smem_u32(smem + sl0 * kPageBytes), 16, 9216);
-              const uint64_t b1 = sdesc_sw128(smem_u32(smem + sl1 * kPageBytes), 16, 9216);
-              const uint32_t d = tmem + kTmemS;
-              if (pair && sl1 == sl0 + 1) {
+              const uint32_t lo_slot = pair && sx == 2 ? 1u : sx;
+              const uint64_t b0 = sdesc_sw128(smem_u32(smem + lo_slot * kPageBytes), 16, 9216);
+              const uint32_t d = tmem + (pair && sx == 2 ? kTmemS - 64 : kTmemS);
+              const uint32_t idN = pair ? idS2 : idS;
 #pragma unroll 1
-                for (int c = 0; c < 9; ++c)
+              for (int c = 0; c < 9; ++c)
 #pragma unroll
-                  for (int kk = 0; kk < 4; ++kk)
-                    mma_ts(d, tmem + (uint32_t)(8 * (4 * c + kk)), b0 + (uint64_t)(64 * c + 2 * kk), idS2,
-                           (c | kk) ? 1u : 0u);
-              } else if (pair) {
-#pragma unroll 1
-                for (int c = 0; c < 9; ++c)
-#pragma unroll
-                  for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t at = tmem + (uint32_t)(8 * (4 * c + kk));
-                    const uint32_t acc = (c | kk) ? 1u : 0u;
-                    mma_ts(d, at, b0 + (uint64_t)(64 * c + 2 * kk), idS, acc);
-                    mma_ts(d + 64, at, b1 + (uint64_t)(64 * c + 2 * kk), idS, acc);
-                  }
-              } else {
-#pragma unroll 1
-                for (int c = 0; c < 9; ++c)
-#pragma unroll
-                  for (int kk = 0; kk < 4; ++kk)
-                    mma_ts(d, tmem + (uint32_t)(8 * (4 * c + kk)), b0 + (uint64_t)(64 * c + 2 * kk), idS,
-                           (c | kk) ? 1u : 0u);
-              }
-              mma_commit(&ctl.slot_empty[sl0]);
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_ts(d, tmem + (uint32_t)(8 * (4 * c + kk)), b0 + (uint64_t)(64 * c + 2 * kk), idN,
+                         (c | kk) ? 1u : 0u);
+              mma_commit(&ctl.slot_empty[sx]);
               mma_commit(&ctl.s_full[0]);
               ++s_use[0];
+              slot_uses += 1ull << (21 * sx);
               if (pair) {
-                mma_commit(&ctl.slot_empty[sl1]);
+                mma_commit(&ctl.slot_empty[1]);
                 mma_commit(&ctl.s_full[1]);
                 ++s_use[1];
+                slot_uses += 1ull << 21;
               }
               g += pair ? 2 : 1;
             }
@@ -722,7 +731,11 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
           ++s_seen;
           tc_fence_after();
           float x[64];
-          tmem_ld64(tmem + lane_off + kTmemS + 64 * grp, x);
+          // the first page of unit u at kTmemS; the second 64 columns above,
+          // or below when the pair sits in slots (1, 2)
+          const uint32_t u = g_unit + (uint32_t)(k >> 1);
+          const uint32_t scol = grp == 0 ? kTmemS : (page_slot(u, 0) == 2u ? kTmemS - 64 : kTmemS + 64);
+          tmem_ld64(tmem + lane_off + scol, x);
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
@@ -809,6 +822,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
         }
         if (!ok) { fail(&ctl, a.err); break; }
         g_page += n;
+        g_unit += (uint32_t)(n + 1) / 2;
         ++it_cnt;
       }
     } else if (rank == 0 && warp == 10) {
@@ -1047,13 +1061,11 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_page
   if (warp == 0 && lane == 0) {
     // the last copies issued into each ring slot have landed
     if (rank == 0) {
-      // pages are loaded in order; a skipped load (test hook) leaves a gap
-      for (uint32_t k = 0; k < (uint32_t)kSlots && k < g_issue; ++k) {
-        const uint32_t g = g_issue - 1 - k;
-        if (a.skip_load > 0 && w == 0 && g + 1 == (uint32_t)a.skip_load) continue;
-        if (!mbar_wait(&ctl.slot_full[g % kSlots], (g / kSlots) & 1, &ctl.never, wait_ns))
+      // each slot's last page copy (a skipped load, test hook, was not issued)
+      for (uint32_t sl = 0; sl < (uint32_t)kSlots; ++sl)
+        if (((slot_loaded >> sl) & 1u) &&
+            !mbar_wait(&ctl.slot_full[sl], (uses_of(sl) - 1) & 1, &ctl.never, wait_ns))
           atomicOr(a.err, kErrTimeout);
-      }
     } else {
       for (uint32_t k = 0; k < (uint32_t)kVSlots && k < g_issue; ++k) {
         const uint32_t g = g_issue - 1 - k;
